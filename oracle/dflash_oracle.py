@@ -1,0 +1,514 @@
+"""Plain CPU oracle for one DFlash speculative-decoding step.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or
+execute this module: it is used by ``tests/``, by ``__graft_entry__.smoke()``
+and by the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py``.  It
+shares no code with the CUDA library and does not import it.
+
+Everything is float64 NumPy.  The matrix product (``@``) and ``np.exp`` /
+``np.cos`` / ``np.sin`` are the only library primitives; every step of the
+method is written out in the order the pages state it, with no blocking,
+fusion or reordering.
+
+Sources (page titles as printed on the pages):
+
+* [DD]  "DFlash 深度解析：块扩散模型如何让 LLM 推理加速 6 倍——2026 投机解码完全指南"
+        (chenxutan.com) -- §1.1 autoregressive pseudocode, §1.2 speculative
+        decoding, §2.2 architecture (feature_fusion, kv_injection,
+        draft_inference), §3.3 shared embedding / LM head, §5.1 draft
+        generation, §5.2 feature injection, §8.2 linear verification.
+* [LC]  "从 ICML 论文到你的显卡：llama.cpp 吞下 DFlash，本地推理进入 2 倍速时代"
+        (arex-research.com) -- "投机解码的瓶颈从来不是验证，而是 draft" (accept
+        the matching prefix, cut at the first error) and "KV Injection".
+* [RD]  "我在llama.cpp中测试了最新合并的DFlash在Qwen 3.6 27B本地AI上的表现"
+        (bittide.aicompass.dev) -- greedy verification is lossless; 15-token
+        block limit.
+
+Precision.  ``rounding="none"`` keeps every intermediate in float64 (used for
+the fp32 configuration).  ``rounding="bf16"`` rounds to bfloat16 (round to
+nearest even) exactly at the storage points the bf16 configuration defines:
+every matrix-product input that is an activation (normed hidden states,
+attention output, SwiGLU output, captured hidden states, fused feature), the
+query/key/value entries that attention consumes (after RoPE), and nothing
+else; residual stream and logits stay float64.
+
+Parity pins: every function here is pinned by a test under ``tests/`` against
+values the pages print, closed forms, invariants or brute force.  The one
+composition that no page fixes beyond its pseudocode -- the order of the
+drafter's sub-layers (pre-norm attention then SwiGLU) -- is marked
+"parity unpinned" in ``draft_forward``.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# Shapes and weights
+# ---------------------------------------------------------------------------
+
+
+@dataclass
+class Shape:
+    """Dimensions of one decoder (target or drafter)."""
+
+    n_layers: int
+    hidden: int
+    n_q: int
+    n_kv: int
+    head_dim: int
+    ffn: int
+    vocab: int
+    rope_theta: float = 1.0e6
+    eps: float = 1.0e-6
+
+
+@dataclass
+class Layer:
+    """One pre-norm decoder layer, stored as plain ``nn.Linear`` matrices [out, in]."""
+
+    attn_norm: np.ndarray
+    wq: np.ndarray
+    wk: np.ndarray
+    wv: np.ndarray
+    wo: np.ndarray
+    ffn_norm: np.ndarray
+    w_gate: np.ndarray
+    w_up: np.ndarray
+    w_down: np.ndarray
+
+
+@dataclass
+class Target:
+    shape: Shape
+    embed: np.ndarray
+    layers: list
+    final_norm: np.ndarray
+    lm_head: np.ndarray
+    capture: tuple
+
+
+@dataclass
+class Draft:
+    """Block-diffusion drafter.  Its token embedding and LM head are the
+    target's ([DD] §3.3: shared and frozen), so only these are its own."""
+
+    shape: Shape
+    w_fc: np.ndarray          # [H, 5H]  fusion Linear
+    fc_norm: np.ndarray       # [H]      fusion RMSNorm gain
+    layers: list
+    final_norm: np.ndarray
+    mask_id: int
+
+
+def f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Rounding
+# ---------------------------------------------------------------------------
+
+
+def round_bf16(x):
+    """Round float64 values to the nearest bfloat16 (ties to even).
+
+    bfloat16 keeps 8 significant bits and float32's exponent range.  Written
+    from that definition: x = m * 2**e with 0.5 <= |m| < 1, so the quantum is
+    2**(e-8) for normal numbers and 2**-133 below 2**-126 (subnormals)."""
+    x = f64(x)
+    _, e = np.frexp(x)
+    q = np.maximum(e.astype(np.int64) - 8, -133)
+    y = np.ldexp(np.rint(np.ldexp(x, -q)), q)
+    big = np.abs(y) > 3.3895313892515355e38
+    return np.where(big, np.copysign(np.inf, x), y)
+
+
+class Rounder:
+    def __init__(self, mode: str):
+        if mode not in ("none", "bf16"):
+            raise ValueError(mode)
+        self.mode = mode
+
+    def __call__(self, x):
+        return round_bf16(x) if self.mode == "bf16" else f64(x)
+
+
+# ---------------------------------------------------------------------------
+# Building blocks
+# ---------------------------------------------------------------------------
+
+
+def layer_indices(n_layers: int) -> list:
+    """The 5 captured target layers: spread uniformly from layer 2 to the
+    third-from-last layer ([DD] §2.2 feature_fusion: ``[2, mid1, mid2, mid3,
+    len-3]``).  0-based decoder-layer indices, the three middle ones at the
+    evenly spaced points rounded half up."""
+    lo, hi = 2, n_layers - 3
+    out = []
+    for i in range(5):
+        t = lo + (hi - lo) * i / 4.0
+        out.append(int(math.floor(t + 0.5)))
+    return out
+
+
+def rmsnorm(x, gain, eps):
+    """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * gain ([DD] §2.2)."""
+    x = f64(x)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * f64(gain)
+
+
+def linear(x, w):
+    """nn.Linear without bias: y = x W^T, W stored [out, in]."""
+    return f64(x) @ f64(w).T
+
+
+def silu(x):
+    x = f64(x)
+    return x / (1.0 + np.exp(-x))
+
+
+def rope(x, positions, theta):
+    """Rotary position embedding, rotate-half pairing.
+
+    x: [n, heads, d]; positions: [n].  Pair (i, i+d/2) of a head vector is
+    rotated by the angle pos * theta**(-2i/d)."""
+    x = f64(x)
+    n, _, d = x.shape
+    half = d // 2
+    inv = theta ** (-np.arange(half, dtype=np.float64) * 2.0 / d)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * inv[None, :]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    a, b = x[..., :half], x[..., half:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def attention(q, k, v, allowed):
+    """Scaled dot-product attention for one head.
+
+    q [nq, d], k [nk, d], v [nk, d], allowed [nq, nk] boolean.
+    softmax(q k^T / sqrt(d)) v with disallowed keys removed."""
+    q, k, v = f64(q), f64(k), f64(v)
+    s = q @ k.T / math.sqrt(q.shape[-1])
+    s = np.where(allowed, s, -np.inf)
+    s = s - np.max(s, axis=-1, keepdims=True)
+    p = np.exp(s)
+    p = p / np.sum(p, axis=-1, keepdims=True)
+    return p @ v
+
+
+def argmax_top2(logits):
+    """Greedy token (lowest index among equal maxima) and the gap between the
+    two largest logits, per row."""
+    logits = f64(logits)
+    idx = np.argmax(logits, axis=-1)
+    top2 = np.sort(logits, axis=-1)[..., -2:]
+    return idx.astype(np.int64), top2[..., 1] - top2[..., 0]
+
+
+# ---------------------------------------------------------------------------
+# KV cache (plain per-layer arrays)
+# ---------------------------------------------------------------------------
+
+
+@dataclass
+class KV:
+    """Keys/values per layer: lists of [n_kv, P, d] float64 arrays."""
+
+    k: list = field(default_factory=list)
+    v: list = field(default_factory=list)
+
+    @staticmethod
+    def empty(n_layers, n_kv, d):
+        return KV([np.zeros((n_kv, 0, d)) for _ in range(n_layers)],
+                  [np.zeros((n_kv, 0, d)) for _ in range(n_layers)])
+
+    def length(self):
+        return self.k[0].shape[1] if self.k else 0
+
+    def append(self, layer, k_rows, v_rows):
+        """k_rows/v_rows: [n, n_kv, d] at the next positions."""
+        self.k[layer] = np.concatenate([self.k[layer], np.transpose(k_rows, (1, 0, 2))], axis=1)
+        self.v[layer] = np.concatenate([self.v[layer], np.transpose(v_rows, (1, 0, 2))], axis=1)
+
+    def truncate(self, length):
+        for i in range(len(self.k)):
+            self.k[i] = self.k[i][:, :length]
+            self.v[i] = self.v[i][:, :length]
+
+    def copy(self):
+        return KV([a.copy() for a in self.k], [a.copy() for a in self.v])
+
+
+# ---------------------------------------------------------------------------
+# One decoder layer
+# ---------------------------------------------------------------------------
+
+
+def decoder_layer(x, lw: Layer, shape: Shape, ctx_k, ctx_v, pos0, causal, rnd):
+    """Pre-norm decoder layer on the rows x [n, H] at positions pos0..pos0+n-1.
+
+    Keys/values attended: the context ctx_k/ctx_v [n_kv, P, d] (positions
+    0..P-1) followed by the rows' own keys/values.  ``causal``: row j sees the
+    context and rows 0..j (target verification, [DD] §1.2).  Otherwise every
+    row sees the context and every row (the drafter's in-block bidirectional
+    attention, [DD] §2.2 "块内双向注意力").
+
+    Returns the new residual rows and the rows' (rounded) keys/values
+    [n, n_kv, d] that a cache would append."""
+    n = x.shape[0]
+    d, nq, nkv = shape.head_dim, shape.n_q, shape.n_kv
+    pos = pos0 + np.arange(n)
+    h = rnd(rmsnorm(x, lw.attn_norm, shape.eps))
+    q = rope(linear(h, lw.wq).reshape(n, nq, d), pos, shape.rope_theta)
+    k = rope(linear(h, lw.wk).reshape(n, nkv, d), pos, shape.rope_theta)
+    v = linear(h, lw.wv).reshape(n, nkv, d)
+    q, k, v = rnd(q), rnd(k), rnd(v)
+    P = ctx_k.shape[1]
+    allowed = np.ones((n, P + n), dtype=bool)
+    if causal:
+        allowed[:, P:] = np.tril(np.ones((n, n), dtype=bool))
+    group = nq // nkv
+    o = np.zeros((n, nq, d))
+    for hq in range(nq):
+        hk = hq // group
+        keys = np.concatenate([ctx_k[hk], k[:, hk]], axis=0)
+        vals = np.concatenate([ctx_v[hk], v[:, hk]], axis=0)
+        o[:, hq] = attention(q[:, hq], keys, vals, allowed)
+    o = rnd(o.reshape(n, nq * d))
+    x = f64(x) + linear(o, lw.wo)
+    h2 = rnd(rmsnorm(x, lw.ffn_norm, shape.eps))
+    a = rnd(silu(linear(h2, lw.w_gate)) * linear(h2, lw.w_up))
+    x = x + linear(a, lw.w_down)
+    return x, k, v
+
+
+# ---------------------------------------------------------------------------
+# Target forward (prefill / verification / autoregressive step)
+# ---------------------------------------------------------------------------
+
+
+@dataclass
+class TargetOut:
+    argmax: np.ndarray        # [n]
+    gap: np.ndarray           # [n] top-2 logit gap
+    logits: np.ndarray        # [n, V]
+    hcap: np.ndarray          # [n, 5H] captured hidden states (rounded)
+    new_k: list               # per layer [n, n_kv, d]
+    new_v: list
+
+
+def target_forward(tg: Target, tokens, cache: KV, rnd, keep_logits=True):
+    """Causal target forward of ``tokens`` at positions P..P+n-1 where P is the
+    cache length.  The cache is NOT modified; the caller appends new_k/new_v
+    for the rows it commits.  Captures the residual stream after each layer
+    of ``tg.capture`` ([DD] §2.2 feature_fusion: hidden states of 5 layers)."""
+    sh = tg.shape
+    tokens = np.asarray(tokens, dtype=np.int64)
+    P = cache.length()
+    x = f64(tg.embed)[tokens]
+    caps = {}
+    new_k, new_v = [], []
+    for li, lw in enumerate(tg.layers):
+        x, k, v = decoder_layer(x, lw, sh, cache.k[li], cache.v[li], P, True, rnd)
+        new_k.append(k)
+        new_v.append(v)
+        if li in tg.capture:
+            caps[li] = rnd(x)
+    hcap = np.concatenate([caps[i] for i in tg.capture], axis=-1)
+    z = rnd(rmsnorm(x, tg.final_norm, sh.eps))
+    logits = linear(z, tg.lm_head)
+    am, gap = argmax_top2(logits)
+    return TargetOut(am, gap, logits if keep_logits else None, hcap, new_k, new_v)
+
+
+def commit(cache: KV, out: TargetOut, rows: int):
+    """Append the first ``rows`` rows of a forward's keys/values to the cache."""
+    for li in range(len(cache.k)):
+        cache.append(li, out.new_k[li][:rows], out.new_v[li][:rows])
+
+
+# ---------------------------------------------------------------------------
+# DFlash stages
+# ---------------------------------------------------------------------------
+
+
+def fuse_features(dr: Draft, hcap, rnd):
+    """Feature fusion ([DD] §2.2 feature_fusion): the 5 captured hidden states
+    are concatenated (already, in hcap [m, 5H]) -> Linear -> RMSNorm."""
+    return rnd(rmsnorm(linear(hcap, dr.w_fc), dr.fc_norm, dr.shape.eps))
+
+
+def inject_kv(dr: Draft, fused, positions, rnd):
+    """KV injection ([DD] §2.2 kv_injection, §5.2; [LC] "KV Injection"): every
+    drafter layer projects the fused context feature with its own K and V
+    projections; the keys carry RoPE at the context position.  Returns per
+    layer ([m, n_kv, d] keys, values) to append to that layer's cache."""
+    sh = dr.shape
+    m = fused.shape[0]
+    out = []
+    for lw in dr.layers:
+        k = rope(linear(fused, lw.wk).reshape(m, sh.n_kv, sh.head_dim), positions, sh.rope_theta)
+        v = linear(fused, lw.wv).reshape(m, sh.n_kv, sh.head_dim)
+        out.append((rnd(k), rnd(v)))
+    return out
+
+
+def draft_forward(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rnd):
+    """One non-causal drafter forward over the block [anchor, MASK x (B-1)] at
+    positions P..P+B-1 (P = drafter cache length): [DD] §5.1 "given [T1] +
+    target_model_context -> single forward pass -> [T2,...]", §2.2
+    draft_inference.  Tokens are embedded with the target's embedding and
+    decoded with the target's LM head ([DD] §3.3).
+
+    parity unpinned: the sub-layer order of the drafter (pre-norm attention,
+    then pre-norm SwiGLU, then a final RMSNorm) is not printed on any page.
+
+    Returns the B drafted tokens, slot 0 holding the anchor itself."""
+    sh = dr.shape
+    P = dcache.length()
+    toks = np.array([anchor] + [dr.mask_id] * (block - 1), dtype=np.int64)
+    x = f64(tg.embed)[toks]
+    for li, lw in enumerate(dr.layers):
+        x, _, _ = decoder_layer(x, lw, sh, dcache.k[li], dcache.v[li], P, False, rnd)
+    z = rnd(rmsnorm(x, dr.final_norm, sh.eps))
+    logits = linear(z[1:], tg.lm_head)
+    am, gap = argmax_top2(logits)
+    return np.concatenate([[anchor], am]).astype(np.int64), gap
+
+
+def accept_length(draft_tokens, target_argmax):
+    """Longest accepted prefix ([DD] §1.2, §8.2 linear verification; [LC]:
+    keep the matching prefix, cut at the first error).  Slot i >= 1 of the
+    block is accepted when it equals the target's greedy choice after slot
+    i-1; the count stops at the first mismatch.  Returns a in [0, B-1]; the
+    step emits target_argmax[0..a] (a drafted tokens plus one target token)."""
+    B = len(draft_tokens)
+    a = 0
+    while a < B - 1 and int(draft_tokens[a + 1]) == int(target_argmax[a]):
+        a += 1
+    return a
+
+
+def teacher_force(draft_tokens, ref, emitted, k, r, vocab):
+    """Overwrite drafted slots so that exactly min(k, B-1) are accepted.
+
+    Slots 1..min(k, B-1) take the reference greedy tokens ref[emitted + j - 1];
+    when k + 1 <= B - 1, slot k+1 takes (ref[emitted + k] + 1 + r) mod V with
+    r in [0, V-2], which differs from the reference token.  k and r are drawn
+    by the caller."""
+    d = np.array(draft_tokens, dtype=np.int64).copy()
+    B = len(d)
+    kk = min(int(k), B - 1)
+    for j in range(1, kk + 1):
+        d[j] = ref[emitted + j - 1]
+    if kk + 1 <= B - 1:
+        d[kk + 1] = (int(ref[emitted + kk]) + 1 + int(r)) % vocab
+    return d
+
+
+# ---------------------------------------------------------------------------
+# Whole decodes
+# ---------------------------------------------------------------------------
+
+
+def greedy_ar(tg: Target, prompt, n_tokens, rnd):
+    """Plain greedy autoregressive decoding ([DD] §1.1): forward, take the
+    argmax of the last row, append, repeat.  Returns tokens and top-2 gaps."""
+    sh = tg.shape
+    cache = KV.empty(sh.n_layers, sh.n_kv, sh.head_dim)
+    out = target_forward(tg, prompt, cache, rnd, keep_logits=False)
+    commit(cache, out, len(prompt))
+    toks, gaps = [int(out.argmax[-1])], [float(out.gap[-1])]
+    while len(toks) < n_tokens:
+        out = target_forward(tg, [toks[-1]], cache, rnd, keep_logits=False)
+        commit(cache, out, 1)
+        toks.append(int(out.argmax[0]))
+        gaps.append(float(out.gap[0]))
+    return np.array(toks, dtype=np.int64), np.array(gaps)
+
+
+def greedy_ar_recompute(tg: Target, prompt, n_tokens, rnd):
+    """Greedy decoding with no cache at all: every token re-runs the whole
+    sequence from position 0 (the literal form of [DD] §1.1)."""
+    sh = tg.shape
+    seq = list(int(t) for t in prompt)
+    toks = []
+    while len(toks) < n_tokens:
+        out = target_forward(tg, seq, KV.empty(sh.n_layers, sh.n_kv, sh.head_dim), rnd,
+                             keep_logits=False)
+        toks.append(int(out.argmax[-1]))
+        seq.append(toks[-1])
+    return np.array(toks, dtype=np.int64)
+
+
+@dataclass
+class StepRecord:
+    P: int                    # committed target length at step start
+    anchor: int
+    draft: np.ndarray         # B tokens, slot 0 = anchor
+    argmax: np.ndarray        # B target greedy tokens
+    gap: np.ndarray           # B target top-2 gaps
+    accept: int               # a
+    emitted: np.ndarray       # a + 1 tokens
+
+
+def spec_decode(tg: Target, dr: Draft, prompt, n_tokens, block, rnd, forcing=None, ref=None,
+                max_steps=None):
+    """DFlash speculative decoding, greedy ([DD] §1.2, §2.2, §5.1; [LC]).
+
+    prefill : target forward over the prompt, cache its keys/values, capture
+              its hidden states, emit the greedy token (the first anchor).
+    per step: fuse the pending captured rows, inject them into every drafter
+              layer's cache, draft one block, verify it with one causal target
+              forward, accept the matching prefix plus one target token, and
+              roll back: keep only the accepted rows' target keys/values and
+              leave those rows' captured states pending for the next step.
+
+    forcing: optional (k[steps], r[steps]) teacher-forcing draws; ``ref`` is
+    the reference greedy stream they index (length >= n_tokens + block)."""
+    sh, dsh = tg.shape, dr.shape
+    tcache = KV.empty(sh.n_layers, sh.n_kv, sh.head_dim)
+    dcache = KV.empty(dsh.n_layers, dsh.n_kv, dsh.head_dim)
+    prompt = np.asarray(prompt, dtype=np.int64)
+    out = target_forward(tg, prompt, tcache, rnd, keep_logits=False)
+    commit(tcache, out, len(prompt))
+    pending = out.hcap
+    emitted = [int(out.argmax[-1])]
+    anchor = emitted[0]
+    steps = []
+    while len(emitted) < n_tokens:
+        if max_steps is not None and len(steps) >= max_steps:
+            break
+        P = tcache.length()
+        # fuse + inject the pending rows (positions P - m .. P - 1)
+        m = pending.shape[0]
+        fused = fuse_features(dr, pending, rnd)
+        for li, (k, v) in enumerate(inject_kv(dr, fused, np.arange(P - m, P), rnd)):
+            dcache.append(li, k, v)
+        # draft
+        d, _ = draft_forward(dr, tg, anchor, block, dcache, rnd)
+        if forcing is not None:
+            ks, rs = forcing
+            s = len(steps)
+            d = teacher_force(d, ref, len(emitted), ks[s], rs[s], sh.vocab)
+        # verify
+        out = target_forward(tg, d, tcache, rnd, keep_logits=False)
+        a = accept_length(d, out.argmax)
+        em = out.argmax[: a + 1].copy()
+        steps.append(StepRecord(P, anchor, d, out.argmax.copy(), out.gap.copy(), a, em))
+        emitted.extend(int(t) for t in em)
+        # rollback: keep rows 0..a
+        commit(tcache, out, a + 1)
+        pending = out.hcap[: a + 1]
+        anchor = int(em[-1])
+    return np.array(emitted[:n_tokens], dtype=np.int64), steps
+
+
+def tau(n_emitted_tokens, n_steps):
+    """Mean tokens emitted per verification step."""
+    return n_emitted_tokens / n_steps

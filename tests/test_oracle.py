@@ -1,0 +1,418 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself:
+values the pages print, closed forms, invariants, library routines on special
+cases, and brute force on tiny inputs.  No GPU."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import dflash_oracle as O
+from conftest import oracle_models, shrink
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+NONE = O.Rounder("none")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- rounding
+
+
+def test_round_bf16_ties_and_library():
+    one = 1.0
+    ulp = 2.0 ** -7
+    assert O.round_bf16(one) == one
+    assert O.round_bf16(one + ulp / 2) == one                     # tie -> even (down)
+    assert O.round_bf16(one + 3 * ulp / 2) == one + 2 * ulp       # tie -> even (up)
+    assert O.round_bf16(one + ulp / 2 + 2.0 ** -30) == one + ulp  # just above the tie
+    assert O.round_bf16(-(one + 3 * ulp / 2)) == -(one + 2 * ulp)
+    assert O.round_bf16(0.0) == 0.0
+    assert np.isinf(O.round_bf16(3.5e38))
+    # float32-representable values: the library conversion must agree
+    torch = pytest.importorskip("torch")
+    x = np.random.default_rng(0).standard_normal(20000).astype(np.float32) * 3.0
+    x = np.concatenate([x, np.float32([1e-39, -3e-40, 6e37, 2.0 ** -130])])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.round_bf16(x.astype(np.float64)), ref)
+
+
+# ---------------------------------------------------------------- layer selection
+
+
+def test_layer_indices_golden():
+    g = golden("pages_figures.json")["layer_selection"]
+    assert O.layer_indices(g["n_layers"]) == g["layers"]
+
+
+@pytest.mark.parametrize("L", [8, 12, 13, 36, 48, 64, 80])
+def test_layer_indices_closed_form(L):
+    s = O.layer_indices(L)
+    assert len(s) == 5 and s[0] == 2 and s[-1] == L - 3
+    assert all(a <= b for a, b in zip(s, s[1:]))
+    # evenly spaced points between 2 and L-3, each within half a layer
+    pts = np.linspace(2, L - 3, 5)
+    assert np.all(np.abs(np.array(s) - pts) <= 0.5)
+
+
+def test_layer_indices_named_targets():
+    assert O.layer_indices(36) == [2, 10, 18, 25, 33]
+    assert O.layer_indices(64) == [2, 17, 32, 46, 61]
+
+
+# ---------------------------------------------------------------- building blocks
+
+
+def test_rmsnorm_closed_forms():
+    H = 64
+    for c in (3.0, -0.25, 1e3):
+        y = O.rmsnorm(np.full((1, H), c), np.ones(H), 0.0)
+        assert np.allclose(y, np.sign(c))
+    x = np.random.default_rng(1).standard_normal((5, H))
+    y = O.rmsnorm(x, np.ones(H), 0.0)
+    assert np.allclose(np.mean(y * y, axis=-1), 1.0)
+    assert np.allclose(O.rmsnorm(7.5 * x, np.ones(H), 0.0), y)             # scale invariance
+    g = np.arange(H, dtype=np.float64)
+    assert np.allclose(O.rmsnorm(x, g, 0.0), y * g)                       # gain multiplies
+    assert np.all(O.rmsnorm(np.zeros((1, H)), np.ones(H), 1e-6) == 0.0)   # eps keeps 0 finite
+    # eps enters under the root: x = 1-vector, eps = 3 -> 1/sqrt(1 + 3) = 0.5
+    assert np.allclose(O.rmsnorm(np.ones((1, 4)), np.ones(4), 3.0), 0.5)
+
+
+def test_linear_hand_values():
+    x = np.array([[1.0, 2.0, 3.0]])
+    w = np.array([[1.0, 0.0, -1.0], [2.0, 1.0, 0.5]])    # [out=2, in=3]
+    assert np.array_equal(O.linear(x, w), [[1 - 3, 2 + 2 + 1.5]])
+
+
+def test_silu_values():
+    assert O.silu(0.0) == 0.0
+    assert math.isclose(O.silu(1.0), 1.0 / (1.0 + math.exp(-1.0)), rel_tol=1e-15)
+    x = np.linspace(-20, 20, 101)
+    assert np.allclose(O.silu(x) - O.silu(-x), x)          # x*s(x) + x*s(-x) = x
+    assert abs(O.silu(40.0) - 40.0) < 1e-12 and abs(O.silu(-40.0)) < 1e-12
+
+
+def test_rope_closed_form_d4():
+    theta = 100.0
+    x = np.zeros((1, 1, 4))
+    x[0, 0, 0] = 1.0
+    p = 3.0
+    y = O.rope(x, [p], theta)
+    # rotate-half: dims (0, 2) rotate by p * theta^0, dims (1, 3) by p * theta^(-1/2)
+    assert np.allclose(y[0, 0], [math.cos(p), 0.0, math.sin(p), 0.0])
+    x = np.zeros((1, 1, 4))
+    x[0, 0, 3] = 1.0
+    y = O.rope(x, [p], theta)
+    a = p * theta ** -0.5
+    assert np.allclose(y[0, 0], [0.0, -math.sin(a), 0.0, math.cos(a)])
+
+
+def test_rope_invariants():
+    rng = np.random.default_rng(2)
+    d = 64
+    q = rng.standard_normal((1, 3, d))
+    k = rng.standard_normal((1, 3, d))
+    assert np.allclose(O.rope(q, [0], 1e6), q)                                   # position 0
+    for p in (1, 17, 4099, 98304):
+        y = O.rope(q, [p], 1e6)
+        assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(q, axis=-1))
+        # composition: rotating by a then by b equals rotating by a + b
+        assert np.allclose(O.rope(O.rope(q, [p], 1e6), [5], 1e6), O.rope(q, [p + 5], 1e6))
+    # relative position: <rope(q, m), rope(k, n)> depends on m - n only
+    for m, n, s in ((5, 2, 100), (0, 7, 4096), (36000, 35990, -35000)):
+        a = np.sum(O.rope(q, [m], 1e6) * O.rope(k, [n], 1e6), axis=-1)
+        b = np.sum(O.rope(q, [m + s], 1e6) * O.rope(k, [n + s], 1e6), axis=-1)
+        assert np.allclose(a, b)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(3)
+    d = 16
+    q = rng.standard_normal((4, d))
+    k = rng.standard_normal((6, d))
+    v = rng.standard_normal((6, d))
+    all_ = np.ones((4, 6), bool)
+    one = np.zeros((4, 6), bool)
+    one[:, 2] = True
+    assert np.allclose(O.attention(q, k, v, one), np.broadcast_to(v[2], (4, d)))   # single key
+    kk = np.broadcast_to(k[0], (6, d))
+    assert np.allclose(O.attention(q, kk, v, all_), np.broadcast_to(v.mean(0), (4, d)))  # equal keys
+    assert np.allclose(O.attention(np.zeros((4, d)), k, v, all_), np.broadcast_to(v.mean(0), (4, d)))
+    # adding the same vector to every key shifts a row's scores by a constant
+    u = rng.standard_normal(d)
+    assert np.allclose(O.attention(q, k + u, v, all_), O.attention(q, k, v, all_))
+    # a dominant key takes all the weight
+    kd = k.copy()
+    kd[4] = q[0] * 1e3
+    assert np.allclose(O.attention(q[:1], kd, v, all_[:1]), v[4])
+    # masked keys have no influence
+    tri = np.tril(np.ones((4, 6), bool), 2)
+    k2 = k.copy()
+    k2[5] += 100.0
+    v2 = v.copy()
+    v2[5] -= 50.0
+    assert np.allclose(O.attention(q[:3], k2, v2, tri[:3]), O.attention(q[:3], k, v, tri[:3]))
+    # explicit two-key softmax
+    q1 = np.array([[1.0, 0.0]])
+    k1 = np.array([[2.0, 0.0], [0.0, 0.0]])
+    v1 = np.array([[1.0, 0.0], [0.0, 1.0]])
+    w0 = 1.0 / (1.0 + math.exp(-2.0 / math.sqrt(2.0)))
+    assert np.allclose(O.attention(q1, k1, v1, np.ones((1, 2), bool)), [[w0, 1.0 - w0]])
+
+
+def test_argmax_ties_and_gap():
+    am, gap = O.argmax_top2(np.array([[1.0, 3.0, 3.0, 2.0], [0.5, -1.0, 0.25, 0.0]]))
+    assert list(am) == [1, 0]
+    assert gap[0] == 0.0 and gap[1] == 0.25
+
+
+# ---------------------------------------------------------------- accept / teacher forcing
+
+
+def test_accept_golden_linear_verification():
+    g = golden("linear_verify_example.json")
+    a = O.accept_length(g["draft"], g["target_argmax"])
+    assert a == g["accept"]
+    assert list(g["target_argmax"][: a + 1]) == g["emitted"]
+
+
+def _accept_brute(draft, target):
+    """Independent definition: the length of the longest k such that the
+    drafted continuation draft[1..k] equals the target continuation
+    target[0..k-1]."""
+    B = len(draft)
+    best = 0
+    for k in range(B):
+        if tuple(draft[1:k + 1]) == tuple(target[:k]):
+            best = k
+    return best
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 4, 5])
+def test_accept_brute_force_all_inputs(B):
+    V = 3
+    for draft in itertools.product(range(V), repeat=B):
+        for tgt in itertools.product(range(V), repeat=B):
+            assert O.accept_length(draft, tgt) == _accept_brute(draft, tgt)
+
+
+def test_teacher_force_gives_exact_accept():
+    rng = np.random.default_rng(4)
+    V = 11
+    for B in (2, 5, 15, 16):
+        for _ in range(200):
+            ref = rng.integers(0, V, size=64)
+            e = int(rng.integers(1, 30))
+            d = rng.integers(0, V, size=B)
+            d[0] = ref[e - 1]
+            k = int(rng.geometric(1 / 8) - 1)
+            r = int(rng.integers(0, V - 1))
+            d2 = O.teacher_force(d, ref, e, k, r, V)
+            assert O.accept_length(d2, ref[e:e + B]) == min(k, B - 1)
+
+
+def test_tau_and_speedup_arithmetic():
+    g = golden("pages_figures.json")
+    t = g["tau"]
+    assert round(O.tau(t["tokens"], t["steps"]), 2) == t["tau"]
+    assert round(100 * O.tau(t["tokens"], t["steps"]) / t["block"], 1) == t["acceptance_pct"]
+    assert round(t["tokens"] / t["seconds"], 1) == round(t["tok_per_s"], 1)
+    for base, new, ratio in g["speedups"]["pairs"]:
+        assert round(new / base, 2) == ratio
+
+
+# ---------------------------------------------------------------- composed forward
+
+
+def _tiny_models(tiny, **kw):
+    wl, w = tiny
+    if kw:
+        wl = shrink(wl, **kw)
+        w = synth.host_weights(wl.target, wl.draft_layers, wl.dtype)
+    return (wl,) + oracle_models(wl, w)
+
+
+def test_cache_equals_recompute(tiny):
+    wl, tg, _ = _tiny_models(tiny)
+    prompt = synth.prompt_tokens(24, wl.target.vocab)
+    a, _ = O.greedy_ar(tg, prompt, 6, NONE)
+    b = O.greedy_ar_recompute(tg, prompt, 6, NONE)
+    assert np.array_equal(a, b)
+
+
+def test_block_forward_equals_row_by_row(tiny):
+    """A causal forward of n rows at once equals n one-row forwards with the
+    cache growing between them (rows see exactly their prefix)."""
+    wl, tg, _ = _tiny_models(tiny)
+    toks = synth.prompt_tokens(20, wl.target.vocab)
+    sh = tg.shape
+    c1 = O.KV.empty(sh.n_layers, sh.n_kv, sh.head_dim)
+    o1 = O.target_forward(tg, toks, c1, NONE)
+    c2 = O.KV.empty(sh.n_layers, sh.n_kv, sh.head_dim)
+    rows = []
+    for t in toks:
+        o = O.target_forward(tg, [t], c2, NONE)
+        O.commit(c2, o, 1)
+        rows.append(o.logits[0])
+    assert np.allclose(o1.logits, np.array(rows), atol=1e-10)
+
+
+def test_capture_order(tiny):
+    """Block s of the captured state is the residual stream after layer S[s]."""
+    wl, tg, _ = _tiny_models(tiny)
+    toks = synth.prompt_tokens(9, wl.target.vocab)
+    sh = tg.shape
+    H = sh.hidden
+    full = O.target_forward(tg, toks, O.KV.empty(sh.n_layers, sh.n_kv, sh.head_dim), NONE)
+    for s, li in enumerate(tg.capture):
+        cut = O.Target(O.Shape(li + 1, *list(vars(sh).values())[1:]), tg.embed, tg.layers[:li + 1],
+                       tg.final_norm, tg.lm_head, (li,) * 5)
+        part = O.target_forward(cut, toks, O.KV.empty(li + 1, sh.n_kv, sh.head_dim), NONE)
+        assert np.array_equal(full.hcap[:, s * H:(s + 1) * H], part.hcap[:, :H])
+
+
+def test_fuse_selects_and_normalises(tiny):
+    wl, tg, dr = _tiny_models(tiny)
+    H = wl.target.hidden
+    rng = np.random.default_rng(5)
+    hcap = rng.standard_normal((3, 5 * H))
+    import dataclasses
+    for s in range(5):
+        sel = np.zeros((H, 5 * H))
+        sel[:, s * H:(s + 1) * H] = np.eye(H)
+        d2 = dataclasses.replace(dr, w_fc=sel)
+        f = O.fuse_features(d2, hcap, NONE)
+        blk = hcap[:, s * H:(s + 1) * H]
+        assert np.allclose(f, blk / np.sqrt(np.mean(blk ** 2, axis=-1, keepdims=True) + 1e-6))
+
+
+def test_draft_is_translation_invariant(tiny):
+    """Context keys carry RoPE at their own positions and block queries at
+    P..P+B-1: shifting every position by the same amount changes nothing."""
+    wl, tg, dr = _tiny_models(tiny)
+    H = wl.target.hidden
+    rng = np.random.default_rng(6)
+    fused = rng.standard_normal((10, H))
+    outs = []
+    for shift in (0, 1000):
+        dc = O.KV.empty(dr.shape.n_layers, dr.shape.n_kv, dr.shape.head_dim)
+        # place the 10 context rows at positions shift .. shift+9 by padding the cache
+        for li, (k, v) in enumerate(O.inject_kv(dr, fused, np.arange(shift, shift + 10), NONE)):
+            dc.k[li] = np.transpose(k, (1, 0, 2))
+            dc.v[li] = np.transpose(v, (1, 0, 2))
+        # draft_forward takes P from the cache length; emulate a cache that starts at `shift`
+        # by calling the layer directly with pos0 = shift + 10.
+        x = np.asarray(tg.embed, dtype=np.float64)[[5] + [dr.mask_id] * 15]
+        for li, lw in enumerate(dr.layers):
+            x, _, _ = O.decoder_layer(x, lw, dr.shape, dc.k[li], dc.v[li], shift + 10, False, NONE)
+        outs.append(x)
+    assert np.allclose(outs[0], outs[1], atol=1e-9)
+
+
+def test_draft_noncausal_block_sees_all_rows(tiny):
+    """Every block row sees every other row: changing the last slot's token
+    changes row 0's output in the drafter, never in the causal target."""
+    wl, tg, dr = _tiny_models(tiny)
+    sh = dr.shape
+    x = np.asarray(tg.embed, dtype=np.float64)[[3, 4, 5]]
+    x2 = np.asarray(tg.embed, dtype=np.float64)[[3, 4, 6]]
+    e = np.zeros((sh.n_kv, 0, sh.head_dim))
+    a, _, _ = O.decoder_layer(x, dr.layers[0], sh, e, e, 0, False, NONE)
+    b, _, _ = O.decoder_layer(x2, dr.layers[0], sh, e, e, 0, False, NONE)
+    assert not np.allclose(a[0], b[0])
+    a, _, _ = O.decoder_layer(x, dr.layers[0], sh, e, e, 0, True, NONE)
+    b, _, _ = O.decoder_layer(x2, dr.layers[0], sh, e, e, 0, True, NONE)
+    assert np.array_equal(a[:2], b[:2])
+
+
+# ---------------------------------------------------------------- losslessness
+
+
+@pytest.mark.parametrize("block", [16, 2, 5])
+def test_lossless_natural_drafting(tiny, block):
+    """Greedy speculative decoding emits exactly the greedy autoregressive
+    stream (the target checks every drafted token)."""
+    wl, tg, dr = _tiny_models(tiny)
+    prompt = synth.prompt_tokens(wl.prompt_len, wl.target.vocab)
+    n = 24
+    ref, _ = O.greedy_ar(tg, prompt, n, NONE)
+    out, steps = O.spec_decode(tg, dr, prompt, n, block, NONE)
+    assert np.array_equal(out, ref)
+    for st in steps:
+        assert st.accept == O.accept_length(st.draft, st.argmax)
+
+
+@pytest.mark.parametrize("block", [16, 15, 8])
+def test_lossless_teacher_forced(tiny, block):
+    wl, tg, dr = _tiny_models(tiny)
+    prompt = synth.prompt_tokens(wl.prompt_len, wl.target.vocab)
+    n = 48
+    ref, _ = O.greedy_ar(tg, prompt, n + block, NONE)
+    k, r = synth.acceptance_draws(64, wl.target.vocab)
+    out, steps = O.spec_decode(tg, dr, prompt, n, block, NONE, forcing=(k[:, 0], r[:, 0]), ref=ref)
+    assert np.array_equal(out, ref[:n])
+    for s, st in enumerate(steps):
+        assert st.accept == min(int(k[s, 0]), block - 1)
+    assert len(steps) < n  # forcing accepted more than one token per step on average
+
+
+def test_lossless_bf16_rounding():
+    wl = shrink(synth.WORKLOADS["small-bf16-gqa4"], n_layers=4, vocab=1024)
+    w = synth.host_weights(wl.target, wl.draft_layers, wl.dtype)
+    tg, dr = oracle_models(wl, w)
+    rnd = O.Rounder("bf16")
+    prompt = synth.prompt_tokens(40, wl.target.vocab)
+    n = 20
+    ref, _ = O.greedy_ar(tg, prompt, n + wl.block, rnd)
+    k, r = synth.acceptance_draws(32, wl.target.vocab)
+    out, steps = O.spec_decode(tg, dr, prompt, n, wl.block, rnd, forcing=(k[:, 0], r[:, 0]), ref=ref)
+    assert np.array_equal(out, ref[:n])
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+
+def test_planted_accept_off_by_one_breaks_losslessness(tiny, monkeypatch):
+    """A plausible slip in acceptance (one token too many) is caught by the
+    losslessness pin."""
+    wl, tg, dr = _tiny_models(tiny)
+    prompt = synth.prompt_tokens(32, wl.target.vocab)
+    ref, _ = O.greedy_ar(tg, prompt, 30, NONE)
+    good = O.accept_length
+    monkeypatch.setattr(O, "accept_length", lambda d, g: min(good(d, g) + 1, len(d) - 1))
+    out, _ = O.spec_decode(tg, dr, prompt, 12, 16, NONE)
+    assert not np.array_equal(out, ref[:12])
+
+
+def test_planted_rollback_slip_breaks_losslessness(tiny, monkeypatch):
+    wl, tg, dr = _tiny_models(tiny)
+    prompt = synth.prompt_tokens(32, wl.target.vocab)
+    ref, _ = O.greedy_ar(tg, prompt, 12, NONE)
+    good = O.commit
+    # keeping one stale row of the rejected tail
+    monkeypatch.setattr(O, "commit", lambda c, o, rows: good(c, o, min(rows + 1, len(o.argmax))))
+    out, _ = O.spec_decode(tg, dr, prompt, 12, 16, NONE)
+    assert not np.array_equal(out, ref)
+
+
+def test_planted_rope_sign_breaks_rotation():
+    q = np.random.default_rng(7).standard_normal((1, 2, 8))
+
+    def bad(x, positions, theta):
+        x = np.asarray(x, dtype=np.float64)
+        half = x.shape[-1] // 2
+        inv = theta ** (-np.arange(half) * 2.0 / x.shape[-1])
+        ang = np.asarray(positions, dtype=np.float64)[:, None] * inv[None, :]
+        c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+        a, b = x[..., :half], x[..., half:]
+        return np.concatenate([a * c + b * s, b * c + a * s], axis=-1)
+
+    y = bad(q, [3], 1e6)
+    assert not np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(q, axis=-1))
