@@ -1,0 +1,549 @@
+// C ABI of the DFlash step library: caches, workspace, and the five stages
+// (fuse, inject, draft, verify, accept/rollback) composed from the kernels.
+// Host code validates arguments and enqueues kernels; it never synchronises
+// except in dflash_status.
+#include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace dfl;
+
+struct dflash_cache {
+  int32_t n_layers, batch, capacity, n_kv, head_dim, dtype;
+  size_t elem;
+  uint8_t* k;
+  uint8_t* v;
+  int32_t* len;
+  float2* rope;
+  size_t layer_stride, seq_stride, head_stride;  // elements
+  bool owns;
+};
+
+struct dflash_workspace {
+  int32_t max_rows, max_ctx;
+  size_t x_elems, xn_elems, f32_elems, q_elems, act_elems, logit_elems;
+  float* x;
+  void* xn;
+  float* f32buf;
+  void* q;
+  void* attn;
+  void* act;
+  float* logits;
+  GemmScratch gs;
+  AttnScratch as;
+  int* status;
+  std::vector<void*> allocs;
+};
+
+static thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+#define CK(expr)                    \
+  do {                              \
+    cudaError_t e_ = (expr);        \
+    if (e_ != cudaSuccess) {        \
+      g_last_cuda = e_;             \
+      return DFLASH_ERR_CUDA;       \
+    }                               \
+  } while (0)
+
+#define REQ(cond)                          \
+  do {                                     \
+    if (!(cond)) return DFLASH_ERR_INVALID_ARG; \
+  } while (0)
+
+static size_t dtype_size(int dt) { return dt == DFLASH_BF16 ? 2 : 4; }
+
+static bool desc_ok(const dflash_model_desc* d) {
+  return d && d->n_layers > 0 && d->hidden > 0 && d->n_q_heads > 0 && d->n_kv_heads > 0 &&
+         d->n_q_heads % d->n_kv_heads == 0 && (d->head_dim == 64 || d->head_dim == 128) && d->ffn > 0 &&
+         d->vocab > 1 && (d->dtype == DFLASH_F32 || d->dtype == DFLASH_BF16) && d->hidden % 4 == 0;
+}
+
+static bool desc_shapes_ok(const dflash_model_desc* d) {
+  if (d->dtype != DFLASH_BF16) return true;
+  const int H = d->hidden, hd = d->head_dim;
+  const int G = d->n_q_heads / d->n_kv_heads;
+  return hd == 128 && (G == 1 || G == 2 || G == 4 || G == 5 || G == 8) &&
+         gemm_shape_ok(DFLASH_BF16, (d->n_q_heads + 2 * d->n_kv_heads) * hd, H) &&
+         gemm_shape_ok(DFLASH_BF16, H, d->n_q_heads * hd) && gemm_shape_ok(DFLASH_BF16, 2 * d->ffn, H) &&
+         gemm_shape_ok(DFLASH_BF16, H, d->ffn) && gemm_shape_ok(DFLASH_BF16, d->vocab, H);
+}
+
+extern "C" {
+
+const char* dflash_strerror(int code) {
+  switch (code) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID_ARG: return "invalid argument";
+    case DFLASH_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case DFLASH_ERR_CUDA: return cudaGetErrorString(g_last_cuda);
+    case DFLASH_ERR_OOM: return "out of device memory";
+    default: return "unknown error";
+  }
+}
+
+int dflash_capture_layers(int32_t n_layers, int32_t out[5]) {
+  REQ(out && n_layers >= 6);
+  const int lo = 2, hi = n_layers - 3;
+  // lo + (hi - lo) * i / 4 rounded half up, in exact integer arithmetic
+  for (int i = 0; i < 5; ++i) out[i] = lo + ((hi - lo) * i * 2 + 4) / 8;
+  return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------ caches
+int dflash_cache_alloc(const dflash_model_desc* d, int32_t n_layers, int32_t batch, int32_t capacity,
+                       dflash_cache** out) {
+  REQ(out && desc_ok(d) && n_layers > 0 && batch > 0 && capacity > 0);
+  *out = nullptr;
+  dflash_cache* c = new dflash_cache();
+  c->n_layers = n_layers;
+  c->batch = batch;
+  c->capacity = capacity;
+  c->n_kv = d->n_kv_heads;
+  c->head_dim = d->head_dim;
+  c->dtype = d->dtype;
+  c->elem = dtype_size(d->dtype);
+  c->head_stride = (size_t)capacity * d->head_dim;
+  c->seq_stride = c->head_stride * d->n_kv_heads;
+  c->layer_stride = c->seq_stride * batch;
+  c->owns = true;
+  const size_t bytes = c->layer_stride * n_layers * c->elem;
+  const int half = d->head_dim / 2;
+  if (cudaMalloc(&c->k, bytes) != cudaSuccess || cudaMalloc(&c->v, bytes) != cudaSuccess ||
+      cudaMalloc(&c->len, sizeof(int32_t) * batch) != cudaSuccess ||
+      cudaMalloc(&c->rope, sizeof(float2) * (size_t)capacity * half) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(c->k);
+    cudaFree(c->v);
+    cudaFree(c->len);
+    cudaFree(c->rope);
+    delete c;
+    return DFLASH_ERR_OOM;
+  }
+  cudaMemset(c->len, 0, sizeof(int32_t) * batch);
+  // RoPE table in double precision: angle = pos * theta^(-2i/d)
+  std::vector<float2> tab((size_t)capacity * half);
+  for (int i = 0; i < half; ++i) {
+    const double inv = pow((double)d->rope_theta, -2.0 * i / (double)d->head_dim);
+    for (int p = 0; p < capacity; ++p) {
+      const double a = (double)p * inv;
+      tab[(size_t)p * half + i] = make_float2((float)cos(a), (float)sin(a));
+    }
+  }
+  if (cudaMemcpy(c->rope, tab.data(), sizeof(float2) * tab.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+    dflash_cache_free(c);
+    return DFLASH_ERR_CUDA;
+  }
+  *out = c;
+  return DFLASH_OK;
+}
+
+int dflash_cache_view(dflash_cache* c, int32_t seq_begin, int32_t seq_count, dflash_cache** out) {
+  REQ(c && out && seq_begin >= 0 && seq_count > 0 && seq_begin + seq_count <= c->batch);
+  dflash_cache* v = new dflash_cache(*c);
+  v->k = c->k + (size_t)seq_begin * c->seq_stride * c->elem;
+  v->v = c->v + (size_t)seq_begin * c->seq_stride * c->elem;
+  v->len = c->len + seq_begin;
+  v->batch = seq_count;
+  v->owns = false;
+  *out = v;
+  return DFLASH_OK;
+}
+
+int dflash_cache_free(dflash_cache* c) {
+  if (!c) return DFLASH_OK;
+  if (c->owns) {
+    cudaFree(c->k);
+    cudaFree(c->v);
+    cudaFree(c->len);
+    cudaFree(c->rope);
+  }
+  delete c;
+  return DFLASH_OK;
+}
+
+int32_t* dflash_cache_lengths(dflash_cache* c) { return c ? c->len : nullptr; }
+
+int dflash_cache_get_lengths(dflash_cache* c, int32_t* host_out, int32_t n, dflash_stream_t stream) {
+  REQ(c && host_out && n > 0);
+  CK(cudaStreamSynchronize((cudaStream_t)stream));
+  CK(cudaMemcpy(host_out, c->len, sizeof(int32_t) * (n < c->batch ? n : c->batch), cudaMemcpyDeviceToHost));
+  return DFLASH_OK;
+}
+
+static int cache_copy(dflash_cache* c, int32_t layer, int32_t seq, int32_t pos0, int32_t n, void* k, void* v,
+                      bool to_cache, cudaStream_t s) {
+  REQ(c && k && v && layer >= 0 && layer < c->n_layers && seq >= 0 && seq < c->batch && pos0 >= 0 && n > 0 &&
+      pos0 + n <= c->capacity);
+  const size_t es = c->elem;
+  const size_t off = ((size_t)layer * c->layer_stride + (size_t)seq * c->seq_stride + (size_t)pos0 * c->head_dim) * es;
+  const size_t pitch_cache = c->head_stride * es, width = (size_t)n * c->head_dim * es;
+  for (int t = 0; t < 2; ++t) {
+    uint8_t* cbase = (t == 0 ? c->k : c->v) + off;
+    void* ubuf = t == 0 ? k : v;
+    if (to_cache)
+      CK(cudaMemcpy2DAsync(cbase, pitch_cache, ubuf, width, width, c->n_kv, cudaMemcpyDeviceToDevice, s));
+    else
+      CK(cudaMemcpy2DAsync(ubuf, width, cbase, pitch_cache, width, c->n_kv, cudaMemcpyDeviceToDevice, s));
+  }
+  return DFLASH_OK;
+}
+
+int dflash_cache_write(dflash_cache* c, int32_t layer, int32_t seq, int32_t pos0, int32_t n, const void* k,
+                       const void* v, dflash_stream_t stream) {
+  return cache_copy(c, layer, seq, pos0, n, const_cast<void*>(k), const_cast<void*>(v), true, (cudaStream_t)stream);
+}
+
+int dflash_cache_read(dflash_cache* c, int32_t layer, int32_t seq, int32_t pos0, int32_t n, void* k, void* v,
+                      dflash_stream_t stream) {
+  return cache_copy(c, layer, seq, pos0, n, k, v, false, (cudaStream_t)stream);
+}
+
+int dflash_cache_set_lengths(dflash_cache* c, const int32_t* host_len, int32_t n, dflash_stream_t stream) {
+  REQ(c && host_len && n > 0 && n <= c->batch);
+  for (int i = 0; i < n; ++i) REQ(host_len[i] >= 0 && host_len[i] <= c->capacity);
+  CK(cudaMemcpyAsync(c->len, host_len, sizeof(int32_t) * n, cudaMemcpyHostToDevice, (cudaStream_t)stream));
+  CK(cudaStreamSynchronize((cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+int dflash_cache_reset(dflash_cache* c, dflash_stream_t stream) {
+  REQ(c);
+  CK(cudaMemsetAsync(c->len, 0, sizeof(int32_t) * c->batch, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------ workspace
+int dflash_workspace_alloc(const dflash_model_desc* t, const dflash_model_desc* d, int32_t max_rows, int32_t max_ctx,
+                           dflash_workspace** out) {
+  REQ(out && desc_ok(t) && (!d || desc_ok(d)) && max_rows > 0 && max_rows <= kMaxRows && max_ctx > 0);
+  if (d) REQ(d->dtype == t->dtype);
+  *out = nullptr;
+  dflash_workspace* w = new dflash_workspace();
+  w->max_rows = max_rows;
+  w->max_ctx = max_ctx;
+  const size_t es = dtype_size(t->dtype);
+  const dflash_model_desc* ds[2] = {t, d ? d : t};
+  size_t H = 0, f32w = 0, qw = 0, F = 0, V = 0, nq = 0;
+  for (const dflash_model_desc* m : ds) {
+    const size_t hd = m->head_dim;
+    H = std::max(H, (size_t)m->hidden);
+    f32w = std::max(f32w, (size_t)(m->n_q_heads + 2 * m->n_kv_heads) * hd);
+    f32w = std::max(f32w, (size_t)m->hidden);
+    qw = std::max(qw, (size_t)m->n_q_heads * hd);
+    F = std::max(F, (size_t)m->ffn);
+    V = std::max(V, (size_t)m->vocab);
+    nq = std::max(nq, (size_t)m->n_q_heads);
+  }
+  if (d) f32w = std::max(f32w, (size_t)d->n_layers * 2 * d->n_kv_heads * d->head_dim);
+  const size_t R = max_rows;
+  const int nchunk = (max_ctx + kAttnChunk - 1) / kAttnChunk;
+  const size_t part = (size_t)2 * num_sms() * 128 * R;
+  struct Req {
+    void** p;
+    size_t bytes;
+  } reqs[] = {
+      {(void**)&w->x, R * H * 4},
+      {(void**)&w->xn, R * H * es},
+      {(void**)&w->f32buf, R * f32w * 4},
+      {(void**)&w->q, R * qw * es},
+      {(void**)&w->attn, R * qw * es},
+      {(void**)&w->act, R * F * es},
+      {(void**)&w->logits, R * V * 4},
+      {(void**)&w->gs.part, part * 4},
+      {(void**)&w->gs.tickets, 4096 * 4},
+      {(void**)&w->as.o, R * nq * nchunk * 128 * 4},
+      {(void**)&w->as.ml, R * nq * nchunk * 2 * 4},
+      {(void**)&w->status, 4},
+  };
+  for (auto& r : reqs) {
+    void* p = nullptr;
+    if (cudaMalloc(&p, r.bytes) != cudaSuccess) {
+      cudaGetLastError();
+      dflash_workspace_free(w);
+      return DFLASH_ERR_OOM;
+    }
+    *r.p = p;
+    w->allocs.push_back(p);
+  }
+  w->gs.part_elems = part;
+  w->gs.n_tickets = 4096;
+  w->as.nchunk = nchunk;
+  cudaMemset(w->gs.tickets, 0, 4096 * 4);
+  cudaMemset(w->status, 0, 4);
+  cudaMemset(w->x, 0, R * H * 4);
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    dflash_workspace_free(w);
+    return DFLASH_ERR_CUDA;
+  }
+  *out = w;
+  return DFLASH_OK;
+}
+
+int dflash_workspace_free(dflash_workspace* w) {
+  if (!w) return DFLASH_OK;
+  for (void* p : w->allocs) cudaFree(p);
+  delete w;
+  return DFLASH_OK;
+}
+
+int dflash_status(dflash_workspace* w, dflash_stream_t stream, int32_t* status_out) {
+  REQ(w && status_out);
+  int32_t v = 0;
+  CK(cudaStreamSynchronize((cudaStream_t)stream));
+  CK(cudaMemcpy(&v, w->status, 4, cudaMemcpyDeviceToHost));
+  CK(cudaMemset(w->status, 0, 4));
+  *status_out = v;
+  return DFLASH_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ kernel timing
+// While enabled (measurement passes only), every weight GEMM launch is
+// bracketed by a pair of CUDA events on its stream.
+namespace {
+struct Profile {
+  bool on = false;
+  int max = 0, n = 0;
+  std::vector<cudaEvent_t> ev;
+  std::vector<int32_t> tags;  // M, K, rows per record
+} g_prof;
+}  // namespace
+
+static cudaError_t pgemm(int dtype, const void* X, int ldx, int rows, const void* W, int M, int K, const Epi& epi,
+                         const GemmScratch& scr, int* status, cudaStream_t s) {
+  const bool rec = g_prof.on && g_prof.n < g_prof.max;
+  if (rec) {
+    cudaError_t e = cudaEventRecord(g_prof.ev[2 * g_prof.n], s);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = gemm(dtype, X, ldx, rows, W, M, K, epi, scr, status, s);
+  if (e != cudaSuccess) return e;
+  if (rec) {
+    e = cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], s);
+    if (e != cudaSuccess) return e;
+    g_prof.tags[3 * g_prof.n] = M;
+    g_prof.tags[3 * g_prof.n + 1] = K;
+    g_prof.tags[3 * g_prof.n + 2] = rows;
+    ++g_prof.n;
+  }
+  return cudaSuccess;
+}
+
+extern "C" long long dflash_launch_count(void) { return launch_count(); }
+
+extern "C" int dflash_profile_begin(int32_t max_records) {
+  REQ(max_records > 0 && max_records <= (1 << 20) && !g_prof.on);
+  if ((int)g_prof.ev.size() < 2 * max_records) {
+    const size_t old = g_prof.ev.size();
+    g_prof.ev.resize(2 * max_records);
+    for (size_t i = old; i < g_prof.ev.size(); ++i) CK(cudaEventCreate(&g_prof.ev[i]));
+  }
+  g_prof.tags.assign(3 * (size_t)max_records, 0);
+  g_prof.max = max_records;
+  g_prof.n = 0;
+  g_prof.on = true;
+  return DFLASH_OK;
+}
+
+extern "C" int dflash_profile_end(float* ms_out, int32_t* tags_out, int32_t max, int32_t* n_out) {
+  REQ(g_prof.on && n_out);
+  g_prof.on = false;
+  const int n = g_prof.n < max ? g_prof.n : max;
+  if (n > 0) CK(cudaEventSynchronize(g_prof.ev[2 * (n - 1) + 1]));
+  for (int i = 0; i < n; ++i) {
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]));
+    if (ms_out) ms_out[i] = ms;
+    if (tags_out)
+      for (int j = 0; j < 3; ++j) tags_out[3 * i + j] = g_prof.tags[3 * i + j];
+  }
+  *n_out = n;
+  return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------ composed forward
+static int layer_forward(const dflash_model_desc& d, const dflash_layer_w& w, dflash_cache* c, int layer, int batch,
+                         int n, int causal, dflash_workspace* ws, cudaStream_t s) {
+  const int rows = batch * n, H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads;
+  const int qkvw = (nq + 2 * nkv) * hd, dt = d.dtype;
+  REQ(w.attn_norm && w.wqkv && w.wo && w.ffn_norm && w.w_gate_up && w.w_down);
+  uint8_t* kc = c->k + (size_t)layer * c->layer_stride * c->elem;
+  uint8_t* vc = c->v + (size_t)layer * c->layer_stride * c->elem;
+  CK(rmsnorm(dt, ws->x, w.attn_norm, ws->xn, rows, H, d.rms_eps, s));
+  CK(pgemm(dt, ws->xn, H, rows, w.wqkv, qkvw, H, Epi{EPI_F32, ws->f32buf, qkvw}, ws->gs, ws->status, s));
+  CK(rope_qkv(dt, ws->f32buf, batch, n, nq, nkv, hd, ws->q, kc, vc, c->seq_stride, c->head_stride, c->capacity,
+              c->len, c->rope, ws->status, s));
+  CK(attention(dt, ws->q, batch, n, nq, nkv, hd, causal, kc, vc, c->seq_stride, c->head_stride, c->capacity, c->len,
+               ws->as, ws->attn, ws->status, s));
+  CK(pgemm(dt, ws->attn, nq * hd, rows, w.wo, H, nq * hd, Epi{EPI_RESID, ws->x, H}, ws->gs, ws->status, s));
+  CK(rmsnorm(dt, ws->x, w.ffn_norm, ws->xn, rows, H, d.rms_eps, s));
+  CK(pgemm(dt, ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, Epi{EPI_SWIGLU, ws->act, d.ffn}, ws->gs, ws->status, s));
+  CK(pgemm(dt, ws->act, d.ffn, rows, w.w_down, H, d.ffn, Epi{EPI_RESID, ws->x, H}, ws->gs, ws->status, s));
+  return DFLASH_OK;
+}
+
+static bool cache_matches(const dflash_cache* c, const dflash_model_desc& d, int n_layers) {
+  return c && c->n_kv == d.n_kv_heads && c->head_dim == d.head_dim && c->dtype == d.dtype &&
+         c->n_layers >= n_layers;
+}
+
+extern "C" {
+
+int target_verify(const dflash_target* tg, const int32_t* tokens, int32_t batch, int32_t n, int32_t commit,
+                  dflash_cache* tc, int32_t* argmax_out, float* top2_gap, void* hcap, int32_t* anchor,
+                  int32_t* n_pend, int32_t* stream, int32_t* stream_len, int32_t stream_cap, dflash_workspace* ws,
+                  dflash_stream_t cuda_stream) {
+  REQ(tg && tokens && argmax_out && ws && desc_ok(&tg->d) && tg->layers && tg->embed && tg->lm_head &&
+      tg->final_norm);
+  const dflash_model_desc& d = tg->d;
+  if (!desc_shapes_ok(&d)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
+  REQ(batch > 0 && n > 0 && n <= kMaxRows && batch * n <= ws->max_rows && commit >= 0 && commit <= 2);
+  REQ(cache_matches(tc, d, d.n_layers) && batch <= tc->batch && tc->capacity <= ws->max_ctx);
+  if (commit == 2) REQ(anchor);
+  for (int i = 0; i < 5; ++i) REQ(tg->capture[i] >= 0 && tg->capture[i] < d.n_layers);
+  cudaStream_t s = (cudaStream_t)cuda_stream;
+  const int rows = batch * n, H = d.hidden;
+  CK(embed(d.dtype, tg->embed, d.vocab, H, tokens, nullptr, 0, batch, n, 0, nullptr, ws->x, ws->status, s));
+  for (int l = 0; l < d.n_layers; ++l) {
+    int rc = layer_forward(d, tg->layers[l], tc, l, batch, n, 1, ws, s);
+    if (rc != DFLASH_OK) return rc;
+    if (hcap)
+      for (int si = 0; si < 5; ++si)
+        if (tg->capture[si] == l) CK(capture(d.dtype, ws->x, hcap, rows, H, si, s));
+  }
+  CK(rmsnorm(d.dtype, ws->x, tg->final_norm, ws->xn, rows, H, d.rms_eps, s));
+  CK(pgemm(d.dtype, ws->xn, H, rows, tg->lm_head, d.vocab, H, Epi{EPI_F32, ws->logits, d.vocab}, ws->gs, ws->status,
+          s));
+  CK(argmax(ws->logits, rows, d.vocab, argmax_out, top2_gap, 0, ws->status, s));
+  if (commit)
+    CK(commit_rows(tc->len, n_pend, anchor, argmax_out, batch, n, commit == 2, stream, stream_len, stream_cap,
+                   ws->status, s));
+  return DFLASH_OK;
+}
+
+int dflash_fuse_features(const dflash_draft* dr, const void* hcap, int32_t rows, void* fused, dflash_workspace* ws,
+                         dflash_stream_t stream) {
+  REQ(dr && hcap && fused && ws && desc_ok(&dr->d) && dr->w_fc && dr->fc_norm);
+  REQ(rows > 0 && rows <= ws->max_rows);
+  const dflash_model_desc& d = dr->d;
+  const int H = d.hidden;
+  if (!gemm_shape_ok(d.dtype, H, 5 * H)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(pgemm(d.dtype, hcap, 5 * H, rows, dr->w_fc, H, 5 * H, Epi{EPI_F32, ws->f32buf, H}, ws->gs, ws->status, s));
+  CK(rmsnorm(d.dtype, ws->f32buf, dr->fc_norm, fused, rows, H, d.rms_eps, s));
+  return DFLASH_OK;
+}
+
+int dflash_inject_kv(const dflash_draft* dr, const void* fused, int32_t batch, int32_t rows_per_seq,
+                     int32_t* n_pend, dflash_cache* dc, dflash_workspace* ws, dflash_stream_t stream) {
+  REQ(dr && fused && n_pend && ws && desc_ok(&dr->d) && dr->w_kv_all);
+  const dflash_model_desc& d = dr->d;
+  REQ(cache_matches(dc, d, d.n_layers) && batch > 0 && batch <= dc->batch && rows_per_seq > 0 &&
+      batch * rows_per_seq <= ws->max_rows);
+  const int H = d.hidden, W = d.n_layers * 2 * d.n_kv_heads * d.head_dim;
+  if (!gemm_shape_ok(d.dtype, W, H)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int rows = batch * rows_per_seq;
+  CK(pgemm(d.dtype, fused, H, rows, dr->w_kv_all, W, H, Epi{EPI_F32, ws->f32buf, W}, ws->gs, ws->status, s));
+  CK(inject_write(d.dtype, ws->f32buf, batch, rows_per_seq, d.n_layers, d.n_kv_heads, d.head_dim, dc->k, dc->v,
+                  dc->layer_stride, dc->seq_stride, dc->head_stride, dc->capacity, dc->len, n_pend, dc->rope,
+                  ws->status, s));
+  CK(advance_len(dc->len, n_pend, batch, s));
+  return DFLASH_OK;
+}
+
+int dflash_draft_block(const dflash_draft* dr, const dflash_target* tg, const int32_t* anchor, int32_t batch,
+                       int32_t block, dflash_cache* dc, int32_t* draft_tokens, dflash_workspace* ws,
+                       dflash_stream_t stream) {
+  REQ(dr && tg && anchor && draft_tokens && ws && desc_ok(&dr->d) && dr->layers && dr->final_norm && tg->embed &&
+      tg->lm_head);
+  const dflash_model_desc& d = dr->d;
+  if (!desc_shapes_ok(&d)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
+  REQ(d.hidden == tg->d.hidden && d.vocab == tg->d.vocab && d.dtype == tg->d.dtype);
+  REQ(block >= 2 && block <= 16 && batch > 0 && batch * block <= ws->max_rows);
+  REQ(cache_matches(dc, d, d.n_layers) && batch <= dc->batch && dc->capacity <= ws->max_ctx);
+  REQ(dr->mask_id >= 0 && dr->mask_id < d.vocab);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int rows = batch * block, H = d.hidden;
+  CK(embed(d.dtype, tg->embed, d.vocab, H, nullptr, anchor, dr->mask_id, batch, block, 1, draft_tokens, ws->x,
+           ws->status, s));
+  for (int l = 0; l < d.n_layers; ++l) {
+    int rc = layer_forward(d, dr->layers[l], dc, l, batch, block, 0, ws, s);
+    if (rc != DFLASH_OK) return rc;
+  }
+  CK(rmsnorm(d.dtype, ws->x, dr->final_norm, ws->xn, rows, H, d.rms_eps, s));
+  CK(pgemm(d.dtype, ws->xn, H, rows, tg->lm_head, d.vocab, H, Epi{EPI_F32, ws->logits, d.vocab}, ws->gs, ws->status,
+          s));
+  CK(argmax(ws->logits, rows, d.vocab, draft_tokens, nullptr, block, ws->status, s));
+  return DFLASH_OK;
+}
+
+int dflash_accept_rollback(const int32_t* draft_tokens, const int32_t* argmax_in, int32_t batch, int32_t block,
+                           dflash_cache* tc, int32_t* anchor, int32_t* n_pend, int32_t* accept_len, int32_t* stream,
+                           int32_t* stream_len, int32_t stream_cap, dflash_workspace* ws, dflash_stream_t cuda_stream) {
+  REQ(draft_tokens && argmax_in && tc && anchor && n_pend && ws);
+  REQ(batch > 0 && batch <= tc->batch && block >= 2 && block <= 32);
+  REQ(!stream || (stream_len && stream_cap > 0));
+  CK(accept_rollback(draft_tokens, argmax_in, batch, block, tc->len, anchor, n_pend, accept_len, stream, stream_len,
+                     stream_cap, ws->status, (cudaStream_t)cuda_stream));
+  return DFLASH_OK;
+}
+
+int dflash_teacher_force(int32_t* draft_tokens, int32_t batch, int32_t block, const int32_t* ref, int32_t ref_stride,
+                         int32_t ref_len, const int32_t* stream_len, const int32_t* k_draw, const int32_t* r_draw,
+                         int32_t max_steps, int32_t* step, int32_t vocab, dflash_workspace* ws,
+                         dflash_stream_t stream) {
+  REQ(draft_tokens && ref && stream_len && k_draw && r_draw && step && ws);
+  REQ(batch > 0 && batch <= 1024 && block >= 2 && ref_stride >= ref_len && ref_len > 0 && max_steps > 0 &&
+      vocab > 1);
+  CK(teacher_force(draft_tokens, batch, block, ref, ref_stride, ref_len, stream_len, k_draw, r_draw, max_steps, step,
+                   vocab, ws->status, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------ building blocks
+int dflash_linear(int32_t dtype, const void* x, const void* w, float* y, int32_t rows, int32_t M, int32_t K,
+                  dflash_workspace* ws, dflash_stream_t stream) {
+  REQ(x && w && y && ws && rows > 0 && rows <= kMaxRows && M > 0 && K > 0);
+  REQ(dtype == DFLASH_F32 || dtype == DFLASH_BF16);
+  if (!gemm_shape_ok(dtype, M, K)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
+  CK(pgemm(dtype, x, K, rows, w, M, K, Epi{EPI_F32, y, M}, ws->gs, ws->status, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+int dflash_rmsnorm(int32_t dtype, const float* x, const void* gain, void* y, int32_t rows, int32_t H, float eps,
+                   dflash_stream_t stream) {
+  REQ(x && gain && y && rows > 0 && H > 0 && H % 4 == 0);
+  REQ(dtype == DFLASH_F32 || dtype == DFLASH_BF16);
+  CK(rmsnorm(dtype, x, gain, y, rows, H, eps, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+int dflash_argmax(const float* logits, int32_t rows, int32_t V, int32_t* argmax_out, float* gap, dflash_workspace* ws,
+                  dflash_stream_t stream) {
+  REQ(logits && argmax_out && ws && rows > 0 && V > 0);
+  CK(argmax(logits, rows, V, argmax_out, gap, 0, ws->status, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+int dflash_attention(const dflash_model_desc* d, const void* q, int32_t batch, int32_t n, int32_t causal,
+                     dflash_cache* c, int32_t layer, void* out, dflash_workspace* ws, dflash_stream_t stream) {
+  REQ(desc_ok(d) && q && out && ws && batch > 0 && n > 0 && batch * n <= ws->max_rows);
+  REQ(cache_matches(c, *d, layer + 1) && layer >= 0 && batch <= c->batch && c->capacity <= ws->max_ctx);
+  if (!desc_shapes_ok(d)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
+  const uint8_t* kc = c->k + (size_t)layer * c->layer_stride * c->elem;
+  const uint8_t* vc = c->v + (size_t)layer * c->layer_stride * c->elem;
+  CK(attention(d->dtype, q, batch, n, d->n_q_heads, d->n_kv_heads, d->head_dim, causal ? 1 : 0, kc, vc,
+               c->seq_stride, c->head_stride, c->capacity, c->len, ws->as, out, ws->status, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+}  // extern "C"

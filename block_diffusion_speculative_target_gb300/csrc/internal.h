@@ -1,0 +1,94 @@
+// Internal launcher interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dflash.h"
+
+namespace dfl {
+
+// GEMM epilogues: y[n][m] = sum_k x[n][k] w[m][k], then
+enum EpiKind {
+  EPI_F32 = 0,     // out f32 [n][ldo]            = y
+  EPI_STORE = 1,   // out T   [n][ldo]            = T(y)
+  EPI_RESID = 2,   // out f32 [n][ldo]           += y   (residual stream)
+  EPI_SWIGLU = 3,  // out T   [n][ldo], col m/2   = T(silu(y[m]) * y[m+1]) for even m (gate/up interleaved)
+};
+
+struct Epi {
+  int kind;
+  void* out;
+  int ldo;
+};
+
+// Split-K scratch for the tensor-core GEMM.
+struct GemmScratch {
+  float* part;       // partial sums
+  size_t part_elems; // capacity in floats
+  int* tickets;      // per-tile arrival counters (kept at 0 between launches)
+  int n_tickets;
+};
+
+// Maximum rows (tokens) one GEMM call handles.
+constexpr int kMaxRows = 128;
+// Fixed attention chunk length (positions); chunk boundaries sit at multiples of it.
+constexpr int kAttnChunk = 256;
+
+int num_sms();
+// Host-side count of kernel launches enqueued by the library (for measurement).
+void count_launch(int n = 1);
+long long launch_count();
+
+cudaError_t gemm(int dtype, const void* X, int ldx, int rows, const void* W, int M, int K, const Epi& epi,
+                 const GemmScratch& scr, int* status, cudaStream_t s);
+// Number of K splits the bf16 GEMM uses for an [M x K] weight (depends on M, K and the GPU only).
+int gemm_splits(int M, int K);
+bool gemm_shape_ok(int dtype, int M, int K);
+
+// Row-wise RMSNorm: y = T(x * 1/sqrt(mean(x^2)+eps) * g).
+cudaError_t rmsnorm(int dtype, const float* x, const void* g, void* y, int rows, int H, float eps,
+                    cudaStream_t s);
+// Copy T(x) into column block `slot` of hcap [rows][5H].
+cudaError_t capture(int dtype, const float* x, void* hcap, int rows, int H, int slot, cudaStream_t s);
+// x[r] = float(E[token(r)]).  mode 0: token = tokens[r]; mode 1 (draft block):
+// token = anchor[b] for slot 0 else mask_id, and draft_out[b][0] = anchor[b].
+cudaError_t embed(int dtype, const void* E, int V, int H, const int32_t* tokens, const int32_t* anchor,
+                  int mask_id, int batch, int n, int mode, int32_t* draft_out, float* x, int* status,
+                  cudaStream_t s);
+// RoPE on the q and k parts of qkv (f32 [rows][(nq+2nkv)hd]); q -> qout (T), k/v -> cache at len[b]+j.
+cudaError_t rope_qkv(int dtype, const float* qkv, int batch, int n, int nq, int nkv, int hd, void* qout,
+                     void* kc, void* vc, size_t seq_stride, size_t head_stride, int capacity,
+                     const int32_t* len, const float2* rope_tab, int* status, cudaStream_t s);
+// Inject: kv f32 [batch*rps][Ld][2][nkv][hd] -> drafter caches (layer stride given) at len[b]+j, j < n_pend[b].
+cudaError_t inject_write(int dtype, const float* kv, int batch, int rps, int Ld, int nkv, int hd, void* kc,
+                         void* vc, size_t layer_stride, size_t seq_stride, size_t head_stride, int capacity,
+                         const int32_t* len, const int32_t* n_pend, const float2* rope_tab, int* status,
+                         cudaStream_t s);
+cudaError_t advance_len(int32_t* len, int32_t* n_pend, int batch, cudaStream_t s);
+
+// Attention partials over fixed chunks + combine.
+struct AttnScratch {
+  float* o;    // [rows][nq][nchunk][hd]
+  float* ml;   // [rows][nq][nchunk][2]
+  int nchunk;  // chunk capacity per row
+};
+cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nkv, int hd, int causal,
+                      const void* kc, const void* vc, size_t seq_stride, size_t head_stride, int capacity,
+                      const int32_t* len, const AttnScratch& sc, void* out, int* status, cudaStream_t s);
+
+// Greedy token and top-2 gap per row.  If skip_first_of (>0), rows with
+// (r % skip_first_of) == 0 are not written to argmax_out.
+cudaError_t argmax(const float* logits, int rows, int V, int32_t* argmax_out, float* gap, int skip_first_of,
+                   int* status, cudaStream_t s);
+
+cudaError_t commit_rows(int32_t* len, int32_t* n_pend, int32_t* anchor, const int32_t* argmax, int batch, int n,
+                        int emit, int32_t* stream, int32_t* stream_len, int stream_cap, int* status,
+                        cudaStream_t s);
+cudaError_t accept_rollback(const int32_t* draft, const int32_t* argmax, int batch, int block, int32_t* len,
+                            int32_t* anchor, int32_t* n_pend, int32_t* accept_len, int32_t* stream,
+                            int32_t* stream_len, int stream_cap, int* status, cudaStream_t s);
+cudaError_t teacher_force(int32_t* draft, int batch, int block, const int32_t* ref, int ref_stride, int ref_len,
+                          const int32_t* stream_len, const int32_t* k_draw, const int32_t* r_draw, int max_steps,
+                          int32_t* step, int vocab, int* status, cudaStream_t s);
+
+}  // namespace dfl

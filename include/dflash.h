@@ -1,0 +1,280 @@
+/*
+ * dflash.h -- C ABI of a GB300 (sm_103a) library for one DFlash
+ * speculative-decoding step: fuse -> inject -> draft -> verify -> accept ->
+ * rollback.  Every stage runs as CUDA kernels of this library on the stream
+ * the caller passes; the host only validates arguments and enqueues work.
+ *
+ * Sources (page titles as printed on the pages):
+ *   [DD] "DFlash 深度解析：块扩散模型如何让 LLM 推理加速 6 倍——2026 投机解码完全指南"
+ *        (chenxutan.com): §1.1 autoregressive decoding, §1.2 speculative
+ *        decoding, §2.2 feature_fusion / kv_injection / draft_inference,
+ *        §3.3 shared embedding and LM head, §5.1 one-forward block drafting,
+ *        §8.2 linear verification.
+ *   [LC] "从 ICML 论文到你的显卡：llama.cpp 吞下 DFlash，本地推理进入 2 倍速时代"
+ *        (arex-research.com): KV injection into every drafter layer; keep the
+ *        matching prefix, cut at the first error.
+ *   [RD] "我在llama.cpp中测试了最新合并的DFlash在Qwen 3.6 27B本地AI上的表现"
+ *        (bittide.aicompass.dev): greedy verification is lossless.
+ *
+ * Conventions
+ *   - All pointers to tensors are DEVICE pointers owned by the caller unless
+ *     stated otherwise; the library never frees them.  Row-major throughout.
+ *   - Matrices are nn.Linear [out_features][in_features].
+ *   - Element type of weights, KV caches, hidden states and captured states
+ *     is the model's dtype (DFLASH_F32 or DFLASH_BF16); residual stream,
+ *     logits and all reductions are float32.
+ *   - Positions and lengths live on the device (per-sequence int32), so every
+ *     call can be captured into a CUDA graph and replayed step after step.
+ *   - Return values: DFLASH_OK (0) or a negative DFLASH_ERR_* code from the
+ *     synchronous argument checks or from a failed CUDA launch.  Conditions
+ *     detected inside kernels (capacity overflow, non-finite logits, a wait
+ *     that ran out) set bits in the workspace's device status word, read with
+ *     dflash_status(); kernels never trap.
+ *   - Calls are asynchronous on `stream` and not thread-safe on one cache or
+ *     workspace.
+ */
+#ifndef DFLASH_H_
+#define DFLASH_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dflash_stream_t; /* = cudaStream_t */
+
+enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = -1,
+  DFLASH_ERR_UNSUPPORTED_SHAPE = -2,
+  DFLASH_ERR_CUDA = -3,
+  DFLASH_ERR_OOM = -4,
+};
+
+/* device status bits (dflash_status) */
+enum {
+  DFLASH_STATUS_CAPACITY = 1,  /* a write beyond a cache's capacity was skipped */
+  DFLASH_STATUS_NONFINITE = 2, /* a logit row held NaN/Inf */
+  DFLASH_STATUS_TIMEOUT = 4,   /* a pipeline wait gave up (kernel returned early) */
+  DFLASH_STATUS_BOUNDS = 8,    /* an index (token id, reference position) was out of range */
+};
+
+enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 };
+
+/* Dimensions of one decoder (target or drafter). head_dim: 64 or 128. */
+typedef struct dflash_model_desc {
+  int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+  float rope_theta, rms_eps;
+  int32_t dtype; /* DFLASH_F32 | DFLASH_BF16 */
+} dflash_model_desc;
+
+/* One pre-norm decoder layer.
+ *   wqkv      [(nq + 2 nkv) * hd][H]  rows: q heads, then k heads, then v heads
+ *   wo        [H][nq * hd]
+ *   w_gate_up [2F][H]  row 2f is gate row f, row 2f+1 is up row f
+ *   w_down    [H][F]
+ *   attn_norm, ffn_norm [H] RMSNorm gains */
+typedef struct dflash_layer_w {
+  const void *attn_norm, *wqkv, *wo, *ffn_norm, *w_gate_up, *w_down;
+} dflash_layer_w;
+
+/* Target model.  capture[5]: 0-based layers whose output residual stream is
+ * captured for feature fusion ([DD] §2.2: 5 layers from 2 to the
+ * third-from-last, see dflash_capture_layers). */
+typedef struct dflash_target {
+  dflash_model_desc d;
+  const void *embed;      /* [V][H] */
+  const void *final_norm; /* [H] */
+  const void *lm_head;    /* [V][H] */
+  const dflash_layer_w *layers; /* HOST array of d.n_layers entries */
+  int32_t capture[5];
+} dflash_target;
+
+/* Block-diffusion drafter.  It reuses the target's embedding and LM head
+ * ([DD] §3.3).  w_kv_all packs, for every drafter layer l in order, that
+ * layer's k rows then v rows of wqkv: [Ld * 2 * nkv * hd][H]; it holds the
+ * same values as the layers' wqkv and lets one product project the fused
+ * feature for all layers ([DD] §5.2 dflash_feature_injection). */
+typedef struct dflash_draft {
+  dflash_model_desc d;
+  const void *w_fc;       /* [H][5H] fusion Linear ([DD] §2.2 feature_fusion) */
+  const void *fc_norm;    /* [H] fusion RMSNorm gain */
+  const void *final_norm; /* [H] */
+  const dflash_layer_w *layers; /* HOST array of d.n_layers entries */
+  const void *w_kv_all;
+  int32_t mask_id;
+} dflash_draft;
+
+/* ------------------------------------------------------------------ caches
+ * A KV cache holds, for `batch` sequences and `n_layers` layers, keys and
+ * values [layer][seq][kv_head][capacity][head_dim] in the model dtype, a
+ * device int32 length per sequence (starts at 0), and a float32 RoPE
+ * cos/sin table for positions 0..capacity-1 (computed on the host in double
+ * precision).  Library-owned device memory (cudaMalloc); free with
+ * dflash_cache_free.  The target cache's length is the committed length P;
+ * the drafter cache's length is the number of injected context rows.
+ * Positions >= length are scratch: target_verify writes the block there and
+ * dflash_draft_block writes its block's keys/values there. */
+typedef struct dflash_cache dflash_cache;
+
+int dflash_cache_alloc(const dflash_model_desc *d, int32_t n_layers, int32_t batch,
+                       int32_t capacity, dflash_cache **out);
+int dflash_cache_free(dflash_cache *c);
+/* A view of sequences [seq_begin, seq_begin + seq_count) sharing memory with
+ * `c` (used to prefill a ragged batch one sequence at a time).  Free views
+ * with dflash_cache_free before freeing their parent. */
+int dflash_cache_view(dflash_cache *c, int32_t seq_begin, int32_t seq_count, dflash_cache **out);
+/* Device pointer to the int32 lengths [batch] (for the caller to read). */
+int32_t *dflash_cache_lengths(dflash_cache *c);
+/* Synchronises `stream` and copies min(n, batch) lengths to host memory. */
+int dflash_cache_get_lengths(dflash_cache *c, int32_t *host_out, int32_t n, dflash_stream_t stream);
+/* Copy keys and values of positions [pos0, pos0 + n) of one layer and one
+ * sequence from (write) or to (read) caller device buffers k, v laid out
+ * [n_kv][n][head_dim] in the cache dtype.  Asynchronous device-to-device
+ * copies; lengths are not changed.  Used to load a saved context. */
+int dflash_cache_write(dflash_cache *c, int32_t layer, int32_t seq, int32_t pos0, int32_t n,
+                       const void *k, const void *v, dflash_stream_t stream);
+int dflash_cache_read(dflash_cache *c, int32_t layer, int32_t seq, int32_t pos0, int32_t n, void *k,
+                      void *v, dflash_stream_t stream);
+/* Set the first n lengths from host memory (asynchronous). */
+int dflash_cache_set_lengths(dflash_cache *c, const int32_t *host_len, int32_t n,
+                             dflash_stream_t stream);
+/* Set every length to 0 (asynchronous). */
+int dflash_cache_reset(dflash_cache *c, dflash_stream_t stream);
+
+/* --------------------------------------------------------------- workspace
+ * Library-owned scratch for activations, split-K partial sums, attention
+ * partials and the device status word.  Sized for both models, for up to
+ * `max_rows` rows per call (batch x rows-per-sequence, <= 128) and contexts
+ * up to `max_ctx` positions.  One workspace serves one stream at a time. */
+typedef struct dflash_workspace dflash_workspace;
+
+int dflash_workspace_alloc(const dflash_model_desc *target, const dflash_model_desc *draft,
+                           int32_t max_rows, int32_t max_ctx, dflash_workspace **out);
+int dflash_workspace_free(dflash_workspace *w);
+/* Synchronises `stream`, returns the status bits in *status_out and clears them. */
+int dflash_status(dflash_workspace *w, dflash_stream_t stream, int32_t *status_out);
+const char *dflash_strerror(int code);
+
+/* Captured layers for a target of n_layers: 5 layers spread uniformly from
+ * layer 2 to layer n_layers-3 ([DD] §2.2 feature_fusion), rounded half up. */
+int dflash_capture_layers(int32_t n_layers, int32_t out[5]);
+
+/* ------------------------------------------------------------------ stages
+ * Sequence state shared by the stages (device int32 arrays, caller-owned):
+ *   anchor[batch]  last emitted token; it sits at position P
+ *   n_pend[batch]  captured rows not yet injected into the drafter cache;
+ *                  they belong to positions P - n_pend .. P - 1
+ * Invariant outside a stage: drafter length + n_pend == target length == P.
+ * A step is: fuse + inject the pending rows, draft, verify, accept/rollback. */
+
+/* Feature fusion ([DD] §2.2 feature_fusion): fused = RMSNorm(hcap · w_fcᵀ)
+ * ⊙ fc_norm for `rows` rows.  hcap [rows][5H] holds the captured hidden
+ * states of the 5 layers side by side (the concat); fused [rows][H]. */
+int dflash_fuse_features(const dflash_draft *dr, const void *hcap, int32_t rows, void *fused,
+                         dflash_workspace *ws, dflash_stream_t stream);
+
+/* KV injection ([DD] §2.2 kv_injection, §5.2; [LC]): for every drafter layer
+ * l, K = RoPE(fused · W_k,lᵀ) and V = fused · W_v,lᵀ are appended to layer
+ * l's cache.  fused is [batch][rows_per_seq][H]; sequence b injects its first
+ * n_pend[b] rows at positions len[b] .. len[b] + n_pend[b] - 1 of
+ * draft_cache, then len[b] += n_pend[b] and n_pend[b] = 0 (the rows are
+ * consumed). */
+int dflash_inject_kv(const dflash_draft *dr, const void *fused, int32_t batch, int32_t rows_per_seq,
+                     int32_t *n_pend, dflash_cache *draft_cache, dflash_workspace *ws,
+                     dflash_stream_t stream);
+
+/* Block drafting ([DD] §5.1, §2.2 draft_inference): one non-causal forward of
+ * the block [anchor, MASK x (block-1)] at positions P .. P+block-1 (P = the
+ * drafter cache length) through every drafter layer; each row attends to the
+ * injected context 0..P-1 and to all block rows.  Tokens are embedded and
+ * decoded with the target's embedding and LM head ([DD] §3.3).  Writes
+ * draft_tokens[b][0] = anchor[b] and draft_tokens[b][j] = argmax of row j
+ * (j >= 1).  block in [2, 16]. */
+int dflash_draft_block(const dflash_draft *dr, const dflash_target *tg, const int32_t *anchor,
+                       int32_t batch, int32_t block, dflash_cache *draft_cache,
+                       int32_t *draft_tokens, dflash_workspace *ws, dflash_stream_t stream);
+
+/* Target forward ([DD] §1.1, §1.2): tokens [batch][n] at positions
+ * P .. P+n-1 (P = target cache length), causal, keys/values written into the
+ * cache at those positions.  Outputs per row: argmax [batch][n] (lowest index
+ * on ties), top2_gap [batch][n] (nullable; largest minus second-largest
+ * logit) and hcap [batch][n][5H] (nullable), the residual stream after each
+ * captured layer.  n in [1, 128], batch * n <= workspace max_rows.
+ *   commit = 0  verification: lengths untouched (dflash_accept_rollback decides)
+ *   commit = 1  prefill chunk: len += n, n_pend = n
+ *   commit = 2  as 1, and the last row's greedy token becomes the anchor and
+ *               is appended to the stream (last chunk of a prefill, or one
+ *               autoregressive step) -- anchor/n_pend/stream may be NULL for
+ *               commit = 0. */
+int target_verify(const dflash_target *tg, const int32_t *tokens, int32_t batch, int32_t n,
+                  int32_t commit, dflash_cache *target_cache, int32_t *argmax, float *top2_gap,
+                  void *hcap, int32_t *anchor, int32_t *n_pend, int32_t *stream,
+                  int32_t *stream_len, int32_t stream_cap, dflash_workspace *ws,
+                  dflash_stream_t cuda_stream);
+
+/* Acceptance and rollback ([DD] §1.2, §8.2; [LC]).  For each sequence b:
+ *   a = the number of leading drafted tokens draft_tokens[b][i] (i >= 1) that
+ *       equal the target's greedy choice argmax[b][i-1], stopping at the
+ *       first mismatch (0 <= a <= block-1);
+ *   emitted: argmax[b][0..a] (a drafted tokens + the target's own next token)
+ *       are appended to stream[b][*] at stream_len[b] (capacity stream_cap);
+ *   rollback: target len[b] = P + a + 1 (rows beyond are discarded in place,
+ *       no data moves), anchor[b] = argmax[b][a], n_pend[b] = a + 1.
+ * accept_len[batch] receives a (nullable). */
+int dflash_accept_rollback(const int32_t *draft_tokens, const int32_t *argmax, int32_t batch,
+                           int32_t block, dflash_cache *target_cache, int32_t *anchor,
+                           int32_t *n_pend, int32_t *accept_len, int32_t *stream,
+                           int32_t *stream_len, int32_t stream_cap, dflash_workspace *ws,
+                           dflash_stream_t cuda_stream);
+
+/* Teacher forcing (benchmark harness for random-init models, whose natural
+ * acceptance is ~0).  For sequence b at step s = *step (device counter,
+ * incremented by this call): k = k_draw[s][b], r = r_draw[s][b],
+ * e = stream_len[b]; slots j = 1..min(k, block-1) take ref[b][e+j-1]; if
+ * k+1 <= block-1, slot k+1 takes (ref[b][e+k] + 1 + r) mod vocab, which
+ * differs from the reference; other slots keep the drafter's tokens.  With
+ * ref the greedy stream, exactly min(k, block-1) drafts are then accepted. */
+int dflash_teacher_force(int32_t *draft_tokens, int32_t batch, int32_t block, const int32_t *ref,
+                         int32_t ref_stride, int32_t ref_len, const int32_t *stream_len,
+                         const int32_t *k_draw, const int32_t *r_draw, int32_t max_steps,
+                         int32_t *step, int32_t vocab, dflash_workspace *ws, dflash_stream_t stream);
+
+/* -------------------------------------------------------- building blocks
+ * The kernels behind the stages, exposed for unit parity tests. */
+
+/* y[n][m] = sum_k x[n][k] w[m][k]; x [rows][K] (dtype), w [M][K] (dtype),
+ * y [rows][M] float32.  rows <= 128. */
+int dflash_linear(int32_t dtype, const void *x, const void *w, float *y, int32_t rows, int32_t M,
+                  int32_t K, dflash_workspace *ws, dflash_stream_t stream);
+/* y = x / sqrt(mean(x^2) + eps) * gain, x float32 [rows][H] -> y dtype. */
+int dflash_rmsnorm(int32_t dtype, const float *x, const void *gain, void *y, int32_t rows,
+                   int32_t H, float eps, dflash_stream_t stream);
+/* Greedy token and top-2 gap of float32 logits [rows][V]. */
+int dflash_argmax(const float *logits, int32_t rows, int32_t V, int32_t *argmax, float *gap,
+                  dflash_workspace *ws, dflash_stream_t stream);
+/* Attention of q [batch][n][nq][hd] (dtype, RoPE applied) against layer
+ * `layer` of `cache` (positions 0 .. len[b] + n - 1, the block's own keys
+ * already written at len[b] ..), causal (row j sees 0..len+j) or not (every
+ * row sees 0..len+n-1).  out [batch][n][nq * hd] dtype. */
+int dflash_attention(const dflash_model_desc *d, const void *q, int32_t batch, int32_t n,
+                     int32_t causal, dflash_cache *cache, int32_t layer, void *out,
+                     dflash_workspace *ws, dflash_stream_t stream);
+
+/* Kernel timing for measurement passes (not for graph capture): between
+ * begin and end, the library brackets each weight-GEMM launch with a CUDA
+ * event pair on the launching stream, up to max_records launches.  end
+ * synchronises on the last event and returns per launch the elapsed
+ * milliseconds and the tags (M, K, rows); *n_out = records returned. */
+int dflash_profile_begin(int32_t max_records);
+int dflash_profile_end(float *ms_out, int32_t *tags_out, int32_t max, int32_t *n_out);
+/* Number of kernel launches this library has enqueued (or recorded into a
+ * graph under capture) since it was loaded, counted on the host. */
+long long dflash_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H_ */

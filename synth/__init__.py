@@ -53,6 +53,7 @@ class Workload:
     gen_tokens: int
     teacher_forced: bool
     batch: int = 1
+    final_gain: float = 1.0   # initial value of the final RMSNorm gains (test workloads widen logit gaps)
 
     @property
     def draft(self) -> ModelShape:
@@ -75,9 +76,9 @@ WORKLOADS = {
                          False),
     # small bf16 cases with the production head layout (d=128, GQA 4 and GQA 5)
     "small-bf16-gqa4": Workload("small-bf16-gqa4", ModelShape(6, 512, 4, 1, 128, 1024, 4096), 2, "bf16",
-                                16, 96, 48, False),
+                                16, 96, 48, False, final_gain=8.0),
     "small-bf16-gqa5": Workload("small-bf16-gqa5", ModelShape(6, 640, 5, 1, 128, 1280, 4096), 2, "bf16",
-                                15, 80, 40, False),
+                                15, 80, 40, False, final_gain=8.0),
     # Qwen3-8B-shaped target, 5-layer drafter, block 16, 4K prompt, teacher forced
     "qwen3-8b-4k": Workload("qwen3-8b-4k", _qwen3_8b_shape(), 5, "bf16", 16, 4096, 2048, True),
     # 27B-class dense target, block 15, 36K prompt, 1500 tokens, teacher forced
@@ -148,12 +149,18 @@ def host_tensor(name_index: int, shape, kind, dtype, seed=WEIGHT_SEED):
     return to_bf16_f32(w) if dtype == "bf16" else w
 
 
-def host_weights(target: ModelShape, draft_layers: int, dtype: str, seed=WEIGHT_SEED):
+def host_weights(target: ModelShape, draft_layers: int, dtype: str, seed=WEIGHT_SEED, final_gain=1.0):
     """All weights as float32 NumPy arrays (bf16-representable for "bf16")."""
     out = {}
     for i, (name, shape, kind) in enumerate(weight_specs(target, draft_layers)):
         out[name] = host_tensor(i, shape, kind, dtype, seed)
+        if name in ("final_norm", "draft.final_norm"):
+            out[name] = out[name] * np.float32(final_gain)
     return out
+
+
+def workload_weights(wl: Workload, seed=WEIGHT_SEED):
+    return host_weights(wl.target, wl.draft_layers, wl.dtype, seed, wl.final_gain)
 
 
 # ---------------------------------------------------------------------------
