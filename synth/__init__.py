@@ -76,9 +76,9 @@ WORKLOADS = {
                          False),
     # small bf16 cases with the production head layout (d=128, GQA 4 and GQA 5)
     "small-bf16-gqa4": Workload("small-bf16-gqa4", ModelShape(6, 512, 4, 1, 128, 1024, 4096), 2, "bf16",
-                                16, 96, 48, False, final_gain=8.0),
+                                16, 96, 48, False),
     "small-bf16-gqa5": Workload("small-bf16-gqa5", ModelShape(6, 640, 5, 1, 128, 1280, 4096), 2, "bf16",
-                                15, 80, 40, False, final_gain=8.0),
+                                15, 80, 40, False),
     # Qwen3-8B-shaped target, 5-layer drafter, block 16, 4K prompt, teacher forced
     "qwen3-8b-4k": Workload("qwen3-8b-4k", _qwen3_8b_shape(), 5, "bf16", 16, 4096, 2048, True),
     # 27B-class dense target, block 15, 36K prompt, 1500 tokens, teacher forced
