@@ -394,11 +394,13 @@ def run_ours(args, dist: Dist):
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
     dist.barrier()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
     evs[0].record()
     for i in range(K):
         graph.replay()
         evs[i + 1].record()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     dist.barrier()
     clk = clocks.stop()
     step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(K)]

@@ -1,0 +1,116 @@
+"""Time single kernels of libdflash.so at production shapes (small device
+footprint, suitable for Nsight Compute captures).
+
+    python -m block_diffusion_speculative_target_gb300.kernel_bench gemm --M 24576 --K 4096 --rows 16
+    python -m block_diffusion_speculative_target_gb300.kernel_bench attention --P 4096 --nq 32 --nkv 8 --n 16
+
+Weights rotate over enough copies that every launch streams from HBM, not L2.
+Prints one JSON line per kernel with the CUDA-event time per launch and the
+achieved algorithmic bandwidth.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import torch
+
+from . import capi
+
+L2_BYTES = 129 * 2 ** 20
+
+
+def _events(n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def bench_gemm(M, K, rows, iters, warmup, copies=None):
+    dev = torch.device("cuda")
+    wbytes = 2 * M * K
+    copies = copies or max(2, -(-3 * L2_BYTES // wbytes))
+    g = torch.Generator(device=dev).manual_seed(0)
+    ws_desc = capi.ModelDesc(1, K, 1, 1, 128, 128, 256, 1e6, 1e-6, capi.BF16)
+    ws = capi.dflash_workspace_alloc(ws_desc, None, 128, 256)
+    W = [torch.empty(M, K, dtype=torch.bfloat16, device=dev).normal_(0, 0.02, generator=g) for _ in range(copies)]
+    x = torch.empty(rows, K, dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+    y = torch.empty(rows, M, dtype=torch.float32, device=dev)
+    for i in range(warmup):
+        capi.dflash_linear(capi.BF16, x, W[i % copies], y, rows, M, K, ws)
+    ev = _events(iters + 1)
+    torch.cuda.synchronize()
+    ev[0].record()
+    for i in range(iters):
+        capi.dflash_linear(capi.BF16, x, W[i % copies], y, rows, M, K, ws)
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(iters)]
+    assert capi.dflash_status(ws) == 0
+    capi.dflash_workspace_free(ws)
+    avg = sum(ms) / len(ms)
+    byt = wbytes + 2 * rows * K + 4 * rows * M
+    return {"kernel": "gemm_tc_kernel", "M": M, "K": K, "rows": rows, "ms": avg, "bytes": byt,
+            "GBps": byt / (avg / 1e3) / 1e9, "splits_copies": copies}
+
+
+def bench_attention(P, nq, nkv, n, iters, warmup, causal=1):
+    dev = torch.device("cuda")
+    hd = 128
+    d = capi.ModelDesc(1, nq * hd, nq, nkv, hd, 256, 256, 1e6, 1e-6, capi.BF16)
+    cap = P + n + 64
+    copies = max(2, -(-3 * L2_BYTES // (2 * 2 * nkv * cap * hd)))
+    caches = [capi.dflash_cache_alloc(d, 1, 1, cap) for _ in range(copies)]
+    ws = capi.dflash_workspace_alloc(d, None, max(16, n), cap)
+    g = torch.Generator(device=dev).manual_seed(1)
+    kv = torch.empty(nkv, P + n, hd, dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+    for c in caches:
+        capi.dflash_cache_write(c, 0, 0, 0, P + n, kv, kv)
+        capi.dflash_cache_set_lengths(c, [P])
+    q = torch.empty(n, nq, hd, dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+    out = torch.empty(n, nq * hd, dtype=torch.bfloat16, device=dev)
+    for i in range(warmup):
+        capi.dflash_attention(d, q, 1, n, causal, caches[i % copies], 0, out, ws)
+    ev = _events(iters + 1)
+    torch.cuda.synchronize()
+    ev[0].record()
+    for i in range(iters):
+        capi.dflash_attention(d, q, 1, n, causal, caches[i % copies], 0, out, ws)
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(iters)]
+    assert capi.dflash_status(ws) == 0
+    for c in caches:
+        capi.dflash_cache_free(c)
+    capi.dflash_workspace_free(ws)
+    avg = sum(ms) / len(ms)
+    byt = 2 * 2 * nkv * (P + n) * hd
+    return {"kernel": "attn_bf16_kernel+attn_combine_kernel", "P": P, "nq": nq, "nkv": nkv, "n": n, "ms": avg,
+            "bytes": byt, "GBps": byt / (avg / 1e3) / 1e9}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("kernel", choices=["gemm", "attention", "step-gemms"])
+    ap.add_argument("--M", type=int, default=24576)
+    ap.add_argument("--K", type=int, default=4096)
+    ap.add_argument("--rows", type=int, default=16)
+    ap.add_argument("--P", type=int, default=4096)
+    ap.add_argument("--nq", type=int, default=32)
+    ap.add_argument("--nkv", type=int, default=8)
+    ap.add_argument("--n", type=int, default=16)
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    a = ap.parse_args()
+    capi.load()
+    if a.kernel == "gemm":
+        print(json.dumps(bench_gemm(a.M, a.K, a.rows, a.iters, a.warmup)))
+    elif a.kernel == "attention":
+        print(json.dumps(bench_attention(a.P, a.nq, a.nkv, a.n, a.iters, a.warmup)))
+    else:
+        # every weight-GEMM shape of one Qwen3-8B-shaped step (4096 hidden, 32/8 x 128 heads, FFN 12288)
+        for M, K in ((6144, 4096), (4096, 4096), (24576, 4096), (4096, 12288), (151936, 4096), (4096, 20480),
+                     (10240, 4096)):
+            print(json.dumps(bench_gemm(M, K, a.rows, a.iters, a.warmup)))
+
+
+if __name__ == "__main__":
+    main()
