@@ -244,7 +244,7 @@ int dflash_workspace_alloc(const dflash_model_desc* t, const dflash_model_desc* 
   if (d) f32w = std::max(f32w, (size_t)d->n_layers * 2 * d->n_kv_heads * d->head_dim);
   const size_t R = max_rows;
   const int nchunk = (max_ctx + kAttnChunk - 1) / kAttnChunk;
-  const size_t part = (size_t)2 * num_sms() * 128 * R;
+  const size_t part = (size_t)2 * gemm_splits(1 << 20, 1 << 20) * 128 * R;
   struct Req {
     void** p;
     size_t bytes;

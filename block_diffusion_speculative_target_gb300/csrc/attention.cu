@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(G * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = hk * G + warp;
   const int g = lane >> 2, t = lane & 3;
+  pdl_launch();
   pdl_wait();
   const int P = len[b];
   const int r_last = min(rb * 16 + 15, n - 1);
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(NT)
   const int c = blockIdx.x, hq = blockIdx.y, r = blockIdx.z;
   const int b = r / n, j = r % n;
   const int hk = hq / (nq / nkv);
+  pdl_launch();
   pdl_wait();
   const int P = len[b];
   const int lim = min(causal ? P + j + 1 : P + n, capacity);
@@ -264,6 +266,7 @@ __global__ void attn_combine_kernel(const float* __restrict__ part_o, const floa
                                     T* __restrict__ out) {
   const int r = blockIdx.x, hq = blockIdx.y;
   const int b = r / n, j = r % n;
+  pdl_launch();
   pdl_wait();
   const int P = len[b];
   const int lim = min(causal ? P + j + 1 : P + n, capacity);
@@ -285,7 +288,6 @@ __global__ void attn_combine_kernel(const float* __restrict__ part_o, const floa
     }
     out[((size_t)r * nq + hq) * hd + i] = from_f<T>(acc * invL);
   }
-  pdl_launch();
 }
 
 cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nkv, int hd, int causal, const void* kc,
@@ -296,23 +298,21 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
   const int nchunk_launch = (capacity + kAttnChunk - 1) / kAttnChunk;
   if (nchunk_launch > sc.nchunk || hd > kHD) return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
-  cudaError_t e;
   if (dtype == DFLASH_BF16) {
     if (hd != kHD) return cudaErrorInvalidValue;
     const int G = nq / nkv;
-    dim3 grid(nchunk_launch, nkv, batch * ((n + 15) / 16));
-#define DFL_ATTN_CASE(GG)                                                                                        \
-  case GG: {                                                                                                     \
-    static bool set = false;                                                                                     \
-    if (!set) {                                                                                                  \
-      e = cudaFuncSetAttribute(attn_bf16_kernel<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);    \
-      if (e != cudaSuccess) return e;                                                                            \
-      set = true;                                                                                                \
-    }                                                                                                            \
-    attn_bf16_kernel<GG><<<grid, GG * 32, kAttnSmem, s>>>((const bf16*)q, n, nq, causal, (const bf16*)kc,        \
-                                                          (const bf16*)vc, seq_stride, head_stride, capacity, len, \
-                                                          sc.o, sc.ml, sc.nchunk, scale_log2);                   \
-    break;                                                                                                       \
+    const dim3 grid(nchunk_launch, nkv, batch * ((n + 15) / 16));
+#define DFL_ATTN_CASE(GG)                                                                                     \
+  case GG: {                                                                                                  \
+    static bool set = false;                                                                                  \
+    if (!set) {                                                                                               \
+      DFL_RET(cudaFuncSetAttribute(attn_bf16_kernel<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem)); \
+      set = true;                                                                                             \
+    }                                                                                                         \
+    DFL_RET(launch_pdl(attn_bf16_kernel<GG>, grid, dim3(GG * 32), kAttnSmem, s, (const bf16*)q, n, nq, causal,  \
+                       (const bf16*)kc, (const bf16*)vc, seq_stride, head_stride, capacity, len, sc.o, sc.ml,  \
+                       sc.nchunk, scale_log2));                                                                \
+    break;                                                                                                    \
   }
     switch (G) {
       DFL_ATTN_CASE(1)
@@ -324,22 +324,18 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
         return cudaErrorInvalidValue;
     }
 #undef DFL_ATTN_CASE
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    attn_combine_kernel<bf16><<<dim3(batch * n, nq), kHD, 0, s>>>(sc.o, sc.ml, n, nq, hd, causal, capacity, len,
-                                                                  sc.nchunk, (bf16*)out);
+    DFL_RET(launch_pdl(attn_combine_kernel<bf16>, dim3(batch * n, nq), dim3(kHD), 0, s, sc.o, sc.ml, n, nq, hd,
+                       causal, capacity, len, sc.nchunk, (bf16*)out));
   } else {
-    dim3 grid(nchunk_launch, nq, batch * n);
-    attn_f32_kernel<128><<<grid, 128, 0, s>>>((const float*)q, n, nq, nkv, hd, causal, (const float*)kc,
-                                              (const float*)vc, seq_stride, head_stride, capacity, len, sc.o, sc.ml,
-                                              sc.nchunk, scale_log2);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    attn_combine_kernel<float><<<dim3(batch * n, nq), hd, 0, s>>>(sc.o, sc.ml, n, nq, hd, causal, capacity, len,
-                                                                  sc.nchunk, (float*)out);
+    const dim3 grid(nchunk_launch, nq, batch * n);
+    DFL_RET(launch_pdl(attn_f32_kernel<128>, grid, dim3(128), 0, s, (const float*)q, n, nq, nkv, hd, causal,
+                       (const float*)kc, (const float*)vc, seq_stride, head_stride, capacity, len, sc.o, sc.ml,
+                       sc.nchunk, scale_log2));
+    DFL_RET(launch_pdl(attn_combine_kernel<float>, dim3(batch * n, nq), dim3(hd), 0, s, sc.o, sc.ml, n, nq, hd,
+                       causal, capacity, len, sc.nchunk, (float*)out));
   }
   count_launch(2);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace dfl

@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__
   const int mp = tid & 31, nq = tid >> 5;  // m pair index, n pair index
   const int ml = 2 * mp, nl = 2 * nq;
   float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+  pdl_launch();
   pdl_wait();
   for (int k0 = 0; k0 < K; k0 += SB_K) {
     for (int i = tid; i < SB_M * SB_K; i += 256) {
@@ -68,13 +69,12 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__
       }
     }
   }
-  pdl_launch();
 }
 
 cudaError_t gemm_simt(const float* X, int ldx, int rows, const float* W, int M, int K, const Epi& epi,
                       cudaStream_t s) {
   dim3 grid((M + SB_M - 1) / SB_M, (rows + SB_N - 1) / SB_N);
-  gemm_f32_kernel<<<grid, 256, 0, s>>>(X, ldx, rows, W, M, K, epi);
+  DFL_RET(launch_pdl(gemm_f32_kernel, dim3(grid), dim3(256), 0, s, X, ldx, rows, W, M, K, epi));
   count_launch();
   return cudaGetLastError();
 }

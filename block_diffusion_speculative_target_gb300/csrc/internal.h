@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/dflash.h"
 
 namespace dfl {
@@ -35,6 +37,31 @@ constexpr int kMaxRows = 128;
 constexpr int kAttnChunk = 256;
 
 int num_sms();
+
+// Launch with programmatic dependent launch allowed: the kernel may start
+// while its predecessor finishes; every kernel of this library calls
+// griddepcontrol.wait before touching data another kernel produces or reads.
+#define DFL_RET(expr)                 \
+  do {                                \
+    cudaError_t e_ = (expr);          \
+    if (e_ != cudaSuccess) return e_; \
+  } while (0)
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 // Host-side count of kernel launches enqueued by the library (for measurement).
 void count_launch(int n = 1);
 long long launch_count();

@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(NT) rmsnorm_kernel(const float* __restrict__ x
   __shared__ float red[NT / 32];
   const float* xr = x + (size_t)blockIdx.x * H;
   T* yr = y + (size_t)blockIdx.x * H;
+  pdl_launch();
   pdl_wait();
   float ss = 0.f;
   for (int i = threadIdx.x * 4; i < H; i += NT * 4) {
@@ -36,16 +37,15 @@ __global__ void __launch_bounds__(NT) rmsnorm_kernel(const float* __restrict__ x
     yr[i + 2] = from_f<T>(v.z * inv * to_f<T>(g[i + 2]));
     yr[i + 3] = from_f<T>(v.w * inv * to_f<T>(g[i + 3]));
   }
-  pdl_launch();
 }
 
 cudaError_t rmsnorm(int dtype, const float* x, const void* g, void* y, int rows, int H, float eps,
                     cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
-    rmsnorm_kernel<bf16, 256><<<rows, 256, 0, s>>>(x, (const bf16*)g, (bf16*)y, H, eps);
+    DFL_RET(launch_pdl(rmsnorm_kernel<bf16, 256>, dim3(rows), dim3(256), 0, s, x, (const bf16*)g, (bf16*)y, H, eps));
   else
-    rmsnorm_kernel<float, 256><<<rows, 256, 0, s>>>(x, (const float*)g, (float*)y, H, eps);
+    DFL_RET(launch_pdl(rmsnorm_kernel<float, 256>, dim3(rows), dim3(256), 0, s, x, (const float*)g, (float*)y, H, eps));
   count_launch();
   return cudaGetLastError();
 }
@@ -55,17 +55,17 @@ template <typename T>
 __global__ void capture_kernel(const float* __restrict__ x, T* __restrict__ hcap, int H, int slot) {
   const float* xr = x + (size_t)blockIdx.x * H;
   T* hr = hcap + (size_t)blockIdx.x * 5 * H + (size_t)slot * H;
+  pdl_launch();
   pdl_wait();
   for (int i = threadIdx.x; i < H; i += blockDim.x) hr[i] = from_f<T>(xr[i]);
-  pdl_launch();
 }
 
 cudaError_t capture(int dtype, const float* x, void* hcap, int rows, int H, int slot, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
-    capture_kernel<bf16><<<rows, 256, 0, s>>>(x, (bf16*)hcap, H, slot);
+    DFL_RET(launch_pdl(capture_kernel<bf16>, dim3(rows), dim3(256), 0, s, x, (bf16*)hcap, H, slot));
   else
-    capture_kernel<float><<<rows, 256, 0, s>>>(x, (float*)hcap, H, slot);
+    DFL_RET(launch_pdl(capture_kernel<float>, dim3(rows), dim3(256), 0, s, x, (float*)hcap, H, slot));
   count_launch();
   return cudaGetLastError();
 }
@@ -76,6 +76,7 @@ __global__ void embed_kernel(const T* __restrict__ E, int V, int H, const int32_
                              const int32_t* __restrict__ anchor, int mask_id, int n, int mode,
                              int32_t* __restrict__ draft_out, float* __restrict__ x, int* status) {
   const int r = blockIdx.x, b = r / n, j = r % n;
+  pdl_launch();
   pdl_wait();
   int tok;
   if (mode == 0) {
@@ -91,7 +92,6 @@ __global__ void embed_kernel(const T* __restrict__ E, int V, int H, const int32_
   const T* er = E + (size_t)tok * H;
   float* xr = x + (size_t)r * H;
   for (int i = threadIdx.x; i < H; i += blockDim.x) xr[i] = to_f<T>(er[i]);
-  pdl_launch();
 }
 
 cudaError_t embed(int dtype, const void* E, int V, int H, const int32_t* tokens, const int32_t* anchor, int mask_id,
@@ -99,11 +99,11 @@ cudaError_t embed(int dtype, const void* E, int V, int H, const int32_t* tokens,
   const int rows = batch * n;
   if (rows <= 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
-    embed_kernel<bf16><<<rows, 256, 0, s>>>((const bf16*)E, V, H, tokens, anchor, mask_id, n, mode, draft_out, x,
-                                            status);
+    DFL_RET(launch_pdl(embed_kernel<bf16>, dim3(rows), dim3(256), 0, s, (const bf16*)E, V, H, tokens, anchor, mask_id, n, mode, draft_out, x,
+                                            status));
   else
-    embed_kernel<float><<<rows, 256, 0, s>>>((const float*)E, V, H, tokens, anchor, mask_id, n, mode, draft_out, x,
-                                             status);
+    DFL_RET(launch_pdl(embed_kernel<float>, dim3(rows), dim3(256), 0, s, (const float*)E, V, H, tokens, anchor, mask_id, n, mode, draft_out, x,
+                                             status));
   count_launch();
   return cudaGetLastError();
 }
@@ -119,6 +119,7 @@ __global__ void rope_qkv_kernel(const float* __restrict__ qkv, int n, int nq, in
   const int r = blockIdx.x, b = r / n, j = r % n;
   const int half = hd / 2;
   const int width = (nq + 2 * nkv) * hd;
+  pdl_launch();
   pdl_wait();
   const int pos = len[b] + j;
   const bool in_cap = pos < capacity;
@@ -147,7 +148,6 @@ __global__ void rope_qkv_kernel(const float* __restrict__ qkv, int n, int nq, in
           from_f<T>(src[(nq + nkv) * hd + t]);
     }
   }
-  pdl_launch();
 }
 
 cudaError_t rope_qkv(int dtype, const float* qkv, int batch, int n, int nq, int nkv, int hd, void* qout, void* kc,
@@ -156,11 +156,11 @@ cudaError_t rope_qkv(int dtype, const float* qkv, int batch, int n, int nq, int 
   const int rows = batch * n;
   if (rows <= 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
-    rope_qkv_kernel<bf16><<<rows, 256, 0, s>>>(qkv, n, nq, nkv, hd, (bf16*)qout, (bf16*)kc, (bf16*)vc, seq_stride,
-                                               head_stride, capacity, len, tab, status);
+    DFL_RET(launch_pdl(rope_qkv_kernel<bf16>, dim3(rows), dim3(256), 0, s, qkv, n, nq, nkv, hd, (bf16*)qout, (bf16*)kc, (bf16*)vc, seq_stride,
+                                               head_stride, capacity, len, tab, status));
   else
-    rope_qkv_kernel<float><<<rows, 256, 0, s>>>(qkv, n, nq, nkv, hd, (float*)qout, (float*)kc, (float*)vc,
-                                                seq_stride, head_stride, capacity, len, tab, status);
+    DFL_RET(launch_pdl(rope_qkv_kernel<float>, dim3(rows), dim3(256), 0, s, qkv, n, nq, nkv, hd, (float*)qout, (float*)kc, (float*)vc,
+                                                seq_stride, head_stride, capacity, len, tab, status));
   count_launch();
   return cudaGetLastError();
 }
@@ -172,15 +172,14 @@ __global__ void inject_kernel(const float* __restrict__ kv, int rps, int Ld, int
                               int capacity, const int32_t* __restrict__ len, const int32_t* __restrict__ n_pend,
                               const float2* __restrict__ tab, int* status) {
   const int r = blockIdx.x, b = r / rps, j = r % rps;
+  pdl_launch();
   pdl_wait();
   if (j >= n_pend[b]) {
-    pdl_launch();
     return;
   }
   const int pos = len[b] + j;
   if (pos >= capacity) {
     if (threadIdx.x == 0) set_status(status, DFLASH_STATUS_CAPACITY);
-    pdl_launch();
     return;
   }
   const int half = hd / 2;
@@ -201,7 +200,6 @@ __global__ void inject_kernel(const float* __restrict__ kv, int rps, int Ld, int
     vc[(size_t)l * layer_stride + (size_t)b * seq_stride + (size_t)h * head_stride + (size_t)pos * hd + i] =
         from_f<T>(vs[i]);
   }
-  pdl_launch();
 }
 
 cudaError_t inject_write(int dtype, const float* kv, int batch, int rps, int Ld, int nkv, int hd, void* kc, void* vc,
@@ -211,28 +209,28 @@ cudaError_t inject_write(int dtype, const float* kv, int batch, int rps, int Ld,
   const int rows = batch * rps;
   if (rows <= 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
-    inject_kernel<bf16><<<rows, 256, 0, s>>>(kv, rps, Ld, nkv, hd, (bf16*)kc, (bf16*)vc, layer_stride, seq_stride,
-                                             head_stride, capacity, len, n_pend, tab, status);
+    DFL_RET(launch_pdl(inject_kernel<bf16>, dim3(rows), dim3(256), 0, s, kv, rps, Ld, nkv, hd, (bf16*)kc, (bf16*)vc, layer_stride, seq_stride,
+                                             head_stride, capacity, len, n_pend, tab, status));
   else
-    inject_kernel<float><<<rows, 256, 0, s>>>(kv, rps, Ld, nkv, hd, (float*)kc, (float*)vc, layer_stride,
-                                              seq_stride, head_stride, capacity, len, n_pend, tab, status);
+    DFL_RET(launch_pdl(inject_kernel<float>, dim3(rows), dim3(256), 0, s, kv, rps, Ld, nkv, hd, (float*)kc, (float*)vc, layer_stride,
+                                              seq_stride, head_stride, capacity, len, n_pend, tab, status));
   count_launch();
   return cudaGetLastError();
 }
 
 // The injected rows are consumed: len += n_pend, n_pend = 0.
 __global__ void advance_len_kernel(int32_t* len, int32_t* n_pend, int batch) {
+  pdl_launch();
   pdl_wait();
   const int b = threadIdx.x;
   if (b < batch) {
     len[b] += n_pend[b];
     n_pend[b] = 0;
   }
-  pdl_launch();
 }
 
 cudaError_t advance_len(int32_t* len, int32_t* n_pend, int batch, cudaStream_t s) {
-  advance_len_kernel<<<1, 32 * ((batch + 31) / 32), 0, s>>>(len, n_pend, batch);
+  DFL_RET(launch_pdl(advance_len_kernel, dim3(1), dim3(32 * ((batch + 31) / 32)), 0, s, len, n_pend, batch));
   count_launch();
   return cudaGetLastError();
 }
@@ -259,6 +257,7 @@ __global__ void __launch_bounds__(NT) argmax_kernel(const float* __restrict__ lo
                                                     float* __restrict__ gap, int skip_first_of, int* status) {
   __shared__ Top2 sh[NT / 32];
   const float* row = logits + (size_t)blockIdx.x * V;
+  pdl_launch();
   pdl_wait();
   Top2 t{-INFINITY, -INFINITY, 0x7fffffff};
   bool bad = false;
@@ -294,13 +293,12 @@ __global__ void __launch_bounds__(NT) argmax_kernel(const float* __restrict__ lo
     if (!skip) out[blockIdx.x] = r.i1;
     if (gap) gap[blockIdx.x] = r.v1 - r.v2;
   }
-  pdl_launch();
 }
 
 cudaError_t argmax(const float* logits, int rows, int V, int32_t* out, float* gap, int skip_first_of, int* status,
                    cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  argmax_kernel<1024><<<rows, 1024, 0, s>>>(logits, V, out, gap, skip_first_of, status);
+  DFL_RET(launch_pdl(argmax_kernel<1024>, dim3(rows), dim3(1024), 0, s, logits, V, out, gap, skip_first_of, status));
   count_launch();
   return cudaGetLastError();
 }
@@ -308,6 +306,7 @@ cudaError_t argmax(const float* logits, int rows, int V, int32_t* out, float* ga
 // ------------------------------------------------------------------ commit (prefill / AR)
 __global__ void commit_kernel(int32_t* len, int32_t* n_pend, int32_t* anchor, const int32_t* argmax, int batch, int n,
                               int emit, int32_t* stream, int32_t* stream_len, int stream_cap, int* status) {
+  pdl_launch();
   pdl_wait();
   const int b = threadIdx.x;
   if (b < batch) {
@@ -327,13 +326,12 @@ __global__ void commit_kernel(int32_t* len, int32_t* n_pend, int32_t* anchor, co
       }
     }
   }
-  pdl_launch();
 }
 
 cudaError_t commit_rows(int32_t* len, int32_t* n_pend, int32_t* anchor, const int32_t* argmax, int batch, int n,
                         int emit, int32_t* stream, int32_t* stream_len, int stream_cap, int* status, cudaStream_t s) {
-  commit_kernel<<<1, 32 * ((batch + 31) / 32), 0, s>>>(len, n_pend, anchor, argmax, batch, n, emit, stream,
-                                                       stream_len, stream_cap, status);
+  DFL_RET(launch_pdl(commit_kernel, dim3(1), dim3(32 * ((batch + 31) / 32)), 0, s, len, n_pend, anchor, argmax, batch, n, emit, stream,
+                                                       stream_len, stream_cap, status));
   count_launch();
   return cudaGetLastError();
 }
@@ -345,11 +343,11 @@ cudaError_t commit_rows(int32_t* len, int32_t* n_pend, int32_t* anchor, const in
 __global__ void accept_kernel(const int32_t* __restrict__ draft, const int32_t* __restrict__ argmax, int batch,
                               int block, int32_t* len, int32_t* anchor, int32_t* n_pend, int32_t* accept_len,
                               int32_t* stream, int32_t* stream_len, int stream_cap, int* status) {
+  pdl_launch();
   pdl_wait();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= batch) {
-    pdl_launch();
     return;
   }
   const int32_t* d = draft + (size_t)b * block;
@@ -372,15 +370,14 @@ __global__ void accept_kernel(const int32_t* __restrict__ draft, const int32_t* 
     if (accept_len) accept_len[b] = a;
     if (stream_len) stream_len[b] = min(e + a + 1, stream_cap);
   }
-  pdl_launch();
 }
 
 cudaError_t accept_rollback(const int32_t* draft, const int32_t* argmax, int batch, int block, int32_t* len,
                             int32_t* anchor, int32_t* n_pend, int32_t* accept_len, int32_t* stream,
                             int32_t* stream_len, int stream_cap, int* status, cudaStream_t s) {
   const int warps = batch < 8 ? batch : 8;
-  accept_kernel<<<(batch + warps - 1) / warps, 32 * warps, 0, s>>>(draft, argmax, batch, block, len, anchor, n_pend,
-                                                                   accept_len, stream, stream_len, stream_cap, status);
+  DFL_RET(launch_pdl(accept_kernel, dim3((batch + warps - 1) / warps), dim3(32 * warps), 0, s, draft, argmax, batch, block, len, anchor, n_pend,
+                                                                   accept_len, stream, stream_len, stream_cap, status));
   count_launch();
   return cudaGetLastError();
 }
@@ -390,6 +387,7 @@ __global__ void teacher_force_kernel(int32_t* draft, int batch, int block, const
                                      int ref_stride, int ref_len, const int32_t* __restrict__ stream_len,
                                      const int32_t* __restrict__ k_draw, const int32_t* __restrict__ r_draw,
                                      int max_steps, int32_t* step, int vocab, int* status) {
+  pdl_launch();
   pdl_wait();
   const int st = *step;
   const int b = threadIdx.x;
@@ -413,15 +411,14 @@ __global__ void teacher_force_kernel(int32_t* draft, int batch, int block, const
   }
   __syncthreads();
   if (threadIdx.x == 0) *step = st + 1;
-  pdl_launch();
 }
 
 cudaError_t teacher_force(int32_t* draft, int batch, int block, const int32_t* ref, int ref_stride, int ref_len,
                           const int32_t* stream_len, const int32_t* k_draw, const int32_t* r_draw, int max_steps,
                           int32_t* step, int vocab, int* status, cudaStream_t s) {
-  teacher_force_kernel<<<1, 32 * ((batch + 31) / 32), 0, s>>>(draft, batch, block, ref, ref_stride, ref_len,
+  DFL_RET(launch_pdl(teacher_force_kernel, dim3(1), dim3(32 * ((batch + 31) / 32)), 0, s, draft, batch, block, ref, ref_stride, ref_len,
                                                               stream_len, k_draw, r_draw, max_steps, step, vocab,
-                                                              status);
+                                                              status));
   count_launch();
   return cudaGetLastError();
 }

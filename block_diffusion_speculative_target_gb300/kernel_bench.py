@@ -5,8 +5,10 @@ footprint, suitable for Nsight Compute captures).
     python -m block_diffusion_speculative_target_gb300.kernel_bench attention --P 4096 --nq 32 --nkv 8 --n 16
 
 Weights rotate over enough copies that every launch streams from HBM, not L2.
-Prints one JSON line per kernel with the CUDA-event time per launch and the
-achieved algorithmic bandwidth.
+The timed launches are captured in a CUDA graph, so host launch overhead is
+excluded: time per launch = graph time / launches (back-to-back kernels).
+Prints one JSON line per kernel with the time per launch and the achieved
+algorithmic bandwidth.
 """
 from __future__ import annotations
 
@@ -20,8 +22,27 @@ from . import capi
 L2_BYTES = 129 * 2 ** 20
 
 
-def _events(n):
-    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+def _graph_time(fn, launches, replays=5):
+    """Capture fn() (issuing `launches` kernels' worth of work) in a CUDA graph
+    and return the median milliseconds per launch over several replays."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / launches)
+    times.sort()
+    return times[len(times) // 2]
 
 
 def bench_gemm(M, K, rows, iters, warmup, copies=None):
@@ -36,17 +57,10 @@ def bench_gemm(M, K, rows, iters, warmup, copies=None):
     y = torch.empty(rows, M, dtype=torch.float32, device=dev)
     for i in range(warmup):
         capi.dflash_linear(capi.BF16, x, W[i % copies], y, rows, M, K, ws)
-    ev = _events(iters + 1)
-    torch.cuda.synchronize()
-    ev[0].record()
-    for i in range(iters):
-        capi.dflash_linear(capi.BF16, x, W[i % copies], y, rows, M, K, ws)
-        ev[i + 1].record()
-    torch.cuda.synchronize()
-    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(iters)]
+    avg = _graph_time(lambda: [capi.dflash_linear(capi.BF16, x, W[i % copies], y, rows, M, K, ws)
+                               for i in range(iters)], iters)
     assert capi.dflash_status(ws) == 0
     capi.dflash_workspace_free(ws)
-    avg = sum(ms) / len(ms)
     byt = wbytes + 2 * rows * K + 4 * rows * M
     return {"kernel": "gemm_tc_kernel", "M": M, "K": K, "rows": rows, "ms": avg, "bytes": byt,
             "GBps": byt / (avg / 1e3) / 1e9, "splits_copies": copies}
@@ -69,19 +83,12 @@ def bench_attention(P, nq, nkv, n, iters, warmup, causal=1):
     out = torch.empty(n, nq * hd, dtype=torch.bfloat16, device=dev)
     for i in range(warmup):
         capi.dflash_attention(d, q, 1, n, causal, caches[i % copies], 0, out, ws)
-    ev = _events(iters + 1)
-    torch.cuda.synchronize()
-    ev[0].record()
-    for i in range(iters):
-        capi.dflash_attention(d, q, 1, n, causal, caches[i % copies], 0, out, ws)
-        ev[i + 1].record()
-    torch.cuda.synchronize()
-    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(iters)]
+    avg = _graph_time(lambda: [capi.dflash_attention(d, q, 1, n, causal, caches[i % copies], 0, out, ws)
+                               for i in range(iters)], iters)
     assert capi.dflash_status(ws) == 0
     for c in caches:
         capi.dflash_cache_free(c)
     capi.dflash_workspace_free(ws)
-    avg = sum(ms) / len(ms)
     byt = 2 * 2 * nkv * (P + n) * hd
     return {"kernel": "attn_bf16_kernel+attn_combine_kernel", "P": P, "nq": nq, "nkv": nkv, "n": n, "ms": avg,
             "bytes": byt, "GBps": byt / (avg / 1e3) / 1e9}
