@@ -35,7 +35,6 @@ struct dflash_workspace {
   void* attn;
   void* act;
   float* logits;
-  GemmScratch gs;
   AttnScratch as;
   int* status;
   std::vector<void*> allocs;
@@ -244,7 +243,6 @@ int dflash_workspace_alloc(const dflash_model_desc* t, const dflash_model_desc* 
   if (d) f32w = std::max(f32w, (size_t)d->n_layers * 2 * d->n_kv_heads * d->head_dim);
   const size_t R = max_rows;
   const int nchunk = (max_ctx + kAttnChunk - 1) / kAttnChunk;
-  const size_t part = (size_t)2 * gemm_splits(1 << 20, 1 << 20) * 128 * R;
   struct Req {
     void** p;
     size_t bytes;
@@ -256,8 +254,7 @@ int dflash_workspace_alloc(const dflash_model_desc* t, const dflash_model_desc* 
       {(void**)&w->attn, R * qw * es},
       {(void**)&w->act, R * F * es},
       {(void**)&w->logits, R * V * 4},
-      {(void**)&w->gs.part, part * 4},
-      {(void**)&w->gs.tickets, 4096 * 4},
+
       {(void**)&w->as.o, R * nq * nchunk * 128 * 4},
       {(void**)&w->as.ml, R * nq * nchunk * 2 * 4},
       {(void**)&w->status, 4},
@@ -272,10 +269,8 @@ int dflash_workspace_alloc(const dflash_model_desc* t, const dflash_model_desc* 
     *r.p = p;
     w->allocs.push_back(p);
   }
-  w->gs.part_elems = part;
-  w->gs.n_tickets = 4096;
   w->as.nchunk = nchunk;
-  cudaMemset(w->gs.tickets, 0, 4096 * 4);
+
   cudaMemset(w->status, 0, 4);
   cudaMemset(w->x, 0, R * H * 4);
   if (cudaDeviceSynchronize() != cudaSuccess) {
@@ -306,34 +301,30 @@ int dflash_status(dflash_workspace* w, dflash_stream_t stream, int32_t* status_o
 }  // extern "C"
 
 // ------------------------------------------------------------------ kernel timing
-// While enabled (measurement passes only), every weight GEMM launch is
-// bracketed by a pair of CUDA events on its stream.
+// While enabled (measurement passes only), every weight product is bracketed
+// by a pair of CUDA events on its stream; tags record the kind (1: bf16
+// tensor-core kernel, 0: fp32), the rows and the weight kilobytes.
 namespace {
 struct Profile {
   bool on = false;
   int max = 0, n = 0;
   std::vector<cudaEvent_t> ev;
-  std::vector<int32_t> tags;  // M, K, rows per record
+  std::vector<int32_t> tags;  // kind, rows, weight KB per record
 } g_prof;
 }  // namespace
 
-static cudaError_t pgemm(int dtype, const void* X, int ldx, int rows, const void* W, int M, int K, const Epi& epi,
-                         const GemmScratch& scr, int* status, cudaStream_t s) {
-  const bool rec = g_prof.on && g_prof.n < g_prof.max;
-  if (rec) {
-    cudaError_t e = cudaEventRecord(g_prof.ev[2 * g_prof.n], s);
-    if (e != cudaSuccess) return e;
-  }
-  cudaError_t e = gemm(dtype, X, ldx, rows, W, M, K, epi, scr, status, s);
+static cudaError_t prof_begin(cudaStream_t s) {
+  if (g_prof.on && g_prof.n < g_prof.max) return cudaEventRecord(g_prof.ev[2 * g_prof.n], s);
+  return cudaSuccess;
+}
+static cudaError_t prof_end(cudaStream_t s, int kind, int rows, double weight_bytes) {
+  if (!(g_prof.on && g_prof.n < g_prof.max)) return cudaSuccess;
+  cudaError_t e = cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], s);
   if (e != cudaSuccess) return e;
-  if (rec) {
-    e = cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], s);
-    if (e != cudaSuccess) return e;
-    g_prof.tags[3 * g_prof.n] = M;
-    g_prof.tags[3 * g_prof.n + 1] = K;
-    g_prof.tags[3 * g_prof.n + 2] = rows;
-    ++g_prof.n;
-  }
+  g_prof.tags[3 * g_prof.n] = kind;
+  g_prof.tags[3 * g_prof.n + 1] = rows;
+  g_prof.tags[3 * g_prof.n + 2] = (int32_t)(weight_bytes / 1024.0);
+  ++g_prof.n;
   return cudaSuccess;
 }
 
@@ -369,30 +360,118 @@ extern "C" int dflash_profile_end(float* ms_out, int32_t* tags_out, int32_t max,
   return DFLASH_OK;
 }
 
+// ------------------------------------------------------------------ weight products
+static GemmEpi epi_of(int kind, void* out, int ldo) {
+  GemmEpi e;
+  memset(&e, 0, sizeof(e));
+  e.kind = kind;
+  e.out = out;
+  e.ldo = ldo;
+  return e;
+}
+
+static GemmEpi epi_cache(int kind, void* out, int ldo, dflash_cache* c, int layer, int nq, int rows_per_seq,
+                         const int32_t* n_pend) {
+  GemmEpi e = epi_of(kind, out, ldo);
+  e.nq = nq;
+  e.nkv = c->n_kv;
+  e.rows_per_seq = rows_per_seq;
+  e.capacity = c->capacity;
+  e.len = c->len;
+  e.rope = c->rope;
+  e.n_pend = n_pend;
+  e.kc = c->k + (size_t)layer * c->layer_stride * c->elem;
+  e.vc = c->v + (size_t)layer * c->layer_stride * c->elem;
+  e.layer_stride = c->layer_stride;
+  e.seq_stride = c->seq_stride;
+  e.head_stride = c->head_stride;
+  return e;
+}
+
+static cudaError_t gemm_b16(const void* X, int ldx, int rows, const void* W, int M, int K, const GemmEpi& epi,
+                            dflash_workspace* ws, cudaStream_t s) {
+  DFL_RET(prof_begin(s));
+  DFL_RET(gemm_bf16(X, ldx, rows, W, M, K, epi, ws->status, s));
+  return prof_end(s, 1, rows, 2.0 * M * K);
+}
+
+static cudaError_t gemm_f32(const void* X, int ldx, int rows, const void* W, int M, int K, const Epi& epi,
+                            cudaStream_t s) {
+  DFL_RET(prof_begin(s));
+  DFL_RET(gemm_simt((const float*)X, ldx, rows, (const float*)W, M, K, epi, s));
+  return prof_end(s, 0, rows, 4.0 * M * K);
+}
+
 // ------------------------------------------------------------------ composed forward
-static int layer_forward(const dflash_model_desc& d, const dflash_layer_w& w, dflash_cache* c, int layer, int batch,
-                         int n, int causal, dflash_workspace* ws, cudaStream_t s) {
+static bool cache_matches(const dflash_cache* c, const dflash_model_desc& d, int n_layers) {
+  return c && c->n_kv == d.n_kv_heads && c->head_dim == d.head_dim && c->dtype == d.dtype &&
+         c->n_layers >= n_layers;
+}
+
+static int layer_forward_f32(const dflash_model_desc& d, const dflash_layer_w& w, dflash_cache* c, int layer,
+                             int batch, int n, int causal, dflash_workspace* ws, cudaStream_t s) {
   const int rows = batch * n, H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads;
   const int qkvw = (nq + 2 * nkv) * hd, dt = d.dtype;
-  REQ(w.attn_norm && w.wqkv && w.wo && w.ffn_norm && w.w_gate_up && w.w_down);
   uint8_t* kc = c->k + (size_t)layer * c->layer_stride * c->elem;
   uint8_t* vc = c->v + (size_t)layer * c->layer_stride * c->elem;
   CK(rmsnorm(dt, ws->x, w.attn_norm, ws->xn, rows, H, d.rms_eps, s));
-  CK(pgemm(dt, ws->xn, H, rows, w.wqkv, qkvw, H, Epi{EPI_F32, ws->f32buf, qkvw}, ws->gs, ws->status, s));
+  CK(gemm_f32(ws->xn, H, rows, w.wqkv, qkvw, H, Epi{EPI_F32, ws->f32buf, qkvw}, s));
   CK(rope_qkv(dt, ws->f32buf, batch, n, nq, nkv, hd, ws->q, kc, vc, c->seq_stride, c->head_stride, c->capacity,
               c->len, c->rope, ws->status, s));
   CK(attention(dt, ws->q, batch, n, nq, nkv, hd, causal, kc, vc, c->seq_stride, c->head_stride, c->capacity, c->len,
                ws->as, ws->attn, ws->status, s));
-  CK(pgemm(dt, ws->attn, nq * hd, rows, w.wo, H, nq * hd, Epi{EPI_RESID, ws->x, H}, ws->gs, ws->status, s));
+  CK(gemm_f32(ws->attn, nq * hd, rows, w.wo, H, nq * hd, Epi{EPI_RESID, ws->x, H}, s));
   CK(rmsnorm(dt, ws->x, w.ffn_norm, ws->xn, rows, H, d.rms_eps, s));
-  CK(pgemm(dt, ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, Epi{EPI_SWIGLU, ws->act, d.ffn}, ws->gs, ws->status, s));
-  CK(pgemm(dt, ws->act, d.ffn, rows, w.w_down, H, d.ffn, Epi{EPI_RESID, ws->x, H}, ws->gs, ws->status, s));
+  CK(gemm_f32(ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, Epi{EPI_SWIGLU, ws->act, d.ffn}, s));
+  CK(gemm_f32(ws->act, d.ffn, rows, w.w_down, H, d.ffn, Epi{EPI_RESID, ws->x, H}, s));
   return DFLASH_OK;
 }
 
-static bool cache_matches(const dflash_cache* c, const dflash_model_desc& d, int n_layers) {
-  return c && c->n_kv == d.n_kv_heads && c->head_dim == d.head_dim && c->dtype == d.dtype &&
-         c->n_layers >= n_layers;
+// The decoder stack and LM head on x (already embedded).  Per layer: RMSNorm,
+// QKV product (bf16: RoPE and the KV-cache write fused in its epilogue),
+// attention, O product + residual, RMSNorm, gate/up product + SwiGLU, down
+// product + residual.  Captured states (hcap != null) after the layers in
+// capture[].
+static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layers, dflash_cache* c, int batch, int n,
+                         int causal, const int32_t* capture, void* hcap, const void* final_norm, const void* lm_head,
+                         dflash_workspace* ws, cudaStream_t s) {
+  const int rows = batch * n, H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, L = d.n_layers;
+  for (int l = 0; l < L; ++l) {
+    const dflash_layer_w& w = layers[l];
+    REQ(w.attn_norm && w.wqkv && w.wo && w.ffn_norm && w.w_gate_up && w.w_down);
+  }
+  if (d.dtype != DFLASH_BF16) {
+    for (int l = 0; l < L; ++l) {
+      int rc = layer_forward_f32(d, layers[l], c, l, batch, n, causal, ws, s);
+      if (rc != DFLASH_OK) return rc;
+      if (hcap)
+        for (int si = 0; si < 5; ++si)
+          if (capture[si] == l) CK(dfl::capture(d.dtype, ws->x, hcap, rows, H, si, s));
+    }
+    CK(rmsnorm(d.dtype, ws->x, final_norm, ws->xn, rows, H, d.rms_eps, s));
+    CK(gemm_f32(ws->xn, H, rows, lm_head, d.vocab, H, Epi{EPI_F32, ws->logits, d.vocab}, s));
+    return DFLASH_OK;
+  }
+  const int qkvw = (nq + 2 * nkv) * hd;
+  for (int l = 0; l < L; ++l) {
+    const dflash_layer_w& w = layers[l];
+    uint8_t* kc = c->k + (size_t)l * c->layer_stride * c->elem;
+    uint8_t* vc = c->v + (size_t)l * c->layer_stride * c->elem;
+    CK(rmsnorm(d.dtype, ws->x, w.attn_norm, ws->xn, rows, H, d.rms_eps, s));
+    CK(gemm_b16(ws->xn, H, rows, w.wqkv, qkvw, H, epi_cache(GE_QKV, ws->q, nq * hd, c, l, nq, n, nullptr), ws, s));
+    CK(attention(d.dtype, ws->q, batch, n, nq, nkv, hd, causal, kc, vc, c->seq_stride, c->head_stride, c->capacity,
+                 c->len, ws->as, ws->attn, ws->status, s));
+    CK(gemm_b16(ws->attn, nq * hd, rows, w.wo, H, nq * hd, epi_of(GE_RESID, ws->x, H), ws, s));
+    CK(rmsnorm(d.dtype, ws->x, w.ffn_norm, ws->xn, rows, H, d.rms_eps, s));
+    CK(gemm_b16(ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, epi_of(GE_SWIGLU, ws->act, d.ffn), ws, s));
+    CK(gemm_b16(ws->act, d.ffn, rows, w.w_down, H, d.ffn, epi_of(GE_RESID, ws->x, H), ws, s));
+    if (hcap)
+      for (int si = 0; si < 5; ++si)
+        if (capture[si] == l) CK(dfl::capture(d.dtype, ws->x, hcap, rows, H, si, s));
+  }
+  CK(rmsnorm(d.dtype, ws->x, final_norm, ws->xn, rows, H, d.rms_eps, s));
+  CK(gemm_b16(ws->xn, H, rows, lm_head, d.vocab, H, epi_of(GE_F32, ws->logits, d.vocab), ws, s));
+  return DFLASH_OK;
 }
 
 extern "C" {
@@ -412,16 +491,8 @@ int target_verify(const dflash_target* tg, const int32_t* tokens, int32_t batch,
   cudaStream_t s = (cudaStream_t)cuda_stream;
   const int rows = batch * n, H = d.hidden;
   CK(embed(d.dtype, tg->embed, d.vocab, H, tokens, nullptr, 0, batch, n, 0, nullptr, ws->x, ws->status, s));
-  for (int l = 0; l < d.n_layers; ++l) {
-    int rc = layer_forward(d, tg->layers[l], tc, l, batch, n, 1, ws, s);
-    if (rc != DFLASH_OK) return rc;
-    if (hcap)
-      for (int si = 0; si < 5; ++si)
-        if (tg->capture[si] == l) CK(capture(d.dtype, ws->x, hcap, rows, H, si, s));
-  }
-  CK(rmsnorm(d.dtype, ws->x, tg->final_norm, ws->xn, rows, H, d.rms_eps, s));
-  CK(pgemm(d.dtype, ws->xn, H, rows, tg->lm_head, d.vocab, H, Epi{EPI_F32, ws->logits, d.vocab}, ws->gs, ws->status,
-          s));
+  int rc = decoder_stack(d, tg->layers, tc, batch, n, 1, tg->capture, hcap, tg->final_norm, tg->lm_head, ws, s);
+  if (rc != DFLASH_OK) return rc;
   CK(argmax(ws->logits, rows, d.vocab, argmax_out, top2_gap, 0, ws->status, s));
   if (commit)
     CK(commit_rows(tc->len, n_pend, anchor, argmax_out, batch, n, commit == 2, stream, stream_len, stream_cap,
@@ -437,7 +508,12 @@ int dflash_fuse_features(const dflash_draft* dr, const void* hcap, int32_t rows,
   const int H = d.hidden;
   if (!gemm_shape_ok(d.dtype, H, 5 * H)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t s = (cudaStream_t)stream;
-  CK(pgemm(d.dtype, hcap, 5 * H, rows, dr->w_fc, H, 5 * H, Epi{EPI_F32, ws->f32buf, H}, ws->gs, ws->status, s));
+  if (d.dtype != DFLASH_BF16) {
+    CK(gemm_f32(hcap, 5 * H, rows, dr->w_fc, H, 5 * H, Epi{EPI_F32, ws->f32buf, H}, s));
+    CK(rmsnorm(d.dtype, ws->f32buf, dr->fc_norm, fused, rows, H, d.rms_eps, s));
+    return DFLASH_OK;
+  }
+  CK(gemm_b16(hcap, 5 * H, rows, dr->w_fc, H, 5 * H, epi_of(GE_F32, ws->f32buf, H), ws, s));
   CK(rmsnorm(d.dtype, ws->f32buf, dr->fc_norm, fused, rows, H, d.rms_eps, s));
   return DFLASH_OK;
 }
@@ -452,10 +528,16 @@ int dflash_inject_kv(const dflash_draft* dr, const void* fused, int32_t batch, i
   if (!gemm_shape_ok(d.dtype, W, H)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t s = (cudaStream_t)stream;
   const int rows = batch * rows_per_seq;
-  CK(pgemm(d.dtype, fused, H, rows, dr->w_kv_all, W, H, Epi{EPI_F32, ws->f32buf, W}, ws->gs, ws->status, s));
-  CK(inject_write(d.dtype, ws->f32buf, batch, rows_per_seq, d.n_layers, d.n_kv_heads, d.head_dim, dc->k, dc->v,
-                  dc->layer_stride, dc->seq_stride, dc->head_stride, dc->capacity, dc->len, n_pend, dc->rope,
-                  ws->status, s));
+  if (d.dtype != DFLASH_BF16) {
+    CK(gemm_f32(fused, H, rows, dr->w_kv_all, W, H, Epi{EPI_F32, ws->f32buf, W}, s));
+    CK(inject_write(d.dtype, ws->f32buf, batch, rows_per_seq, d.n_layers, d.n_kv_heads, d.head_dim, dc->k, dc->v,
+                    dc->layer_stride, dc->seq_stride, dc->head_stride, dc->capacity, dc->len, n_pend, dc->rope,
+                    ws->status, s));
+  } else {
+    REQ(d.head_dim == 128);
+    CK(gemm_b16(fused, H, rows, dr->w_kv_all, W, H, epi_cache(GE_INJECT, nullptr, 0, dc, 0, 0, rows_per_seq, n_pend), ws,
+                s));
+  }
   CK(advance_len(dc->len, n_pend, batch, s));
   return DFLASH_OK;
 }
@@ -475,13 +557,8 @@ int dflash_draft_block(const dflash_draft* dr, const dflash_target* tg, const in
   const int rows = batch * block, H = d.hidden;
   CK(embed(d.dtype, tg->embed, d.vocab, H, nullptr, anchor, dr->mask_id, batch, block, 1, draft_tokens, ws->x,
            ws->status, s));
-  for (int l = 0; l < d.n_layers; ++l) {
-    int rc = layer_forward(d, dr->layers[l], dc, l, batch, block, 0, ws, s);
-    if (rc != DFLASH_OK) return rc;
-  }
-  CK(rmsnorm(d.dtype, ws->x, dr->final_norm, ws->xn, rows, H, d.rms_eps, s));
-  CK(pgemm(d.dtype, ws->xn, H, rows, tg->lm_head, d.vocab, H, Epi{EPI_F32, ws->logits, d.vocab}, ws->gs, ws->status,
-          s));
+  int rc = decoder_stack(d, dr->layers, dc, batch, block, 0, nullptr, nullptr, dr->final_norm, tg->lm_head, ws, s);
+  if (rc != DFLASH_OK) return rc;
   CK(argmax(ws->logits, rows, d.vocab, draft_tokens, nullptr, block, ws->status, s));
   return DFLASH_OK;
 }
@@ -512,10 +589,15 @@ int dflash_teacher_force(int32_t* draft_tokens, int32_t batch, int32_t block, co
 // ------------------------------------------------------------------ building blocks
 int dflash_linear(int32_t dtype, const void* x, const void* w, float* y, int32_t rows, int32_t M, int32_t K,
                   dflash_workspace* ws, dflash_stream_t stream) {
-  REQ(x && w && y && ws && rows > 0 && rows <= kMaxRows && M > 0 && K > 0);
+  REQ(x && w && y && ws && rows > 0 && rows <= kMaxRows && rows <= ws->max_rows && M > 0 && K > 0);
   REQ(dtype == DFLASH_F32 || dtype == DFLASH_BF16);
   if (!gemm_shape_ok(dtype, M, K)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
-  CK(pgemm(dtype, x, K, rows, w, M, K, Epi{EPI_F32, y, M}, ws->gs, ws->status, (cudaStream_t)stream));
+  cudaStream_t s = (cudaStream_t)stream;
+  if (dtype != DFLASH_BF16) {
+    CK(gemm_f32(x, K, rows, w, M, K, Epi{EPI_F32, y, M}, s));
+    return DFLASH_OK;
+  }
+  CK(gemm_b16(x, K, rows, w, M, K, epi_of(GE_F32, y, M), ws, s));
   return DFLASH_OK;
 }
 

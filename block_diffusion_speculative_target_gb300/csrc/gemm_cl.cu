@@ -1,0 +1,374 @@
+// Weight-streaming GEMM on the tcgen05 tensor cores with cluster split-K.
+//
+//   y[n][m] = sum_k x[n][k] * w[m][k]        w: [M][K] bf16, x: [rows][K] bf16
+//
+// Swap-AB: a 128-row weight tile is the MMA's A operand, the 1..128 tokens
+// the B operand (rows past `rows` are zero-filled by TMA), the fp32
+// accumulator lives in TMEM.  Decode-sized products have few 128-row tiles,
+// so K is split S ways (S depends only on M, K and the SM count) and the S
+// CTAs that share a tile form one thread-block cluster.  Each CTA streams its
+// K-slice of weights through a TMA ring with an evict-first L2 policy; at the
+// end it parks its partial tile in its own shared memory (the drained ring),
+// the cluster synchronises once, and CTA r reduces rows r, r+S, ... by reading
+// the S partials over distributed shared memory in split order.  The result
+// is deterministic and independent of the token count; no partial sum goes
+// through global memory.
+//
+// Roles (128 threads): warp 0 lane 0 issues TMA (weights first: they do not
+// depend on the previous kernel), warp 1 lane 0 issues MMAs, warp 2 owns TMEM,
+// all four warps run the epilogue (warp w reads TMEM lanes 32w.., i.e. output
+// features m0 + 32w + lane).
+//
+// Epilogues: f32 store, f32 residual add, bf16 store, SwiGLU on interleaved
+// gate/up rows, and QKV / drafter-KV with rotate-half RoPE and the KV-cache
+// write at each row's position.
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dfl {
+
+constexpr uint64_t kGemmWaitNs = 500000000ull;  // 500 ms per wait
+
+template <int BN, int STAGES>
+struct ClCfg {
+  static constexpr int BM = 128, BK = 64;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+  static constexpr int RED_BYTES = BN * BM * 4;  // partial tile, aliases the ring
+  static constexpr int RING = STAGES * STAGE_BYTES;
+  static constexpr int SMEM = (RING > RED_BYTES ? RING : RED_BYTES) + 1024 + 256;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Final value y of output (n, m): apply the epilogue.  `partner` is y[n][m^1]
+// (SwiGLU) or y[n][m^64] within the head (RoPE).
+__device__ __forceinline__ void gemm_epi(const GemmEpi& e, int n, int m, float v, float partner, int* status) {
+  switch (e.kind) {
+    case GE_F32:
+      reinterpret_cast<float*>(e.out)[(size_t)n * e.ldo + m] = v;
+      break;
+    case GE_RESID:
+      reinterpret_cast<float*>(e.out)[(size_t)n * e.ldo + m] += v;
+      break;
+    case GE_STORE:
+      reinterpret_cast<bf16*>(e.out)[(size_t)n * e.ldo + m] = __float2bfloat16_rn(v);
+      break;
+    case GE_SWIGLU:
+      if ((m & 1) == 0)
+        reinterpret_cast<bf16*>(e.out)[(size_t)n * e.ldo + (m >> 1)] = __float2bfloat16_rn(silu_f(v) * partner);
+      break;
+    case GE_QKV:
+    case GE_INJECT: {
+      const int t = m >> 7, ml = m & 127;
+      int kind, h, layer = 0;  // kind: 0 q, 1 k, 2 v
+      if (e.kind == GE_QKV) {
+        kind = t < e.nq ? 0 : (t < e.nq + e.nkv ? 1 : 2);
+        h = kind == 0 ? t : (kind == 1 ? t - e.nq : t - e.nq - e.nkv);
+      } else {
+        layer = t / (2 * e.nkv);
+        const int rem = t % (2 * e.nkv);
+        kind = rem < e.nkv ? 1 : 2;
+        h = rem % e.nkv;
+      }
+      const int b = n / e.rows_per_seq, jj = n % e.rows_per_seq;
+      if (e.kind == GE_INJECT && jj >= e.n_pend[b]) break;
+      const int pos = e.len[b] + jj;
+      float r = v;
+      if (kind != 2) {
+        const float2 cs = pos < e.capacity ? e.rope[(size_t)pos * 64 + (ml & 63)] : make_float2(1.f, 0.f);
+        r = ml < 64 ? v * cs.x - partner * cs.y : v * cs.x + partner * cs.y;
+      }
+      if (kind == 0) {
+        reinterpret_cast<bf16*>(e.out)[((size_t)n * e.nq + h) * 128 + ml] = __float2bfloat16_rn(r);
+        break;
+      }
+      if (pos >= e.capacity) {
+        set_status(status, DFLASH_STATUS_CAPACITY);
+        break;
+      }
+      bf16* dst = reinterpret_cast<bf16*>(kind == 1 ? e.kc : e.vc);
+      dst[(size_t)layer * e.layer_stride + (size_t)b * e.seq_stride + (size_t)h * e.head_stride + (size_t)pos * 128 +
+          ml] = __float2bfloat16_rn(r);
+      break;
+    }
+  }
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(128)
+    gemm_cl_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const GemmEpi epi,
+                   const int rows, const int K, const int S, int* status) {
+  using C = ClCfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * C::A_BYTES;
+  float* red = reinterpret_cast<float*>(smem);  // [BN][128] partial tile after the main loop
+  uint8_t* tail = smem + (C::RING > C::RED_BYTES ? C::RING : C::RED_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tail);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accb = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = (int)cluster_rank();  // split index
+  const int tile = blockIdx.y;
+  const int KB = K / C::BK;
+  const int kb0 = (int)((long long)r * KB / S), kb1 = (int)((long long)(r + 1) * KB / S);
+  const int nkb = kb1 - kb0;
+  const int m0 = tile * C::BM;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(accb, 1);
+    flags[0] = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch();
+
+  int issued = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const int pre = nkb < STAGES ? nkb : STAGES;
+      for (int i = 0; i < pre; ++i) {  // weights first: independent of the previous kernel
+        mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+        tma_load_2d_hint(sA + i * C::A_BYTES, &tmW, &full[i], (kb0 + i) * C::BK, m0, pol);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * C::B_BYTES, &tmX, &full[i], (kb0 + i) * C::BK, 0);
+      issued = pre;
+      for (int kb = pre; kb < nkb; ++kb) {
+        const int s = kb % STAGES;
+        if (!mbar_wait(&empty[s], (uint32_t)((kb / STAGES) - 1) & 1u, kGemmWaitNs) || flags[0]) {
+          flags[0] = 1;
+          set_status(status, DFLASH_STATUS_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        tma_load_2d_hint(sA + s * C::A_BYTES, &tmW, &full[s], (kb0 + kb) * C::BK, m0, pol);
+        tma_load_2d(sB + s * C::B_BYTES, &tmX, &full[s], (kb0 + kb) * C::BK, 0);
+        issued = kb + 1;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(C::BM, BN);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % STAGES;
+        if (!mbar_wait(&full[s], (uint32_t)(kb / STAGES) & 1u, kGemmWaitNs)) {
+          flags[0] = 1;
+          set_status(status, DFLASH_STATUS_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint64_t da = smem_desc_sw128(sA + s * C::A_BYTES);
+        const uint64_t db = smem_desc_sw128(sB + s * C::B_BYTES);
+#pragma unroll
+        for (int k = 0; k < C::BK / 16; ++k) tc_mma_f16(tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+        tc_commit(&empty[s]);
+      }
+      tc_commit(accb);
+    }
+    __syncwarp();
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  if (threadIdx.x == 0 && !mbar_wait(accb, 0, kGemmWaitNs)) {
+    flags[0] = 1;
+    set_status(status, DFLASH_STATUS_TIMEOUT);
+  }
+  __syncthreads();
+  // Drain: after a time-out, wait (bounded) for loads still in flight before
+  // the ring is reused or released.
+  if (flags[0] && warp == 0 && lane == 0) {
+    const int first = issued > STAGES ? issued - STAGES : 0;
+    for (int i = first; i < issued; ++i) mbar_wait(&full[i % STAGES], (uint32_t)(i / STAGES) & 1u, kGemmWaitNs / 4);
+  }
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();
+  const int ml = warp * 32 + lane;
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  // park the partial tile: red[n][ml]
+#pragma unroll 1
+  for (int c = 0; c < BN / 16; ++c) {
+    if (c * 16 >= rows) break;  // uniform
+    float v[16];
+    tmem_ld16(trow + c * 16, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) red[(c * 16 + i) * C::BM + ml] = flags[0] ? 0.f : v[i];
+  }
+  tc_fence_before();
+  cluster_sync();  // every partial of the tile is in shared memory
+  const bool rope = epi.kind == GE_QKV || epi.kind == GE_INJECT;
+  const uint32_t red_local = smem_u32(red);
+  for (int n = r; n < rows; n += S) {
+    float acc = 0.f, pacc = 0.f;
+    const uint32_t off = (uint32_t)((n * C::BM + ml) * 4);
+    const uint32_t poff = (uint32_t)((n * C::BM + (ml ^ 64)) * 4);
+    for (int cc = 0; cc < S; ++cc) {
+      const uint32_t base = dsmem_addr(red_local, (uint32_t)cc);
+      acc += ld_dsmem(base + off);
+      if (rope) pacc += ld_dsmem(base + poff);
+    }
+    const float partner = rope ? pacc : __shfl_xor_sync(0xffffffffu, acc, 1);
+    if (!flags[0]) gemm_epi(epi, n, m0 + ml, acc, partner, status);
+  }
+  cluster_sync();  // no CTA leaves while its partial may still be read
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*PFN_encodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                      const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                      CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static PFN_encodeTiled_t encode_fn() {
+  static PFN_encodeTiled_t fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiled_t>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [outer][inner] matrix with row stride `ld`
+// elements, 128-byte swizzled boxes of box_inner x box_outer.
+static bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                     uint32_t box_inner, uint32_t box_outer) {
+  PFN_encodeTiled_t fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+bool gemm_shape_ok(int dtype, int M, int K) {
+  if (dtype != DFLASH_BF16) return M > 0 && K > 0;
+  return M > 0 && K > 0 && M % 128 == 0 && K % 64 == 0;
+}
+
+// Split count for an [M x K] weight: enough clusters to cover two CTAs per SM,
+// at most 8 (portable cluster size), at least 4 k-blocks per CTA.
+int gemm_splits(int M, int K) {
+  const int tiles = M / 128, KB = K / 64;
+  const int slots = 2 * num_sms();
+  int s = tiles >= slots ? 1 : slots / tiles;
+  if (s > 8) s = 8;
+  if (s > KB / 4) s = KB / 4;
+  return s < 1 ? 1 : s;
+}
+
+template <int BN, int STAGES>
+static cudaError_t launch_cl(const CUtensorMap& tw, const CUtensorMap& tx, const GemmEpi& epi, int rows, int M, int K,
+                             int S, int* status, cudaStream_t s) {
+  using C = ClCfg<BN, STAGES>;
+  static bool set = false;
+  if (!set) {
+    DFL_RET(cudaFuncSetAttribute(gemm_cl_kernel<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+    set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S, M / 128, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = S;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, gemm_cl_kernel<BN, STAGES>, tw, tx, epi, rows, K, S, status);
+}
+
+cudaError_t gemm_bf16(const void* X, int ldx, int rows, const void* W, int M, int K, const GemmEpi& epi, int* status,
+                      cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (rows > kMaxRows || !gemm_shape_ok(DFLASH_BF16, M, K)) return cudaErrorInvalidValue;
+  if ((epi.kind == GE_QKV || epi.kind == GE_INJECT) && (!epi.len || !epi.rope || epi.rows_per_seq <= 0))
+    return cudaErrorInvalidValue;
+  const int S = gemm_splits(M, K);
+  const int bn = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
+  CUtensorMap tw, tx;
+  if (!make_map(&tw, W, (uint64_t)K, (uint64_t)M, (uint64_t)K, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&tx, X, (uint64_t)K, (uint64_t)rows, (uint64_t)ldx, 64, (uint32_t)bn)) return cudaErrorInvalidValue;
+  switch (bn) {
+    case 16: return launch_cl<16, 6>(tw, tx, epi, rows, M, K, S, status, s);
+    case 32: return launch_cl<32, 5>(tw, tx, epi, rows, M, K, S, status, s);
+    case 64: return launch_cl<64, 4>(tw, tx, epi, rows, M, K, S, status, s);
+    default: return launch_cl<128, 3>(tw, tx, epi, rows, M, K, S, status, s);
+  }
+}
+
+}  // namespace dfl

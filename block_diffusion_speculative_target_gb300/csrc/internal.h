@@ -1,5 +1,6 @@
 // Internal launcher interface between the C-ABI layer (api.cu) and the kernels.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -9,7 +10,7 @@
 
 namespace dfl {
 
-// GEMM epilogues: y[n][m] = sum_k x[n][k] w[m][k], then
+// fp32 GEMM epilogues: y[n][m] = sum_k x[n][k] w[m][k], then
 enum EpiKind {
   EPI_F32 = 0,     // out f32 [n][ldo]            = y
   EPI_STORE = 1,   // out T   [n][ldo]            = T(y)
@@ -23,16 +24,40 @@ struct Epi {
   int ldo;
 };
 
-// Split-K scratch for the tensor-core GEMM.
-struct GemmScratch {
-  float* part;       // partial sums
-  size_t part_elems; // capacity in floats
-  int* tickets;      // per-tile arrival counters (kept at 0 between launches)
-  int n_tickets;
-};
-
 // Maximum rows (tokens) one GEMM call handles.
 constexpr int kMaxRows = 128;
+
+// ------------------------------------------------------------------ bf16 GEMM
+// Epilogues of the tensor-core weight product y[n][m] = sum_k x[n][k] w[m][k]:
+enum GemmEpiKind {
+  GE_F32 = 0,     // out f32 [rows][ldo] = y
+  GE_RESID = 1,   // out f32 [rows][ldo] += y  (residual stream)
+  GE_STORE = 2,   // out bf16 [rows][ldo] = y
+  GE_SWIGLU = 3,  // out bf16 [rows][ldo], column m/2 = silu(y[m]) * y[m+1] (gate/up rows interleaved)
+  GE_QKV = 4,     // 128-row tile t = head t of q|k|v: RoPE on q/k; q -> out [rows][nq][128], k/v -> cache
+  GE_INJECT = 5,  // tile t = drafter layer t/(2 nkv), k or v head: RoPE on k; rows j < n_pend[b] -> cache
+};
+
+struct GemmEpi {
+  int kind;
+  void* out;
+  int ldo;
+  // GE_QKV / GE_INJECT: row n = b * rows_per_seq + j sits at position len[b] + j
+  int nq, nkv, rows_per_seq, capacity;
+  const int32_t* len;
+  const float2* rope;      // [capacity][64] cos, sin
+  const int32_t* n_pend;   // GE_INJECT
+  void* kc;
+  void* vc;
+  size_t layer_stride, seq_stride, head_stride;
+};
+
+// bf16 weight product on tcgen05 with cluster split-K (M % 128 == 0, K % 64 == 0, rows <= 128).
+cudaError_t gemm_bf16(const void* X, int ldx, int rows, const void* W, int M, int K, const GemmEpi& epi, int* status,
+                      cudaStream_t s);
+// K splits (cluster size) for an [M x K] weight: depends on M, K and the SM count only.
+int gemm_splits(int M, int K);
+
 // Fixed attention chunk length (positions); chunk boundaries sit at multiples of it.
 constexpr int kAttnChunk = 256;
 
@@ -66,10 +91,10 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 void count_launch(int n = 1);
 long long launch_count();
 
-cudaError_t gemm(int dtype, const void* X, int ldx, int rows, const void* W, int M, int K, const Epi& epi,
-                 const GemmScratch& scr, int* status, cudaStream_t s);
-// Number of K splits the bf16 GEMM uses for an [M x K] weight (depends on M, K and the GPU only).
-int gemm_splits(int M, int K);
+// float32 weight product on the CUDA cores (fp32 configuration).
+cudaError_t gemm_simt(const float* X, int ldx, int rows, const float* W, int M, int K, const Epi& epi,
+                      cudaStream_t s);
+// Shapes the bf16 tensor-core path accepts: M % 128 == 0, K % 64 == 0.
 bool gemm_shape_ok(int dtype, int M, int K);
 
 // Row-wise RMSNorm: y = T(x * 1/sqrt(mean(x^2)+eps) * g).
