@@ -23,7 +23,19 @@ struct dflash_cache {
   float2* rope;
   size_t layer_stride, seq_stride, head_stride;  // elements
   bool owns;
+  bool has_maps;          // bf16, head_dim 128: TMA maps over the whole allocation
+  CUtensorMap tk, tv;
+  int32_t total_batch;    // sequences of the allocation (views share it)
+  int32_t seq_base;       // first sequence of this view
 };
+
+static KvMaps kv_maps(const dflash_cache* c, int layer) {
+  KvMaps m;
+  m.k = c->tk;
+  m.v = c->tv;
+  m.row0 = ((long long)layer * c->total_batch + c->seq_base) * c->n_kv * c->capacity;
+  return m;
+}
 
 struct dflash_workspace {
   int32_t max_rows, max_ctx;
@@ -126,6 +138,18 @@ int dflash_cache_alloc(const dflash_model_desc* d, int32_t n_layers, int32_t bat
     return DFLASH_ERR_OOM;
   }
   cudaMemset(c->len, 0, sizeof(int32_t) * batch);
+  cudaMemset(c->k, 0, bytes);  // every position holds a finite value from the start
+  cudaMemset(c->v, 0, bytes);
+  c->total_batch = batch;
+  c->seq_base = 0;
+  c->has_maps = false;
+  if (d->dtype == DFLASH_BF16 && d->head_dim == 128) {
+    if (!make_kv_maps(c->k, c->v, (long long)n_layers * batch * d->n_kv_heads * capacity, &c->tk, &c->tv)) {
+      dflash_cache_free(c);
+      return DFLASH_ERR_CUDA;
+    }
+    c->has_maps = true;
+  }
   // RoPE table in double precision: angle = pos * theta^(-2i/d)
   std::vector<float2> tab((size_t)capacity * half);
   for (int i = 0; i < half; ++i) {
@@ -150,6 +174,7 @@ int dflash_cache_view(dflash_cache* c, int32_t seq_begin, int32_t seq_count, dfl
   v->v = c->v + (size_t)seq_begin * c->seq_stride * c->elem;
   v->len = c->len + seq_begin;
   v->batch = seq_count;
+  v->seq_base = c->seq_base + seq_begin;
   v->owns = false;
   *out = v;
   return DFLASH_OK;
@@ -419,7 +444,7 @@ static int layer_forward_f32(const dflash_model_desc& d, const dflash_layer_w& w
   CK(rope_qkv(dt, ws->f32buf, batch, n, nq, nkv, hd, ws->q, kc, vc, c->seq_stride, c->head_stride, c->capacity,
               c->len, c->rope, ws->status, s));
   CK(attention(dt, ws->q, batch, n, nq, nkv, hd, causal, kc, vc, c->seq_stride, c->head_stride, c->capacity, c->len,
-               ws->as, ws->attn, ws->status, s));
+               nullptr, ws->as, ws->attn, ws->status, s));
   CK(gemm_f32(ws->attn, nq * hd, rows, w.wo, H, nq * hd, Epi{EPI_RESID, ws->x, H}, s));
   CK(rmsnorm(dt, ws->x, w.ffn_norm, ws->xn, rows, H, d.rms_eps, s));
   CK(gemm_f32(ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, Epi{EPI_SWIGLU, ws->act, d.ffn}, s));
@@ -459,8 +484,9 @@ static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layer
     uint8_t* vc = c->v + (size_t)l * c->layer_stride * c->elem;
     CK(rmsnorm(d.dtype, ws->x, w.attn_norm, ws->xn, rows, H, d.rms_eps, s));
     CK(gemm_b16(ws->xn, H, rows, w.wqkv, qkvw, H, epi_cache(GE_QKV, ws->q, nq * hd, c, l, nq, n, nullptr), ws, s));
+    const KvMaps maps = kv_maps(c, l);
     CK(attention(d.dtype, ws->q, batch, n, nq, nkv, hd, causal, kc, vc, c->seq_stride, c->head_stride, c->capacity,
-                 c->len, ws->as, ws->attn, ws->status, s));
+                 c->len, &maps, ws->as, ws->attn, ws->status, s));
     CK(gemm_b16(ws->attn, nq * hd, rows, w.wo, H, nq * hd, epi_of(GE_RESID, ws->x, H), ws, s));
     CK(rmsnorm(d.dtype, ws->x, w.ffn_norm, ws->xn, rows, H, d.rms_eps, s));
     CK(gemm_b16(ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, epi_of(GE_SWIGLU, ws->act, d.ffn), ws, s));
@@ -623,8 +649,10 @@ int dflash_attention(const dflash_model_desc* d, const void* q, int32_t batch, i
   if (!desc_shapes_ok(d)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
   const uint8_t* kc = c->k + (size_t)layer * c->layer_stride * c->elem;
   const uint8_t* vc = c->v + (size_t)layer * c->layer_stride * c->elem;
+  const KvMaps maps = kv_maps(c, layer);
   CK(attention(d->dtype, q, batch, n, d->n_q_heads, d->n_kv_heads, d->head_dim, causal ? 1 : 0, kc, vc,
-               c->seq_stride, c->head_stride, c->capacity, c->len, ws->as, out, ws->status, (cudaStream_t)stream));
+               c->seq_stride, c->head_stride, c->capacity, c->len, c->has_maps ? &maps : nullptr, ws->as, out,
+               ws->status, (cudaStream_t)stream));
   return DFLASH_OK;
 }
 

@@ -11,9 +11,8 @@
 // injected context plus the whole block).
 //
 // bf16 path (head_dim 128): one warp per query head of the GQA group, 16 block
-// rows per warp, QK^T and PV on mma.sync m16n8k16 with fp32 accumulation;
-// K/V sub-tiles of 64 keys double-buffered in shared memory (cp.async,
-// XOR-swizzled 16-byte chunks so ldmatrix is conflict-free).
+// rows per warp, QK^T and PV on mma.sync m16n8k16 with fp32 accumulation; the
+// chunk's keys and values arrive by TMA in one go (see attn_tma_kernel).
 // fp32 path: CUDA-core dot products, one CTA per (chunk, head, row).
 #include "common.cuh"
 #include "internal.h"
@@ -21,17 +20,26 @@
 namespace dfl {
 
 constexpr int kHD = 128;
-constexpr int kKT = 64;  // keys per shared-memory sub-tile
-constexpr int kAttnSmem = 2 * 2 * kKT * kHD * 2;  // 2 buffers x (K + V) bf16
+constexpr int kKT = 64;  // keys per sub-tile of the online softmax
+
+// bf16, whole 256-position chunk per CTA loaded by TMA (2-D maps over the
+// cache, 128-byte swizzle): K and V of the chunk land in shared memory as
+// [d-half][key][128 B] with the 16-byte chunk index XOR-ed by key % 8, so the
+// ldmatrix reads below are conflict-free.  Two mbarriers split the chunk into
+// keys 0..127 and 128..255 so math on the first half overlaps the second
+// half's transfer.  kTmaWaitNs bounds every wait.
+constexpr uint64_t kTmaWaitNs = 500000000ull;
+constexpr int kAttnTmaSmem = 4 * 256 * 128 + 1024 + 64;  // K/V x d-half x 256 keys x 128 B
 
 template <int G>
 __global__ void __launch_bounds__(G * 32)
-    attn_bf16_kernel(const bf16* __restrict__ q, int n, int nq, int causal, const bf16* __restrict__ kc,
-                     const bf16* __restrict__ vc, size_t seq_stride, size_t head_stride, int capacity,
-                     const int32_t* __restrict__ len, float* __restrict__ part_o, float* __restrict__ part_ml,
-                     int nchunk, float scale_log2) {
-  constexpr int NT = G * 32;
-  extern __shared__ __align__(128) uint8_t smem[];
+    attn_tma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const bf16* __restrict__ q, int n, int nq, int causal, long long row0, int nkv, int capacity,
+                    const int32_t* __restrict__ len, float* __restrict__ part_o, float* __restrict__ part_ml,
+                    int nchunk, float scale_log2, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 4 * 256 * 128);
   const int c = blockIdx.x, hk = blockIdx.y;
   const int nrb = (n + 15) >> 4;
   const int b = blockIdx.z / nrb, rb = blockIdx.z % nrb;
@@ -46,12 +54,25 @@ __global__ void __launch_bounds__(G * 32)
   const int k_begin = c * kAttnChunk;
   if (k_begin >= kmax) return;
   const int k_end = min(k_begin + kAttnChunk, kmax);
+  const int nhalf = (k_end - k_begin) > 128 ? 2 : 1;
+  const uint32_t sbase = smem_u32(smem);
+  // regions: K d-half 0, K d-half 1, V d-half 0, V d-half 1; each [256 keys][128 B]
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_barrier_init();
+    const int row = (int)(row0 + ((long long)b * nkv + hk) * capacity + k_begin);
+    for (int kh = 0; kh < nhalf; ++kh) {
+      mbar_arrive_expect_tx(&bar[kh], 4 * 128 * 128);
+      for (int reg = 0; reg < 4; ++reg) {
+        const CUtensorMap* map = reg < 2 ? &tmK : &tmV;
+        tma_load_2d(smem + reg * 256 * 128 + kh * 128 * 128, map, &bar[kh], (reg & 1) * 64, row + kh * 128);
+      }
+    }
+  }
   const int i0 = rb * 16 + g, i1 = i0 + 8;
   const int lim0 = min(causal ? P + i0 + 1 : P + n, k_end);
   const int lim1 = min(causal ? P + i1 + 1 : P + n, k_end);
-
-  const bf16* kbase = kc + (size_t)b * seq_stride + (size_t)hk * head_stride;
-  const bf16* vbase = vc + (size_t)b * seq_stride + (size_t)hk * head_stride;
 
   uint32_t qa[8][4];
   {
@@ -67,59 +88,48 @@ __global__ void __launch_bounds__(G * 32)
       qa[kk][3] = v1 ? *reinterpret_cast<const uint32_t*>(q1 + col + 8) : 0u;
     }
   }
+  __syncthreads();  // barriers initialised before anyone waits on them
   float o[16][4];
 #pragma unroll
   for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float mr0 = -INFINITY, mr1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
   const int nsub = (k_end - k_begin + kKT - 1) / kKT;
-  const uint32_t sbase = smem_u32(smem);
-  auto load = [&](int sub, int buf) {
-    const int kb = k_begin + sub * kKT;
-    const uint32_t ks = sbase + buf * (2 * kKT * kHD * 2);
-    const uint32_t vs = ks + kKT * kHD * 2;
-    for (int i = threadIdx.x; i < kKT * 16; i += NT) {
-      const int key = i >> 4, ch = i & 15;
-      const int gk = kb + key;
-      const bool valid = gk < k_end;
-      const size_t off = (size_t)(valid ? gk : k_begin) * kHD + ch * 8;
-      const uint32_t dst = key * 256 + ((ch ^ (key & 7)) << 4);
-      cp_async16_zfill(ks + dst, kbase + off, valid);
-      cp_async16_zfill(vs + dst, vbase + off, valid);
-    }
-    cp_async_commit();
-  };
-
-  load(0, 0);
+  const int mi = lane >> 3, rr = lane & 7;
+  bool ok = true;
+  const int valid = k_end - k_begin;  // keys of this chunk inside the cache's visible range
   for (int sub = 0; sub < nsub; ++sub) {
-    if (sub + 1 < nsub) {
-      load(sub + 1, (sub + 1) & 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    if (sub == 0 || sub == 2) {
+      const int kh = sub >> 1;
+      ok = mbar_wait(&bar[kh], 0, kTmaWaitNs) && ok;
+      // Rows past `valid` carry whatever the cache holds there; their weights
+      // are zero, so clear their values (0 * NaN would poison the sum).
+      const int z0 = valid > kh * 128 ? valid : kh * 128, z1 = (kh + 1) * 128;
+      if (z0 < z1) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < (z1 - z0) * 16; i += G * 32) {
+          const int key = z0 + (i >> 4), part = i & 15;  // 16 x 16 B per key row over both d-halves
+          uint4* dst = reinterpret_cast<uint4*>(smem + (2 + (part >> 3)) * 256 * 128 + key * 128 + (part & 7) * 16);
+          *dst = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncthreads();
+      }
     }
-    __syncthreads();
-    const uint32_t ks = sbase + (sub & 1) * (2 * kKT * kHD * 2);
-    const uint32_t vs = ks + kKT * kHD * 2;
     const int kb = k_begin + sub * kKT;
-
     float s[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-    const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
 #pragma unroll
       for (int kp = 0; kp < 4; ++kp) {
         uint32_t r[4];
-        const int key = j * 8 + rr;
-        const int ch = kp * 4 + mi;
-        ldmatrix_x4(r, ks + key * 256 + ((ch ^ (key & 7)) << 4));
+        const int key = sub * kKT + j * 8 + rr;
+        const int ch = kp * 4 + mi;  // 16-byte chunk of d (0..15)
+        ldmatrix_x4(r, sbase + (ch >> 3) * 256 * 128 + key * 128 + (((ch & 7) ^ (key & 7)) << 4));
         mma_bf16_16816(s[j], qa[2 * kp], r[0], r[1]);
         mma_bf16_16816(s[j], qa[2 * kp + 1], r[2], r[3]);
       }
     }
-    // mask, running max
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -162,7 +172,6 @@ __global__ void __launch_bounds__(G * 32)
       o[j][2] *= al1;
       o[j][3] *= al1;
     }
-    // O += P V
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       uint32_t pa[4];
@@ -173,14 +182,18 @@ __global__ void __launch_bounds__(G * 32)
 #pragma unroll
       for (int jp = 0; jp < 8; ++jp) {
         uint32_t r[4];
-        const int key = kk * 16 + (mi & 1) * 8 + rr;
+        const int key = sub * kKT + kk * 16 + (mi & 1) * 8 + rr;
         const int ch = 2 * jp + (mi >> 1);
-        ldmatrix_x4_trans(r, vs + key * 256 + ((ch ^ (key & 7)) << 4));
+        ldmatrix_x4_trans(r, sbase + 2 * 256 * 128 + (ch >> 3) * 256 * 128 + key * 128 + (((ch & 7) ^ (key & 7)) << 4));
         mma_bf16_16816(o[2 * jp], pa, r[0], r[1]);
         mma_bf16_16816(o[2 * jp + 1], pa, r[2], r[3]);
       }
     }
-    __syncthreads();
+  }
+  if (!ok) {
+    if (lane == 0) set_status(status, DFLASH_STATUS_TIMEOUT);
+    if (threadIdx.x == 0)  // bounded drain of copies still in flight
+      for (int kh = 0; kh < nhalf; ++kh) mbar_wait(&bar[kh], 0, kTmaWaitNs / 4);
   }
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -260,59 +273,119 @@ __global__ void __launch_bounds__(NT)
   }
 }
 
+// Merge the chunk partials of one (row, query head): weights w_c =
+// 2^(m_c - max m) staged in shared memory, then out[d] = sum_c w_c o_c[d] /
+// sum_c w_c l_c.  256 threads: thread (d, half) sums one half of the chunks
+// (loads unrolled for memory-level parallelism); the halves are added in a
+// fixed order, so the result does not depend on other rows.
+constexpr int kCombineMaxChunks = 1024;
+
 template <typename T>
-__global__ void attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int n, int nq,
-                                    int hd, int causal, int capacity, const int32_t* __restrict__ len, int nchunk,
-                                    T* __restrict__ out) {
+__global__ void __launch_bounds__(256)
+    attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int n, int nq, int hd,
+                        int causal, int capacity, const int32_t* __restrict__ len, int nchunk, T* __restrict__ out) {
+  __shared__ float w[kCombineMaxChunks];
+  __shared__ float lsum[kCombineMaxChunks];
+  __shared__ float half1[kHD];
+  __shared__ float Msh, Lsh;
   const int r = blockIdx.x, hq = blockIdx.y;
   const int b = r / n, j = r % n;
   pdl_launch();
   pdl_wait();
   const int P = len[b];
   const int lim = min(causal ? P + j + 1 : P + n, capacity);
-  const int nch = (lim + kAttnChunk - 1) / kAttnChunk;
+  const int nch = min((lim + kAttnChunk - 1) / kAttnChunk, kCombineMaxChunks);
   const size_t row0 = ((size_t)r * nq + hq) * nchunk;
-  float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, part_ml[(row0 + c) * 2]);
-  float L = 0.f;
-  for (int c = 0; c < nch; ++c) {
-    const float mc = part_ml[(row0 + c) * 2];
-    if (mc != -INFINITY) L += part_ml[(row0 + c) * 2 + 1] * exp2f(mc - M);
+  for (int c = threadIdx.x; c < nch; c += blockDim.x) {
+    const float2 ml = *reinterpret_cast<const float2*>(part_ml + (row0 + c) * 2);
+    w[c] = ml.x;
+    lsum[c] = ml.y;
   }
-  const float invL = 1.0f / L;
-  for (int i = threadIdx.x; i < hd; i += blockDim.x) {
-    float acc = 0.f;
-    for (int c = 0; c < nch; ++c) {
-      const float mc = part_ml[(row0 + c) * 2];
-      if (mc != -INFINITY) acc += part_o[(row0 + c) * kHD + i] * exp2f(mc - M);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = -INFINITY;
+    for (int c = 0; c < nch; ++c) M = fmaxf(M, w[c]);
+    Msh = M;
+  }
+  __syncthreads();
+  const float M = Msh;
+  for (int c = threadIdx.x; c < nch; c += blockDim.x) w[c] = (w[c] == -INFINITY) ? 0.f : exp2f(w[c] - M);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float L = 0.f;
+    for (int c = 0; c < nch; ++c) L += w[c] * lsum[c];
+    Lsh = L;
+  }
+  const int d = threadIdx.x & 127, h = threadIdx.x >> 7;
+  const int cmid = nch / 2;
+  const int c0 = h == 0 ? 0 : cmid, c1 = h == 0 ? cmid : nch;
+  float acc = 0.f;
+  if (d < hd) {
+    const float* po = part_o + row0 * kHD + d;
+    int c = c0;
+    for (; c + 8 <= c1; c += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = po[(size_t)(c + u) * kHD];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc += w[c + u] * v[u];
     }
-    out[((size_t)r * nq + hq) * hd + i] = from_f<T>(acc * invL);
+    for (; c < c1; ++c) acc += w[c] * po[(size_t)c * kHD];
   }
+  if (h == 1) half1[d] = acc;
+  __syncthreads();
+  if (h == 0 && d < hd) out[((size_t)r * nq + hq) * hd + d] = from_f<T>((acc + half1[d]) / Lsh);
+}
+
+typedef CUresult (*PFN_encodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                      const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                      CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// 2-D maps over a whole bf16 cache viewed as [rows_total][128]: boxes of 64
+// elements (128 B, swizzled) by 128 positions.
+bool make_kv_maps(const void* k, const void* v, long long rows_total, CUtensorMap* mk, CUtensorMap* mv) {
+  static PFN_encodeTiled_t fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<PFN_encodeTiled_t>(p);
+  }
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows_total};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  for (int i = 0; i < 2; ++i)
+    if (fn(i == 0 ? mk : mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(i == 0 ? k : v), dims, strides, box,
+           es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  return true;
 }
 
 cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nkv, int hd, int causal, const void* kc,
                       const void* vc, size_t seq_stride, size_t head_stride, int capacity, const int32_t* len,
-                      const AttnScratch& sc, void* out, int* status, cudaStream_t s) {
-  (void)status;
+                      const KvMaps* maps, const AttnScratch& sc, void* out, int* status, cudaStream_t s) {
   if (batch * n <= 0) return cudaSuccess;
   const int nchunk_launch = (capacity + kAttnChunk - 1) / kAttnChunk;
-  if (nchunk_launch > sc.nchunk || hd > kHD) return cudaErrorInvalidValue;
+  if (nchunk_launch > sc.nchunk || nchunk_launch > kCombineMaxChunks || hd > kHD) return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
   if (dtype == DFLASH_BF16) {
-    if (hd != kHD) return cudaErrorInvalidValue;
+    if (hd != kHD || !maps) return cudaErrorInvalidValue;
     const int G = nq / nkv;
     const dim3 grid(nchunk_launch, nkv, batch * ((n + 15) / 16));
-#define DFL_ATTN_CASE(GG)                                                                                     \
-  case GG: {                                                                                                  \
-    static bool set = false;                                                                                  \
-    if (!set) {                                                                                               \
-      DFL_RET(cudaFuncSetAttribute(attn_bf16_kernel<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem)); \
-      set = true;                                                                                             \
-    }                                                                                                         \
-    DFL_RET(launch_pdl(attn_bf16_kernel<GG>, grid, dim3(GG * 32), kAttnSmem, s, (const bf16*)q, n, nq, causal,  \
-                       (const bf16*)kc, (const bf16*)vc, seq_stride, head_stride, capacity, len, sc.o, sc.ml,  \
-                       sc.nchunk, scale_log2));                                                                \
-    break;                                                                                                    \
+#define DFL_ATTN_CASE(GG)                                                                                      \
+  case GG: {                                                                                                   \
+    static bool set = false;                                                                                   \
+    if (!set) {                                                                                                \
+      DFL_RET(cudaFuncSetAttribute(attn_tma_kernel<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnTmaSmem)); \
+      set = true;                                                                                              \
+    }                                                                                                          \
+    DFL_RET(launch_pdl(attn_tma_kernel<GG>, grid, dim3(GG * 32), kAttnTmaSmem, s, maps->k, maps->v, (const bf16*)q, \
+                       n, nq, causal, maps->row0, nkv, capacity, len, sc.o, sc.ml, sc.nchunk, scale_log2, status));  \
+    break;                                                                                                     \
   }
     switch (G) {
       DFL_ATTN_CASE(1)
@@ -324,14 +397,14 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
         return cudaErrorInvalidValue;
     }
 #undef DFL_ATTN_CASE
-    DFL_RET(launch_pdl(attn_combine_kernel<bf16>, dim3(batch * n, nq), dim3(kHD), 0, s, sc.o, sc.ml, n, nq, hd,
+    DFL_RET(launch_pdl(attn_combine_kernel<bf16>, dim3(batch * n, nq), dim3(256), 0, s, sc.o, sc.ml, n, nq, hd,
                        causal, capacity, len, sc.nchunk, (bf16*)out));
   } else {
     const dim3 grid(nchunk_launch, nq, batch * n);
     DFL_RET(launch_pdl(attn_f32_kernel<128>, grid, dim3(128), 0, s, (const float*)q, n, nq, nkv, hd, causal,
                        (const float*)kc, (const float*)vc, seq_stride, head_stride, capacity, len, sc.o, sc.ml,
                        sc.nchunk, scale_log2));
-    DFL_RET(launch_pdl(attn_combine_kernel<float>, dim3(batch * n, nq), dim3(hd), 0, s, sc.o, sc.ml, n, nq, hd,
+    DFL_RET(launch_pdl(attn_combine_kernel<float>, dim3(batch * n, nq), dim3(256), 0, s, sc.o, sc.ml, n, nq, hd,
                        causal, capacity, len, sc.nchunk, (float*)out));
   }
   count_launch(2);

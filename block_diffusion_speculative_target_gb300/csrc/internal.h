@@ -124,9 +124,17 @@ struct AttnScratch {
   float* ml;   // [rows][nq][nchunk][2]
   int nchunk;  // chunk capacity per row
 };
+// TMA maps over a bf16 cache's keys/values viewed as [rows][128]; row0 is the
+// row of (layer, first sequence of the view, head 0, position 0).
+struct KvMaps {
+  CUtensorMap k, v;
+  long long row0;
+};
+bool make_kv_maps(const void* k, const void* v, long long rows_total, CUtensorMap* mk, CUtensorMap* mv);
 cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nkv, int hd, int causal,
                       const void* kc, const void* vc, size_t seq_stride, size_t head_stride, int capacity,
-                      const int32_t* len, const AttnScratch& sc, void* out, int* status, cudaStream_t s);
+                      const int32_t* len, const KvMaps* maps, const AttnScratch& sc, void* out, int* status,
+                      cudaStream_t s);
 
 // Greedy token and top-2 gap per row.  If skip_first_of (>0), rows with
 // (r % skip_first_of) == 0 are not written to argmax_out.
