@@ -48,6 +48,7 @@ struct dflash_workspace {
   void* act;
   float* logits;
   AttnScratch as;
+  ArgmaxScratch am;
   int* status;
   std::vector<void*> allocs;
 };
@@ -283,6 +284,8 @@ int dflash_workspace_alloc(const dflash_model_desc* t, const dflash_model_desc* 
       {(void**)&w->as.o, R * nq * nchunk * 128 * 4},
       {(void**)&w->as.ml, R * nq * nchunk * 2 * 4},
       {(void**)&w->status, 4},
+      {(void**)&w->am.part, R * kArgmaxSlices * 16},
+      {(void**)&w->am.tickets, R * 4},
   };
   for (auto& r : reqs) {
     void* p = nullptr;
@@ -295,6 +298,8 @@ int dflash_workspace_alloc(const dflash_model_desc* t, const dflash_model_desc* 
     w->allocs.push_back(p);
   }
   w->as.nchunk = nchunk;
+  w->am.max_rows = (int)R;
+  cudaMemset(w->am.tickets, 0, R * 4);
 
   cudaMemset(w->status, 0, 4);
   cudaMemset(w->x, 0, R * H * 4);
@@ -490,10 +495,14 @@ static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layer
     CK(gemm_b16(ws->attn, nq * hd, rows, w.wo, H, nq * hd, epi_of(GE_RESID, ws->x, H), ws, s));
     CK(rmsnorm(d.dtype, ws->x, w.ffn_norm, ws->xn, rows, H, d.rms_eps, s));
     CK(gemm_b16(ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, epi_of(GE_SWIGLU, ws->act, d.ffn), ws, s));
-    CK(gemm_b16(ws->act, d.ffn, rows, w.w_down, H, d.ffn, epi_of(GE_RESID, ws->x, H), ws, s));
-    if (hcap)
+    GemmEpi down = epi_of(GE_RESID, ws->x, H);
+    if (hcap) {
       for (int si = 0; si < 5; ++si)
-        if (capture[si] == l) CK(dfl::capture(d.dtype, ws->x, hcap, rows, H, si, s));
+        if (capture[si] == l) down.cap_mask |= 1 << si;
+      down.hcap = hcap;
+      down.cap_H = H;
+    }
+    CK(gemm_b16(ws->act, d.ffn, rows, w.w_down, H, d.ffn, down, ws, s));
   }
   CK(rmsnorm(d.dtype, ws->x, final_norm, ws->xn, rows, H, d.rms_eps, s));
   CK(gemm_b16(ws->xn, H, rows, lm_head, d.vocab, H, epi_of(GE_F32, ws->logits, d.vocab), ws, s));
@@ -519,7 +528,7 @@ int target_verify(const dflash_target* tg, const int32_t* tokens, int32_t batch,
   CK(embed(d.dtype, tg->embed, d.vocab, H, tokens, nullptr, 0, batch, n, 0, nullptr, ws->x, ws->status, s));
   int rc = decoder_stack(d, tg->layers, tc, batch, n, 1, tg->capture, hcap, tg->final_norm, tg->lm_head, ws, s);
   if (rc != DFLASH_OK) return rc;
-  CK(argmax(ws->logits, rows, d.vocab, argmax_out, top2_gap, 0, ws->status, s));
+  CK(argmax(ws->logits, rows, d.vocab, argmax_out, top2_gap, 0, ws->am, ws->status, s));
   if (commit)
     CK(commit_rows(tc->len, n_pend, anchor, argmax_out, batch, n, commit == 2, stream, stream_len, stream_cap,
                    ws->status, s));
@@ -585,7 +594,7 @@ int dflash_draft_block(const dflash_draft* dr, const dflash_target* tg, const in
            ws->status, s));
   int rc = decoder_stack(d, dr->layers, dc, batch, block, 0, nullptr, nullptr, dr->final_norm, tg->lm_head, ws, s);
   if (rc != DFLASH_OK) return rc;
-  CK(argmax(ws->logits, rows, d.vocab, draft_tokens, nullptr, block, ws->status, s));
+  CK(argmax(ws->logits, rows, d.vocab, draft_tokens, nullptr, block, ws->am, ws->status, s));
   return DFLASH_OK;
 }
 
@@ -638,7 +647,8 @@ int dflash_rmsnorm(int32_t dtype, const float* x, const void* gain, void* y, int
 int dflash_argmax(const float* logits, int32_t rows, int32_t V, int32_t* argmax_out, float* gap, dflash_workspace* ws,
                   dflash_stream_t stream) {
   REQ(logits && argmax_out && ws && rows > 0 && V > 0);
-  CK(argmax(logits, rows, V, argmax_out, gap, 0, ws->status, (cudaStream_t)stream));
+  REQ(rows <= ws->max_rows);
+  CK(argmax(logits, rows, V, argmax_out, gap, 0, ws->am, ws->status, (cudaStream_t)stream));
   return DFLASH_OK;
 }
 

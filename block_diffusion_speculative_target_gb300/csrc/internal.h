@@ -42,6 +42,9 @@ struct GemmEpi {
   int kind;
   void* out;
   int ldo;
+  // GE_RESID: bf16 copies of the new residual into hcap [rows][5 cap_H], slots in cap_mask
+  void* hcap;
+  int cap_mask, cap_H;
   // GE_QKV / GE_INJECT: row n = b * rows_per_seq + j sits at position len[b] + j
   int nq, nkv, rows_per_seq, capacity;
   const int32_t* len;
@@ -138,8 +141,14 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
 
 // Greedy token and top-2 gap per row.  If skip_first_of (>0), rows with
 // (r % skip_first_of) == 0 are not written to argmax_out.
+constexpr int kArgmaxSlices = 16;
+struct ArgmaxScratch {
+  float4* part;  // [max_rows][kArgmaxSlices] slice results
+  int* tickets;  // [max_rows], zero between launches
+  int max_rows;
+};
 cudaError_t argmax(const float* logits, int rows, int V, int32_t* argmax_out, float* gap, int skip_first_of,
-                   int* status, cudaStream_t s);
+                   const ArgmaxScratch& sc, int* status, cudaStream_t s);
 
 cudaError_t commit_rows(int32_t* len, int32_t* n_pend, int32_t* anchor, const int32_t* argmax, int batch, int n,
                         int emit, int32_t* stream, int32_t* stream_len, int stream_cap, int* status,

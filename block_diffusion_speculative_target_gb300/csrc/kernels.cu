@@ -252,16 +252,24 @@ __device__ __forceinline__ Top2 top2_merge(Top2 a, Top2 b) {
   return o;
 }
 
+// Grid (rows, kArgmaxSlices): each CTA scans one contiguous slice of a row;
+// the last CTA of the row (ticket) merges the slice results in slice order,
+// so ties resolve to the lowest index and the result is deterministic.
 template <int NT>
 __global__ void __launch_bounds__(NT) argmax_kernel(const float* __restrict__ logits, int V, int32_t* __restrict__ out,
-                                                    float* __restrict__ gap, int skip_first_of, int* status) {
+                                                    float* __restrict__ gap, int skip_first_of, float4* __restrict__ part,
+                                                    int* __restrict__ tickets, int* status) {
   __shared__ Top2 sh[NT / 32];
-  const float* row = logits + (size_t)blockIdx.x * V;
+  __shared__ int last;
+  const int row_i = blockIdx.x, sl = blockIdx.y, ns = gridDim.y;
+  const float* row = logits + (size_t)row_i * V;
   pdl_launch();
   pdl_wait();
+  const int per = (V + ns - 1) / ns;
+  const int v0 = sl * per, v1 = min(V, v0 + per);
   Top2 t{-INFINITY, -INFINITY, 0x7fffffff};
   bool bad = false;
-  for (int i = threadIdx.x; i < V; i += NT) {
+  for (int i = v0 + threadIdx.x; i < v1; i += NT) {
     const float v = row[i];
     bad |= !(fabsf(v) <= 3.0e38f);
     if (v > t.v1) {
@@ -272,7 +280,6 @@ __global__ void __launch_bounds__(NT) argmax_kernel(const float* __restrict__ lo
       t.v2 = v;
     }
   }
-  if (t.i1 == 0x7fffffff) t.i1 = 0;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     Top2 u;
@@ -289,18 +296,35 @@ __global__ void __launch_bounds__(NT) argmax_kernel(const float* __restrict__ lo
   if (threadIdx.x == 0) {
     Top2 r = sh[0];
     for (int i = 1; i < NT / 32; ++i) r = top2_merge(r, sh[i]);
-    const bool skip = skip_first_of > 0 && (blockIdx.x % skip_first_of) == 0;
-    if (!skip) out[blockIdx.x] = r.i1;
-    if (gap) gap[blockIdx.x] = r.v1 - r.v2;
+    part[(size_t)row_i * ns + sl] = make_float4(r.v1, r.v2, __int_as_float(r.i1), 0.f);
+    __threadfence();
+    last = (atomicAdd(&tickets[row_i], 1) == ns - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (last && threadIdx.x == 0) {
+    __threadfence();
+    Top2 r{-INFINITY, -INFINITY, 0x7fffffff};
+    for (int i = 0; i < ns; ++i) {
+      const float4 p = __ldcg(&part[(size_t)row_i * ns + i]);
+      r = top2_merge(r, Top2{p.x, p.y, __float_as_int(p.z)});
+    }
+    if (r.i1 == 0x7fffffff) r.i1 = 0;
+    const bool skip = skip_first_of > 0 && (row_i % skip_first_of) == 0;
+    if (!skip) out[row_i] = r.i1;
+    if (gap) gap[row_i] = r.v1 - r.v2;
+    tickets[row_i] = 0;
   }
 }
 
-cudaError_t argmax(const float* logits, int rows, int V, int32_t* out, float* gap, int skip_first_of, int* status,
-                   cudaStream_t s) {
+cudaError_t argmax(const float* logits, int rows, int V, int32_t* out, float* gap, int skip_first_of,
+                   const ArgmaxScratch& sc, int* status, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  DFL_RET(launch_pdl(argmax_kernel<1024>, dim3(rows), dim3(1024), 0, s, logits, V, out, gap, skip_first_of, status));
+  if (rows > sc.max_rows) return cudaErrorInvalidValue;
+  const int ns = V >= 16 * 1024 ? kArgmaxSlices : 1;
+  DFL_RET(launch_pdl(argmax_kernel<256>, dim3(rows, ns), dim3(256), 0, s, logits, V, out, gap, skip_first_of, sc.part,
+                     sc.tickets, status));
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 // ------------------------------------------------------------------ commit (prefill / AR)
