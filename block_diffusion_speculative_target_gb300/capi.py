@@ -17,6 +17,10 @@ from . import build as _build
 F32 = 0
 BF16 = 1
 
+ERR_INVALID_ARG = -1
+ERR_TOO_LARGE = -5
+ARGMAX_NOALLOC_MAX_ROWS = 128
+
 STATUS_CAPACITY = 1
 STATUS_NONFINITE = 2
 STATUS_TIMEOUT = 4
@@ -24,7 +28,9 @@ STATUS_BOUNDS = 8
 
 
 class DFlashError(RuntimeError):
-    pass
+    def __init__(self, msg, code=None):
+        super().__init__(msg)
+        self.code = code
 
 
 class ModelDesc(ctypes.Structure):
@@ -73,6 +79,7 @@ _SIGS = {
     "dflash_linear": (_I, [_I, _P, _P, _P, _I, _I, _I, _P, _P]),
     "dflash_rmsnorm": (_I, [_I, _P, _P, _P, _I, _I, c_float, _P]),
     "dflash_argmax": (_I, [_P, _I, _I, _P, _P, _P, _P]),
+    "dflash_argmax_noalloc": (_I, [_P, _I, _I, _P, _P, _P, _P]),
     "dflash_attention": (_I, [POINTER(ModelDesc), _P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "dflash_profile_begin": (_I, [_I]),
     "dflash_launch_count": (ctypes.c_longlong, []),
@@ -126,7 +133,7 @@ def _stream(stream=None):
 
 def _check(rc, what):
     if rc != 0:
-        raise DFlashError(f"{what}: {load().dflash_strerror(rc).decode()} ({rc})")
+        raise DFlashError(f"{what}: {load().dflash_strerror(rc).decode()} ({rc})", rc)
 
 
 # ---------------------------------------------------------------- caches / workspace
@@ -256,6 +263,11 @@ def dflash_rmsnorm(dtype, x, gain, y, rows, H, eps, stream=None):
 def dflash_argmax(logits, rows, V, argmax, gap, ws, stream=None):
     _check(load().dflash_argmax(_ptr(logits), rows, V, _ptr(argmax), _ptr(gap), ws, _stream(stream)),
            "dflash_argmax")
+
+
+def dflash_argmax_noalloc(logits, rows, V, argmax, gap, status=None, stream=None):
+    _check(load().dflash_argmax_noalloc(_ptr(logits), rows, V, _ptr(argmax), _ptr(gap), _ptr(status),
+                                        _stream(stream)), "dflash_argmax_noalloc")
 
 
 def dflash_attention(desc: ModelDesc, q, batch, n, causal, cache, layer, out, ws, stream=None):

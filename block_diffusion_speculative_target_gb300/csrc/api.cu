@@ -55,6 +55,13 @@ struct dflash_workspace {
 
 static thread_local cudaError_t g_last_cuda = cudaSuccess;
 
+namespace dfl {
+int record_cuda_error(cudaError_t e) {
+  g_last_cuda = e;
+  return DFLASH_ERR_CUDA;
+}
+}  // namespace dfl
+
 #define CK(expr)                    \
   do {                              \
     cudaError_t e_ = (expr);        \
@@ -96,6 +103,7 @@ const char* dflash_strerror(int code) {
     case DFLASH_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
     case DFLASH_ERR_CUDA: return cudaGetErrorString(g_last_cuda);
     case DFLASH_ERR_OOM: return "out of device memory";
+    case DFLASH_ERR_TOO_LARGE: return "size above the entry point's fixed maximum";
     default: return "unknown error";
   }
 }

@@ -149,6 +149,9 @@ struct ArgmaxScratch {
 };
 cudaError_t argmax(const float* logits, int rows, int V, int32_t* argmax_out, float* gap, int skip_first_of,
                    const ArgmaxScratch& sc, int* status, cudaStream_t s);
+// Stores e as the thread's last CUDA error (reported by dflash_strerror) and
+// returns DFLASH_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
 
 cudaError_t commit_rows(int32_t* len, int32_t* n_pend, int32_t* anchor, const int32_t* argmax, int batch, int n,
                         int emit, int32_t* stream, int32_t* stream_len, int stream_cap, int* status,

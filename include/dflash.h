@@ -51,6 +51,7 @@ enum {
   DFLASH_ERR_UNSUPPORTED_SHAPE = -2,
   DFLASH_ERR_CUDA = -3,
   DFLASH_ERR_OOM = -4,
+  DFLASH_ERR_TOO_LARGE = -5, /* a size above an entry point's fixed maximum */
 };
 
 /* device status bits (dflash_status) */
@@ -255,6 +256,34 @@ int dflash_rmsnorm(int32_t dtype, const float *x, const void *gain, void *y, int
 /* Greedy token and top-2 gap of float32 logits [rows][V]. */
 int dflash_argmax(const float *logits, int32_t rows, int32_t V, int32_t *argmax, float *gap,
                   dflash_workspace *ws, dflash_stream_t stream);
+/* dflash_argmax without a workspace.  Not an operation of the method (the
+ * pages have no counterpart): the same greedy token and top-2 gap of float32
+ * logits [rows][V], for callers that cannot allocate device memory.  Such
+ * callers hold no dflash_workspace, whose allocation needs both model
+ * descriptors and reserves activation buffers sized for them, and cannot add
+ * a cudaMalloc/cudaFree of their own: a sampler handed another engine's
+ * logits in a serving loop whose memory is owned by a caching allocator, or
+ * a loop where cudaFree's implicit device synchronisation would stall the
+ * pipeline.
+ *   Scratch: a fixed file-scope device array in the library (slice partials
+ *   and per-row tickets, about 33 KiB per device) for at most
+ *   DFLASH_ARGMAX_NOALLOC_MAX_ROWS rows; rows above it return
+ *   DFLASH_ERR_TOO_LARGE before any CUDA call.  The library calls no
+ *   allocator on this path.
+ *   Set-up: the first call on each device, with that device current, resolves
+ *   the array's address (cudaGetSymbolAddress, return code checked; a failure
+ *   returns DFLASH_ERR_CUDA and the next call retries).  Make that first call
+ *   before any stream capture begins.
+ *   Each call clears the rows' tickets (an asynchronous memset on `stream`)
+ *   and launches one kernel.  All calls on a device share the one array:
+ *   calls that overlap in time (other streams, other host threads) race on
+ *   it and must be serialised by the caller.
+ *   argmax [rows] int32 and gap [rows] float32 (may be NULL) are device
+ *   pointers; status (device int32, may be NULL) has DFLASH_STATUS_NONFINITE
+ *   OR-ed in when a row holds NaN/Inf. */
+#define DFLASH_ARGMAX_NOALLOC_MAX_ROWS 128
+int dflash_argmax_noalloc(const float *logits, int32_t rows, int32_t V, int32_t *argmax,
+                          float *gap, int32_t *status, dflash_stream_t stream);
 /* Attention of q [batch][n][nq][hd] (dtype, RoPE applied) against layer
  * `layer` of `cache` (positions 0 .. len[b] + n - 1, the block's own keys
  * already written at len[b] ..), causal (row j sees 0..len+j) or not (every
