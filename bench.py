@@ -36,6 +36,13 @@ import synth  # noqa: E402
 METRIC = "emitted tokens/s per step (draft block+verify) at 4K ctx; % of HBM roofline"
 UNIT = "tokens/s"
 
+# DRAM bytes (read + write) per gemm_cl_kernel launch, averaged over the 168
+# weight-product launches of one step of the 4K workload, from the ncu launch
+# list in profiles/launches__bench_qwen3-8b-4k.md.  Set to None whenever the
+# kernel changes until a new capture is taken.
+GEMM_TRAFFIC = {"workload": "qwen3-8b-4k", "bytes_per_launch": 110.98e6,
+                "source": "profiles/launches__bench_qwen3-8b-4k.md"}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -191,6 +198,11 @@ class Dist:
     def close(self):
         if self.pg:
             self.pg.destroy_process_group()
+
+
+def aggregate(dist: Dist, units: float, seconds: float) -> float:
+    """Whole-job throughput: units of all ranks / the slowest rank's time."""
+    return dist.sum(units) / dist.max(seconds)
 
 
 # ---------------------------------------------------------------------------
@@ -474,10 +486,8 @@ def run_ours(args, dist: Dist):
     ms_step = statistics.median(step_ms)
     peak, peak_kind = measured_peaks()
     step_gbs = bytes_step / (ms_step / 1e3) / 1e9
-    tot_tokens = dist.sum(tokens)
-    t_max = dist.max(total_s)
-    value = tot_tokens / t_max
-    e2e_val = dist.sum(e2e_tokens) / dist.max(e2e_s)
+    value = aggregate(dist, tokens, total_s)
+    e2e_val = aggregate(dist, e2e_tokens, e2e_s)
     tau = tokens / K
 
     cpu = None
@@ -507,10 +517,13 @@ def run_ours(args, dist: Dist):
         "stage_ms": {k: statistics.median(v) for k, v in stage_ms.items()},
         "ar_tokens_per_s": ar_tok_s,
         "roofline": {"bound": "hbm", "kernel": "gemm_cl_kernel", "achieved": gemm_gbs, "peak": peak,
-                     "unit": "GB/s", "frac": (gemm_gbs / peak) if gemm_gbs else None, "traffic": None,
+                     "unit": "GB/s", "frac": (gemm_gbs / peak) if gemm_gbs else None,
+                     "traffic": GEMM_TRAFFIC["bytes_per_launch"] if wl.name == GEMM_TRAFFIC["workload"] else None,
+                     "algorithmic_bytes_per_launch": gemm_bytes / len(chains) if chains else None,
                      "peak_kind": peak_kind,
                      "note": f"{len(chains)} weight-product launches over {PS} eager steps; achieved = weight "
-                             f"bytes of each launch / its CUDA-event duration, summed"},
+                             f"bytes of each launch / its CUDA-event duration, summed; traffic = ncu DRAM read+write "
+                             f"bytes per launch from {GEMM_TRAFFIC['source']}"},
         "clocks": clk,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(kernels_per_step * K),

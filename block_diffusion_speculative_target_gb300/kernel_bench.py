@@ -62,7 +62,7 @@ def bench_gemm(M, K, rows, iters, warmup, copies=None):
     assert capi.dflash_status(ws) == 0
     capi.dflash_workspace_free(ws)
     byt = wbytes + 2 * rows * K + 4 * rows * M
-    return {"kernel": "gemm_tc_kernel", "M": M, "K": K, "rows": rows, "ms": avg, "bytes": byt,
+    return {"kernel": "gemm_cl_kernel", "M": M, "K": K, "rows": rows, "ms": avg, "bytes": byt,
             "GBps": byt / (avg / 1e3) / 1e9, "splits_copies": copies}
 
 
@@ -90,7 +90,7 @@ def bench_attention(P, nq, nkv, n, iters, warmup, causal=1):
         capi.dflash_cache_free(c)
     capi.dflash_workspace_free(ws)
     byt = 2 * 2 * nkv * (P + n) * hd
-    return {"kernel": "attn_bf16_kernel+attn_combine_kernel", "P": P, "nq": nq, "nkv": nkv, "n": n, "ms": avg,
+    return {"kernel": "attn_tma_kernel+attn_combine_kernel", "P": P, "nq": nq, "nkv": nkv, "n": n, "ms": avg,
             "bytes": byt, "GBps": byt / (avg / 1e3) / 1e9}
 
 
