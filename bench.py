@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-METRIC = "emitted tokens/s per step (draft block+verify) at 4K ctx; % of HBM roofline"
+METRIC = "emitted tokens/s per step (draft block+verify) at 4K/36K ctx; % of HBM roofline"
 UNIT = "tokens/s"
 
 # DRAM bytes (read + write) per gemm_cl_kernel launch, averaged over the 168
@@ -210,12 +210,15 @@ def aggregate(dist: Dist, units: float, seconds: float) -> float:
 # ---------------------------------------------------------------------------
 
 
-def oracle_step_sample(wl: synth.Workload, seconds: float, tau: float, P: int, weights_dev=None, repeats=None):
+def oracle_step_sample(wl: synth.Workload, seconds: float, tau: float, P: int, weights_dev=None, repeats=None,
+                       batch=1):
     """Time the oracle on a bounded sample of one DFlash step at the workload's
-    shapes: fusion + injection of 16 rows, one drafter layer and one target
-    layer over a P-position synthetic context (16 block rows), and one LM head
-    (16 rows).  The step time is extrapolated by layer count:
-        t_step = t_fuse + t_inject + Ld*t_dlayer + L*t_tlayer + 2*t_lmhead.
+    shapes: fusion + injection of B rows, one drafter layer and one target
+    layer over a P-position synthetic context (B block rows), and one LM head
+    (B rows).  The step time is extrapolated by layer count and, for a batch,
+    by the number of sequences (the oracle runs them one after another):
+        t_step = batch * (t_fuse + t_inject + Ld*t_dlayer + L*t_tlayer + 2*t_lmhead).
+    ``tau`` is the emitted tokens per step of the whole batch.
     Returns (tokens/s, seconds per step, description, threads)."""
     from oracle import dflash_oracle as O
 
@@ -263,10 +266,11 @@ def oracle_step_sample(wl: synth.Workload, seconds: float, tau: float, P: int, w
         if repeats is None and time.perf_counter() - t_start >= seconds:
             break
     med = {k: statistics.median(v) for k, v in times.items()}
-    t_step = med["fuse"] + med["inject"] + wl.draft_layers * med["dlayer"] + s.n_layers * med["tlayer"] + 2 * med["lm"]
+    t_seq = med["fuse"] + med["inject"] + wl.draft_layers * med["dlayer"] + s.n_layers * med["tlayer"] + 2 * med["lm"]
+    t_step = batch * t_seq
     desc = (f"{it} sample(s) of: fuse+inject of {B} rows, 1 drafter + 1 target layer over a {P}-position context, "
-            f"1 LM head; step time extrapolated to {wl.draft_layers} drafter + {s.n_layers} target layers + 2 LM heads "
-            f"({t_step:.2f} s/step), tokens/step = {tau:.2f}")
+            f"1 LM head; step time extrapolated to {wl.draft_layers} drafter + {s.n_layers} target layers + 2 LM heads"
+            + (f" x {batch} sequences" if batch > 1 else "") + f" ({t_step:.2f} s/step), tokens/step = {tau:.2f}")
     return tau / t_step, t_step, desc, _blas_threads()
 
 
@@ -298,16 +302,16 @@ def run_reference(args, dist: Dist):
         return
     wl = synth.WORKLOADS[args.workload]
     B = wl.block
-    k, _ = synth.acceptance_draws(max(args.steps, 1), wl.target.vocab)
-    tau = float(np.mean(np.minimum(k[:, 0], B - 1) + 1))
-    P = wl.prompt_len
+    k, _ = synth.acceptance_draws(max(args.steps, 1), wl.target.vocab, batch=wl.batch)
+    tau = float(np.mean(np.sum(np.minimum(k, B - 1) + 1, axis=1)))
+    P = int(round(np.mean(synth.prompt_lengths(wl))))
     for _ in range(args.warmup):
-        oracle_step_sample(wl, 0.0, tau, P, repeats=1)
+        oracle_step_sample(wl, 0.0, tau, P, repeats=1, batch=wl.batch)
     t0 = time.perf_counter()
     vals = []
     desc = ""
     for _ in range(args.steps):
-        v, t_step, desc, thr = oracle_step_sample(wl, 0.0, tau, P, repeats=1)
+        v, t_step, desc, thr = oracle_step_sample(wl, 0.0, tau, P, repeats=1, batch=wl.batch)
         vals.append(t_step)
     wall = time.perf_counter() - t0
     t_step = statistics.median(vals)
@@ -316,7 +320,7 @@ def run_reference(args, dist: Dist):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "batch": 1, "block": B, "context": P, "target_layers": wl.target.n_layers,
+        "config": {"workload": wl.name, "batch": wl.batch, "block": B, "context": P, "target_layers": wl.target.n_layers,
                    "draft_layers": wl.draft_layers},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
                          "sample": desc + f"; {args.steps} timed samples, wall {wall:.1f} s"},
@@ -356,19 +360,27 @@ def run_ours(args, dist: Dist):
     capi.load()
     wl = synth.WORKLOADS[args.workload]
     s = wl.target
-    B, P0, V = wl.block, wl.prompt_len, s.vocab
+    B, V, nb = wl.block, s.vocab, wl.batch
+    lens0 = synth.prompt_lengths(wl)
     K, W, PS = args.steps, max(args.warmup, 3), args.profile_steps
     n_steps = 1 + W + K + K + 2 * PS + 2          # eager, warm-up, timed, e2e, profile passes, margin
     n_ref = 1 + n_steps * B + B
-    cap = P0 + n_ref + 64
+    cap = max(lens0) + n_ref + 64
 
     t_setup = time.perf_counter()
     m = build_model(wl, dev)
-    prompt = synth.prompt_tokens(P0, V, stream=dist.rank)
+    prompts = [synth.prompt_tokens(P, V, stream=1000 * dist.rank + b) for b, P in enumerate(lens0)]
 
-    # greedy AR reference stream (and the plain AR decode rate on this GPU)
-    ar = Session(m, batch=1, capacity=cap, block=B, with_draft=False, stream_cap=n_ref + 8)
-    ar.prefill([prompt], inject=False)
+    # the speculative session: prefill (target forward over the prompts, fusion and injection)
+    sess = Session(m, batch=nb, capacity=cap, block=B, stream_cap=n_ref + 8)
+    sess.prefill(prompts)
+    torch.cuda.synchronize()
+    t_prefill = time.perf_counter() - t_setup
+
+    # greedy AR reference stream from the same committed state (and the plain
+    # AR decode rate on this GPU)
+    ar = Session(m, batch=nb, capacity=cap, block=B, with_draft=False, stream_cap=n_ref + 8)
+    ar.copy_target_from(sess)
     ar.ar_step()
     g_ar = ar.capture_graph(ar.ar_step)
     torch.cuda.synchronize()
@@ -378,16 +390,14 @@ def run_ours(args, dist: Dist):
         g_ar.replay()
     e1.record()
     torch.cuda.synchronize()
-    ar_tok_s = (n_ref - 2) / (e0.elapsed_time(e1) / 1e3)
-    G = ar.emitted()[0]
-    assert len(G) == n_ref and ar.status() == 0
+    ar_tok_s = nb * (n_ref - 2) / (e0.elapsed_time(e1) / 1e3)
+    G = ar.emitted()
+    assert all(len(g) == n_ref for g in G) and ar.status() == 0
     ar.close()
     del g_ar
 
-    k_draw, r_draw = synth.acceptance_draws(n_steps, V, seed=synth.ACCEPT_SEED + dist.rank)
-    sess = Session(m, batch=1, capacity=cap, block=B, stream_cap=n_ref + 8)
-    sess.prefill([prompt])
-    sess.set_teacher(G[None, :], k_draw, r_draw)
+    k_draw, r_draw = synth.acceptance_draws(n_steps, V, batch=nb, seed=synth.ACCEPT_SEED + dist.rank)
+    sess.set_teacher(np.stack(G), k_draw, r_draw)
     sess.step(teacher=True)                      # eager first step
     launches0 = capi.dflash_launch_count()
     graph = sess.capture_graph(lambda: sess.step(teacher=True))
@@ -398,8 +408,8 @@ def run_ours(args, dist: Dist):
     setup_s = time.perf_counter() - t_setup
 
     # ---------------------------------------------------------------- timed region
-    len0 = int(sess.stream_len.item())
-    P_before = sess.target_len()[0]
+    len0 = int(sess.stream_len.sum().item())
+    P_before = sess.target_len()
     clocks = ClockSampler(dist.local)
     clocks.start()
     time.sleep(0.4)
@@ -417,15 +427,15 @@ def run_ours(args, dist: Dist):
     clk = clocks.stop()
     step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(K)]
     total_s = evs[0].elapsed_time(evs[K]) / 1e3
-    tokens = int(sess.stream_len.item()) - len0
-    P_after = sess.target_len()[0]
+    tokens = int(sess.stream_len.sum().item()) - len0
+    P_after = sess.target_len()
     assert sess.status() == 0, "device status set during the timed region"
 
     # ---------------------------------------------------------------- end to end (host buffers)
     pin_k = torch.from_numpy(k_draw.astype(np.int32)).pin_memory()
     pin_r = torch.from_numpy(r_draw.astype(np.int32)).pin_memory()
-    out_acc = torch.zeros(1, dtype=torch.int32).pin_memory()
-    out_tok = torch.zeros(B, dtype=torch.int32).pin_memory()
+    out_acc = torch.zeros(nb, dtype=torch.int32).pin_memory()
+    out_tok = torch.zeros(nb * B, dtype=torch.int32).pin_memory()
     st_host = int(sess.step_ctr.item())
     torch.cuda.synchronize()
     e2e_tokens = 0
@@ -437,12 +447,12 @@ def run_ours(args, dist: Dist):
         sess.r_draw[si].copy_(pin_r[si], non_blocking=True)
         graph.replay()
         out_acc.copy_(sess.accept_len, non_blocking=True)
-        out_tok.copy_(sess.argmax[:B], non_blocking=True)
+        out_tok.copy_(sess.argmax[:nb * B], non_blocking=True)
         torch.cuda.current_stream().synchronize()
-        e2e_tokens += int(out_acc[0]) + 1
+        e2e_tokens += int(out_acc.sum()) + nb
     e2e_s = time.perf_counter() - t_e2e
-    h2d = 2 * 4
-    d2h = 4 + 4 * B
+    h2d = 2 * 4 * nb
+    d2h = 4 * nb + 4 * nb * B
 
     # ---------------------------------------------------------------- kernel timing pass (eager)
     stage_ms = {k: [] for k in ("fuse", "inject", "draft", "teacher", "verify", "accept")}
@@ -481,8 +491,8 @@ def run_ours(args, dist: Dist):
     gemm_gbs = gemm_bytes / (gemm_ms / 1e3) / 1e9 if gemm_ms > 0 else None
 
     # ---------------------------------------------------------------- results
-    P_mean = 0.5 * (P_before + P_after)
-    bytes_step, w_bytes, kv_bytes = step_bytes(wl, P_mean)
+    P_mean = 0.5 * (float(np.mean(P_before)) + float(np.mean(P_after)))
+    bytes_step, w_bytes, kv_bytes = step_bytes(wl, P_mean, batch=nb)
     ms_step = statistics.median(step_ms)
     peak, peak_kind = measured_peaks()
     step_gbs = bytes_step / (ms_step / 1e3) / 1e9
@@ -491,13 +501,14 @@ def run_ours(args, dist: Dist):
     tau = tokens / K
 
     cpu = None
-    if dist.rank == 0 and dist.world >= 1 and not args.no_cpu_baseline:
+    if dist.rank == 0 and not args.no_cpu_baseline:
         try:
             views = m.views()
             need = {n: views[n] for n in ["embed", "lm_head", "final_norm", "draft.w_fc", "draft.fc_norm"]
                     + [f"layers.0.{p}" for p in synth.LAYER_PARTS]
                     + [f"draft.layers.0.{p}" for p in synth.LAYER_PARTS]}
-            v, t_step, desc, thr = oracle_step_sample(wl, args.cpu_seconds, tau, P0, weights_dev=need)
+            v, t_step, desc, thr = oracle_step_sample(wl, args.cpu_seconds, tau, int(round(np.mean(lens0))),
+                                                      weights_dev=need, batch=nb)
             cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc}
         except Exception as e:  # the baseline is reported, never required
             cpu = {"value": None, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
@@ -507,7 +518,8 @@ def run_ours(args, dist: Dist):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K, "warmup": W,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (random-init weights N(0,0.02), uniform random prompt, teacher-forced acceptance)",
-        "config": {"workload": wl.name, "batch": 1, "block": B, "context": P0, "context_mean_timed": P_mean,
+        "config": {"workload": wl.name, "batch": nb, "block": B,
+                   "context": lens0[0] if nb == 1 else lens0, "context_mean_timed": P_mean,
                    "target_layers": s.n_layers, "draft_layers": wl.draft_layers, "hidden": s.hidden,
                    "vocab": V, "parallelism": f"replicas{dist.world}",
                    "l2": "inputs larger than L2 (weights+KV read per step >> 129 MB)", "graph": "one CUDA graph per step"},
@@ -530,6 +542,7 @@ def run_ours(args, dist: Dist):
         "kernels_per_step": int(kernels_per_step),
         "cpu_baseline": cpu,
         "setup_s": setup_s,
+        "prefill_s": t_prefill,
     }
     sess.close()
     if dist.rank == 0:

@@ -213,6 +213,28 @@ class Session:
                 if dv:
                     capi.dflash_cache_free(dv)
 
+    def copy_target_from(self, other: "Session"):
+        """Take over another session's committed target state (keys/values of
+        positions 0..len-1 of every layer, lengths, anchors and emitted
+        streams) instead of prefilling the same prompts again."""
+        s = self.m.shape
+        lens = other.target_len()
+        tdt = _DT[self.m.dtype][1]
+        for b, n in enumerate(lens):
+            if n == 0:
+                continue
+            k = torch.empty(s.n_kv, n, s.head_dim, dtype=tdt, device=self.m.device)
+            v = torch.empty_like(k)
+            for li in range(s.n_layers):
+                capi.dflash_cache_read(other.tcache, li, b, 0, n, k, v)
+                capi.dflash_cache_write(self.tcache, li, b, 0, n, k, v)
+        capi.dflash_cache_set_lengths(self.tcache, lens)
+        self.anchor.copy_(other.anchor)
+        w = min(self.stream_cap, other.stream_cap)
+        self.stream[:, :w].copy_(other.stream[:, :w])
+        self.stream_len.copy_(other.stream_len)
+        torch.cuda.synchronize()
+
     # -------------------------------------------------------------- decoding
     def set_teacher(self, ref, k_draw, r_draw):
         """Teacher-forcing inputs: ref [batch][L] greedy streams, draws [steps][batch]."""

@@ -83,7 +83,17 @@ WORKLOADS = {
     "qwen3-8b-4k": Workload("qwen3-8b-4k", _qwen3_8b_shape(), 5, "bf16", 16, 4096, 2048, True),
     # 27B-class dense target, block 15, 36K prompt, 1500 tokens, teacher forced
     "dense27b-36k": Workload("dense27b-36k", _dense27b_shape(), 5, "bf16", 15, 36864, 1500, True),
+    # Qwen3-8B shapes, 8 sequences with prompt lengths uniform on 2048..6144
+    # (batch_prompt_lengths; prompt_len is the upper end), block 16
+    "qwen3-8b-batch8": Workload("qwen3-8b-batch8", _qwen3_8b_shape(), 5, "bf16", 16, 6144, 512, True, batch=8),
 }
+
+
+def prompt_lengths(wl: Workload):
+    """Per-sequence prompt lengths of a workload."""
+    if wl.batch == 1:
+        return [wl.prompt_len]
+    return [int(x) for x in batch_prompt_lengths(wl.batch, hi=wl.prompt_len)]
 
 
 # ---------------------------------------------------------------------------
