@@ -139,6 +139,12 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
                       const int32_t* len, const KvMaps* maps, const AttnScratch& sc, void* out, int* status,
                       cudaStream_t s);
 
+// tcgen05 variant of the bf16 attention chunk kernel (head_dim 128, G in
+// {1, 2, 4, 5, 8}); writes the same chunk partials as the mma.sync kernel.
+cudaError_t attention_tc(int G, const KvMaps& maps, const bf16* q, int batch, int n, int nq, int nkv, int causal,
+                         int capacity, const int32_t* len, const AttnScratch& sc, int nchunk_launch, float scale_log2,
+                         int* status, cudaStream_t s);
+
 // Greedy token and top-2 gap per row.  If skip_first_of (>0), rows with
 // (r % skip_first_of) == 0 are not written to argmax_out.
 constexpr int kArgmaxSlices = 16;

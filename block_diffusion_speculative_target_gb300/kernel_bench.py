@@ -90,7 +90,7 @@ def bench_attention(P, nq, nkv, n, iters, warmup, causal=1):
         capi.dflash_cache_free(c)
     capi.dflash_workspace_free(ws)
     byt = 2 * 2 * nkv * (P + n) * hd
-    return {"kernel": "attn_tma_kernel+attn_combine_kernel", "P": P, "nq": nq, "nkv": nkv, "n": n, "ms": avg,
+    return {"kernel": "attn_tc_kernel+attn_combine_kernel", "P": P, "nq": nq, "nkv": nkv, "n": n, "ms": avg,
             "bytes": byt, "GBps": byt / (avg / 1e3) / 1e9}
 
 
