@@ -65,6 +65,27 @@ __device__ __forceinline__ float ld_dsmem(uint32_t addr) {
   return v;
 }
 
+// Sum of the SS split partials of one element (and of its RoPE partner) in
+// split order, every load issued before the first add.
+template <int SS>
+__device__ __forceinline__ void sum_partials(uint32_t red_local, uint32_t off, uint32_t poff, bool rope, float& acc,
+                                             float& pacc) {
+  float p[SS], q[SS];
+#pragma unroll
+  for (int cc = 0; cc < SS; ++cc) {
+    const uint32_t base = dsmem_addr(red_local, (uint32_t)cc);
+    p[cc] = ld_dsmem(base + off);
+    q[cc] = rope ? ld_dsmem(base + poff) : 0.f;
+  }
+  acc = 0.f;
+  pacc = 0.f;
+#pragma unroll
+  for (int cc = 0; cc < SS; ++cc) {
+    acc += p[cc];
+    pacc += q[cc];
+  }
+}
+
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 // Final value y of output (n, m): apply the epilogue.  `partner` is y[n][m^1]
@@ -239,6 +260,54 @@ __global__ void __launch_bounds__(128)
   pdl_wait();
   const int ml = warp * 32 + lane;
   const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  const bool rope = epi.kind == GE_QKV || epi.kind == GE_INJECT;
+  if (S == 1 && !rope) {
+    // Unsplit tile: the accumulator is the result.  Read it straight from
+    // TMEM, 16 rows at a time, and run the epilogue with the rows unrolled
+    // (a residual's old values all in flight before the first add).
+#pragma unroll 1
+    for (int c = 0; c < BN / 16; ++c) {
+      if (c * 16 >= rows) break;  // uniform
+      float v[16];
+      tmem_ld16(trow + c * 16, v);
+      if (epi.kind == GE_RESID) {
+        float* col = reinterpret_cast<float*>(epi.out) + m0 + ml;
+        float old[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (c * 16 + i < rows) old[i] = col[(size_t)(c * 16 + i) * epi.ldo];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int n = c * 16 + i;
+          if (n < rows && !flags[0]) {
+            const float x = old[i] + v[i];
+            col[(size_t)n * epi.ldo] = x;
+            if (epi.cap_mask)
+              for (int c5 = 0; c5 < 5; ++c5)
+                if (epi.cap_mask & (1 << c5))
+                  reinterpret_cast<bf16*>(epi.hcap)[(size_t)n * 5 * epi.cap_H + (size_t)c5 * epi.cap_H + m0 + ml] =
+                      __float2bfloat16_rn(x);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int n = c * 16 + i;  // uniform over the CTA
+          if (n < rows) {
+            const float partner = __shfl_xor_sync(0xffffffffu, v[i], 1);
+            if (!flags[0]) gemm_epi(epi, n, m0 + ml, v[i], partner, status);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+      tc_fence_after();
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    return;
+  }
   // park the partial tile: red[n][ml]
 #pragma unroll 1
   for (int c = 0; c < BN / 16; ++c) {
@@ -250,16 +319,22 @@ __global__ void __launch_bounds__(128)
   }
   tc_fence_before();
   cluster_sync();  // every partial of the tile is in shared memory
-  const bool rope = epi.kind == GE_QKV || epi.kind == GE_INJECT;
   const uint32_t red_local = smem_u32(red);
   for (int n = r; n < rows; n += S) {
-    float acc = 0.f, pacc = 0.f;
     const uint32_t off = (uint32_t)((n * C::BM + ml) * 4);
     const uint32_t poff = (uint32_t)((n * C::BM + (ml ^ 64)) * 4);
-    for (int cc = 0; cc < S; ++cc) {
-      const uint32_t base = dsmem_addr(red_local, (uint32_t)cc);
-      acc += ld_dsmem(base + off);
-      if (rope) pacc += ld_dsmem(base + poff);
+    float acc, pacc;
+    switch (S) {  // the split counts the policy produces: all loads of a row in flight together
+      case 2: sum_partials<2>(red_local, off, poff, rope, acc, pacc); break;
+      case 4: sum_partials<4>(red_local, off, poff, rope, acc, pacc); break;
+      case 8: sum_partials<8>(red_local, off, poff, rope, acc, pacc); break;
+      default:
+        acc = pacc = 0.f;
+        for (int cc = 0; cc < S; ++cc) {
+          const uint32_t base = dsmem_addr(red_local, (uint32_t)cc);
+          acc += ld_dsmem(base + off);
+          if (rope) pacc += ld_dsmem(base + poff);
+        }
     }
     const float partner = rope ? pacc : __shfl_xor_sync(0xffffffffu, acc, 1);
     if (!flags[0]) gemm_epi(epi, n, m0 + ml, acc, partner, status);
