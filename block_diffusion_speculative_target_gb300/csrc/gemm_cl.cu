@@ -42,7 +42,9 @@ struct ClCfg {
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
   static constexpr int RED_BYTES = BN * BM * 4;  // partial tile, aliases the ring
   static constexpr int RING = STAGES * STAGE_BYTES;
-  static constexpr int SMEM = (RING > RED_BYTES ? RING : RED_BYTES) + 1024 + 256;
+  static constexpr int TAIL = 256;   // barriers, TMEM slot, flags
+  static constexpr int PRE = 2048;   // epilogue operands prefetched during the main loop
+  static constexpr int SMEM = (RING > RED_BYTES ? RING : RED_BYTES) + 1024 + TAIL + PRE;
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -87,6 +89,36 @@ __device__ __forceinline__ void sum_partials(uint32_t red_local, uint32_t off, u
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// RoPE / KV-cache epilogue of output (n, m) with the row's position and the
+// cos/sin of this column's frequency at that position already at hand.
+__device__ __forceinline__ void gemm_epi_rope(const GemmEpi& e, int n, int m, float v, float partner, int pos,
+                                              float2 cs, int* status) {
+  const int t = m >> 7, ml = m & 127;
+  int kind, h, layer = 0;  // kind: 0 q, 1 k, 2 v
+  if (e.kind == GE_QKV) {
+    kind = t < e.nq ? 0 : (t < e.nq + e.nkv ? 1 : 2);
+    h = kind == 0 ? t : (kind == 1 ? t - e.nq : t - e.nq - e.nkv);
+  } else {
+    layer = t / (2 * e.nkv);
+    const int rem = t % (2 * e.nkv);
+    kind = rem < e.nkv ? 1 : 2;
+    h = rem % e.nkv;
+  }
+  const float r = kind == 2 ? v : (ml < 64 ? v * cs.x - partner * cs.y : v * cs.x + partner * cs.y);
+  if (kind == 0) {
+    reinterpret_cast<bf16*>(e.out)[((size_t)n * e.nq + h) * 128 + ml] = __float2bfloat16_rn(r);
+    return;
+  }
+  if (pos >= e.capacity) {
+    set_status(status, DFLASH_STATUS_CAPACITY);
+    return;
+  }
+  const int b = n / e.rows_per_seq;
+  bf16* dst = reinterpret_cast<bf16*>(kind == 1 ? e.kc : e.vc);
+  dst[(size_t)layer * e.layer_stride + (size_t)b * e.seq_stride + (size_t)h * e.head_stride + (size_t)pos * 128 + ml] =
+      __float2bfloat16_rn(r);
+}
 
 // Final value y of output (n, m): apply the epilogue.  `partner` is y[n][m^1]
 // (SwiGLU) or y[n][m^64] within the head (RoPE).
@@ -165,6 +197,13 @@ __global__ void __launch_bounds__(128)
   uint64_t* accb = empty + STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
+  // Prefetched epilogue operands of this CTA's rows (r, r + S, ...; at most
+  // 4): old residual values [row][128], or RoPE cos/sin [row][64] and the
+  // row's position (-1: row skipped).
+  uint8_t* pre = tail + C::TAIL;
+  float* pre_x = reinterpret_cast<float*>(pre);
+  float2* pre_cs = reinterpret_cast<float2*>(pre);
+  int* pre_pos = reinterpret_cast<int*>(tail + 192);  // [4], after the barriers and flags
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = (int)cluster_rank();  // split index
@@ -173,6 +212,9 @@ __global__ void __launch_bounds__(128)
   const int kb0 = (int)((long long)r * KB / S), kb1 = (int)((long long)(r + 1) * KB / S);
   const int nkb = kb1 - kb0;
   const int m0 = tile * C::BM;
+  const bool rope = epi.kind == GE_QKV || epi.kind == GE_INJECT;
+  // prefetch the epilogue operands when this CTA owns at most 4 rows of a split tile
+  const bool pf = S > 1 && (rows + S - 1) / S <= 4 && (epi.kind == GE_RESID || rope);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -221,6 +263,26 @@ __global__ void __launch_bounds__(128)
       }
     }
     __syncwarp();
+  } else if (warp >= 2 && pf) {
+    // Idle during the main loop: fetch what the epilogue will need for this
+    // CTA's rows, so no row waits on global memory there.
+    const int gt = threadIdx.x - 64;
+    pdl_wait();
+    for (int j = 0; j * S + r < rows; ++j) {
+      const int n = r + j * S;
+      if (epi.kind == GE_RESID) {
+        const float2 v = *reinterpret_cast<const float2*>(reinterpret_cast<const float*>(epi.out) +
+                                                          (size_t)n * epi.ldo + m0 + 2 * gt);
+        pre_x[j * 128 + 2 * gt] = v.x;
+        pre_x[j * 128 + 2 * gt + 1] = v.y;
+      } else {  // GE_QKV / GE_INJECT
+        const int b = n / epi.rows_per_seq, jj = n % epi.rows_per_seq;
+        const bool skip = epi.kind == GE_INJECT && jj >= epi.n_pend[b];
+        const int pos = epi.len[b] + jj;
+        if (gt == 0) pre_pos[j] = skip ? -1 : pos;
+        pre_cs[j * 64 + gt] = pos < epi.capacity ? epi.rope[(size_t)pos * 64 + gt] : make_float2(1.f, 0.f);
+      }
+    }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(C::BM, BN);
@@ -260,7 +322,6 @@ __global__ void __launch_bounds__(128)
   pdl_wait();
   const int ml = warp * 32 + lane;
   const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-  const bool rope = epi.kind == GE_QKV || epi.kind == GE_INJECT;
   if (S == 1 && !rope) {
     // Unsplit tile: the accumulator is the result.  Read it straight from
     // TMEM, 16 rows at a time, and run the epilogue with the rows unrolled
@@ -335,6 +396,22 @@ __global__ void __launch_bounds__(128)
           acc += ld_dsmem(base + off);
           if (rope) pacc += ld_dsmem(base + poff);
         }
+    }
+    if (pf) {  // operands already in shared memory
+      const int j = (n - r) / S;
+      if (flags[0]) continue;
+      if (epi.kind == GE_RESID) {
+        const float x = pre_x[j * 128 + ml] + acc;
+        reinterpret_cast<float*>(epi.out)[(size_t)n * epi.ldo + m0 + ml] = x;
+        if (epi.cap_mask)
+          for (int c5 = 0; c5 < 5; ++c5)
+            if (epi.cap_mask & (1 << c5))
+              reinterpret_cast<bf16*>(epi.hcap)[(size_t)n * 5 * epi.cap_H + (size_t)c5 * epi.cap_H + m0 + ml] =
+                  __float2bfloat16_rn(x);
+      } else if (pre_pos[j] >= 0) {
+        gemm_epi_rope(epi, n, m0 + ml, acc, pacc, pre_pos[j], pre_cs[j * 64 + (ml & 63)], status);
+      }
+      continue;
     }
     const float partner = rope ? pacc : __shfl_xor_sync(0xffffffffu, acc, 1);
     if (!flags[0]) gemm_epi(epi, n, m0 + ml, acc, partner, status);
