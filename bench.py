@@ -40,7 +40,7 @@ UNIT = "tokens/s"
 # weight-product launches of one step of the 4K workload, from the ncu launch
 # list in profiles/launches__bench_qwen3-8b-4k.md.  Set to None whenever the
 # kernel changes until a new capture is taken.
-GEMM_TRAFFIC = {"workload": "qwen3-8b-4k", "bytes_per_launch": None,
+GEMM_TRAFFIC = {"workload": "qwen3-8b-4k", "bytes_per_launch": 111039901,
                 "source": "profiles/launches__bench_qwen3-8b-4k.md"}
 
 
