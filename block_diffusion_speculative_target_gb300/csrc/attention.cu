@@ -13,6 +13,9 @@
 // bf16 path (head_dim 128): the tcgen05 chunk kernel (attention_tc.cu).
 // fp32 path: CUDA-core dot products, one CTA per (chunk, head, row).  This
 // file also holds the chunk combine and the TMA maps over a cache.
+#include <algorithm>
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -145,18 +148,24 @@ typedef CUresult (*PFN_encodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint3
                                       const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                       CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// 2-D maps over a whole bf16 cache viewed as [rows_total][128]: boxes of 64
-// elements (128 B, swizzled) by 128 positions.
-bool make_kv_maps(const void* k, const void* v, long long rows_total, CUtensorMap* mk, CUtensorMap* mv) {
-  static PFN_encodeTiled_t fn = nullptr;
-  if (!fn) {
+// The driver's tensor-map encoder, fetched once (null if unavailable).
+static PFN_encodeTiled_t encoder() {
+  static const PFN_encodeTiled_t fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
-      return false;
-    fn = reinterpret_cast<PFN_encodeTiled_t>(p);
-  }
+      return (PFN_encodeTiled_t) nullptr;
+    return reinterpret_cast<PFN_encodeTiled_t>(p);
+  }();
+  return fn;
+}
+
+// 2-D maps over a whole bf16 cache viewed as [rows_total][128]: boxes of 64
+// elements (128 B, swizzled) by 128 positions.
+bool make_kv_maps(const void* k, const void* v, long long rows_total, CUtensorMap* mk, CUtensorMap* mv) {
+  const PFN_encodeTiled_t fn = encoder();
+  if (!fn) return false;
   cuuint64_t dims[2] = {128, (cuuint64_t)rows_total};
   cuuint64_t strides[1] = {256};
   cuuint32_t box[2] = {64, 128};
@@ -166,6 +175,40 @@ bool make_kv_maps(const void* k, const void* v, long long rows_total, CUtensorMa
            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
+  return true;
+}
+
+bool make_q_map(const void* q, int rows, int nq, int G, CUtensorMap* out) {
+  struct Entry {
+    const void* q;
+    int rows, nq, G;
+    CUtensorMap map;
+  };
+  static Entry cache[16];
+  static int used = 0, next = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].q == q && cache[i].rows == rows && cache[i].nq == nq && cache[i].G == G) {
+      *out = cache[i].map;
+      return true;
+    }
+  const PFN_encodeTiled_t fn = encoder();
+  if (!fn || (reinterpret_cast<uintptr_t>(q) & 15) || rows <= 0) return false;
+  CUtensorMap m;
+  cuuint64_t dims[3] = {128, (cuuint64_t)nq, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {256, (cuuint64_t)nq * 256};
+  cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)std::min(rows, 16)};
+  cuuint32_t es[3] = {1, 1, 1};
+  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Entry& e = cache[next];
+  e = Entry{q, rows, nq, G, m};
+  next = (next + 1) % 16;
+  if (used < 16) ++used;
+  *out = m;
   return true;
 }
 
@@ -179,7 +222,9 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
   if (dtype == DFLASH_BF16) {
     if (hd != kHD || !maps) return cudaErrorInvalidValue;
     const int G = nq / nkv;
-    DFL_RET(attention_tc(G, *maps, (const bf16*)q, batch, n, nq, nkv, causal, capacity, len, sc, nchunk_launch,
+    CUtensorMap qmap;
+    if (!make_q_map(q, batch * n, nq, G, &qmap)) return cudaErrorInvalidValue;
+    DFL_RET(attention_tc(G, *maps, qmap, batch, n, nq, nkv, causal, capacity, len, sc, nchunk_launch,
                          scale_log2, status, s));
     DFL_RET(launch_pdl(attn_combine_kernel<bf16>, dim3(batch * n, nq), dim3(256), 0, s, sc.o, sc.ml, n, nq, hd,
                        causal, capacity, len, sc.nchunk, (bf16*)out));

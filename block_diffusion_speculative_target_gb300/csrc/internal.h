@@ -139,9 +139,12 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
                       const int32_t* len, const KvMaps* maps, const AttnScratch& sc, void* out, int* status,
                       cudaStream_t s);
 
-// tcgen05 variant of the bf16 attention chunk kernel (head_dim 128, G in
-// {1, 2, 4, 5, 8}); writes the same chunk partials as the mma.sync kernel.
-cudaError_t attention_tc(int G, const KvMaps& maps, const bf16* q, int batch, int n, int nq, int nkv, int causal,
+// 3-D map over a bf16 query buffer [rows][nq][128]: boxes of 64 head-dim
+// elements (128 B, swizzled) x G heads x min(16, rows) rows.  Encoded maps are cached by
+// (pointer, rows, nq, G).
+bool make_q_map(const void* q, int rows, int nq, int G, CUtensorMap* out);
+// The bf16 attention chunk kernel on tcgen05 (head_dim 128, G in {1, 2, 4, 5, 8}).
+cudaError_t attention_tc(int G, const KvMaps& maps, const CUtensorMap& qmap, int batch, int n, int nq, int nkv, int causal,
                          int capacity, const int32_t* len, const AttnScratch& sc, int nchunk_launch, float scale_log2,
                          int* status, cudaStream_t s);
 
