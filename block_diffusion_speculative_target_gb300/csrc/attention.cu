@@ -80,68 +80,91 @@ __global__ void __launch_bounds__(NT)
   }
 }
 
-// Merge the chunk partials of one (row, query head): weights w_c =
-// 2^(m_c - max m) staged in shared memory, then out[d] = sum_c w_c o_c[d] /
-// sum_c w_c l_c.  256 threads: thread (d, half) sums one half of the chunks
-// (loads unrolled for memory-level parallelism); the halves are added in a
-// fixed order, so the result does not depend on other rows.
+// Merge of the chunk partials of one (row, head): with w_c = 2^(m_c - max m),
+// out[d] = sum_c w_c o_c[d] / sum_c w_c l_c.  kCombineGroups x 64 threads:
+// thread (d2, g) owns columns 2 d2 and 2 d2 + 1 and sums them over the g-th
+// contiguous slice of the chunks (float2 loads, unrolled for memory-level
+// parallelism); the slices are added in group order, and the max and the
+// denominator are reduced by warp 0 over a fixed butterfly.  The result
+// depends only on the row's own chunks.  (256-thread blocks leave room on each
+// SM for the next kernel's CTAs to start early.)
 constexpr int kCombineMaxChunks = 1024;
+constexpr int kCombineGroups = 4;
+constexpr int kCombineUnroll = 8;  // float2 partial loads in flight per thread
 
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kCombineGroups * 64)
     attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int n, int nq, int hd,
                         int causal, int capacity, const int32_t* __restrict__ len, int nchunk, T* __restrict__ out) {
   __shared__ float w[kCombineMaxChunks];
   __shared__ float lsum[kCombineMaxChunks];
-  __shared__ float half1[kHD];
+  __shared__ float slice[kCombineGroups][kHD];
   __shared__ float Msh, Lsh;
   const int r = blockIdx.x, hq = blockIdx.y;
   const int b = r / n, j = r % n;
+  const int tid = threadIdx.x, lane = tid & 31;
   pdl_launch();
   pdl_wait();
   const int P = len[b];
   const int lim = min(causal ? P + j + 1 : P + n, capacity);
   const int nch = min((lim + kAttnChunk - 1) / kAttnChunk, kCombineMaxChunks);
   const size_t row0 = ((size_t)r * nq + hq) * nchunk;
-  for (int c = threadIdx.x; c < nch; c += blockDim.x) {
+  for (int c = tid; c < nch; c += blockDim.x) {
     const float2 ml = *reinterpret_cast<const float2*>(part_ml + (row0 + c) * 2);
     w[c] = ml.x;
     lsum[c] = ml.y;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float M = -INFINITY;
-    for (int c = 0; c < nch; ++c) M = fmaxf(M, w[c]);
-    Msh = M;
+  if (tid < 32) {
+    float m = -INFINITY;
+    for (int c = lane; c < nch; c += 32) m = fmaxf(m, w[c]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) Msh = m;
   }
   __syncthreads();
   const float M = Msh;
-  for (int c = threadIdx.x; c < nch; c += blockDim.x) w[c] = (w[c] == -INFINITY) ? 0.f : exp2f(w[c] - M);
+  for (int c = tid; c < nch; c += blockDim.x) w[c] = (w[c] == -INFINITY) ? 0.f : exp2f(w[c] - M);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float L = 0.f;
-    for (int c = 0; c < nch; ++c) L += w[c] * lsum[c];
-    Lsh = L;
+  if (tid < 32) {
+    float l = 0.f;
+    for (int c = lane; c < nch; c += 32) l += w[c] * lsum[c];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane == 0) Lsh = l;
   }
-  const int d = threadIdx.x & 127, h = threadIdx.x >> 7;
-  const int cmid = nch / 2;
-  const int c0 = h == 0 ? 0 : cmid, c1 = h == 0 ? cmid : nch;
-  float acc = 0.f;
-  if (d < hd) {
-    const float* po = part_o + row0 * kHD + d;
+  const int d2 = tid & 63, g = tid >> 6;
+  const int c0 = nch * g / kCombineGroups, c1 = nch * (g + 1) / kCombineGroups;
+  float2 acc = make_float2(0.f, 0.f);
+  {
+    const float* po = part_o + row0 * kHD + 2 * d2;
     int c = c0;
-    for (; c + 8 <= c1; c += 8) {
-      float v[8];
+    for (; c + kCombineUnroll <= c1; c += kCombineUnroll) {
+      float2 v[kCombineUnroll];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = po[(size_t)(c + u) * kHD];
+      for (int u = 0; u < kCombineUnroll; ++u) v[u] = *reinterpret_cast<const float2*>(po + (size_t)(c + u) * kHD);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) acc += w[c + u] * v[u];
+      for (int u = 0; u < kCombineUnroll; ++u) {
+        acc.x += w[c + u] * v[u].x;
+        acc.y += w[c + u] * v[u].y;
+      }
     }
-    for (; c < c1; ++c) acc += w[c] * po[(size_t)c * kHD];
+    for (; c < c1; ++c) {
+      const float2 v = *reinterpret_cast<const float2*>(po + (size_t)c * kHD);
+      acc.x += w[c] * v.x;
+      acc.y += w[c] * v.y;
+    }
   }
-  if (h == 1) half1[d] = acc;
+  slice[g][2 * d2] = acc.x;
+  slice[g][2 * d2 + 1] = acc.y;
   __syncthreads();
-  if (h == 0 && d < hd) out[((size_t)r * nq + hq) * hd + d] = from_f<T>((acc + half1[d]) / Lsh);
+  if (tid < kHD) {
+    const int d = tid;
+    float sum = slice[0][d];
+#pragma unroll
+    for (int k = 1; k < kCombineGroups; ++k) sum += slice[k][d];
+    if (d < hd) out[((size_t)r * nq + hq) * hd + d] = from_f<T>(sum / Lsh);
+  }
 }
 
 typedef CUresult (*PFN_encodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -226,15 +249,15 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
     if (!make_q_map(q, batch * n, nq, G, &qmap)) return cudaErrorInvalidValue;
     DFL_RET(attention_tc(G, *maps, qmap, batch, n, nq, nkv, causal, capacity, len, sc, nchunk_launch,
                          scale_log2, status, s));
-    DFL_RET(launch_pdl(attn_combine_kernel<bf16>, dim3(batch * n, nq), dim3(256), 0, s, sc.o, sc.ml, n, nq, hd,
-                       causal, capacity, len, sc.nchunk, (bf16*)out));
+    DFL_RET(launch_pdl(attn_combine_kernel<bf16>, dim3(batch * n, nq), dim3(kCombineGroups * 64), 0, s, sc.o,
+                       sc.ml, n, nq, hd, causal, capacity, len, sc.nchunk, (bf16*)out));
   } else {
     const dim3 grid(nchunk_launch, nq, batch * n);
     DFL_RET(launch_pdl(attn_f32_kernel<128>, grid, dim3(128), 0, s, (const float*)q, n, nq, nkv, hd, causal,
                        (const float*)kc, (const float*)vc, seq_stride, head_stride, capacity, len, sc.o, sc.ml,
                        sc.nchunk, scale_log2));
-    DFL_RET(launch_pdl(attn_combine_kernel<float>, dim3(batch * n, nq), dim3(256), 0, s, sc.o, sc.ml, n, nq, hd,
-                       causal, capacity, len, sc.nchunk, (float*)out));
+    DFL_RET(launch_pdl(attn_combine_kernel<float>, dim3(batch * n, nq), dim3(kCombineGroups * 64), 0, s, sc.o,
+                       sc.ml, n, nq, hd, causal, capacity, len, sc.nchunk, (float*)out));
   }
   count_launch(2);
   return cudaSuccess;

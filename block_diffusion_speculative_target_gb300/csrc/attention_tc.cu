@@ -43,7 +43,8 @@ constexpr uint32_t kRegQ = 131072;     // query [d-half][128 rows][128 B]; later
 constexpr uint32_t kStats = 196608;    // row max [4][128], row sum [4][128]
 constexpr uint32_t kBars = kStats + 4096;
 constexpr uint32_t kLens = kBars + 64;      // sequence lengths (batch <= 128)
-constexpr int kTcSmem = kLens + 512 + 1024;  // + alignment slack
+constexpr uint32_t kNext = kLens + 512;     // the next item: index + TcItem fields
+constexpr int kTcSmem = kNext + 32 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;    // S: columns 0..255, O: 256..383
 constexpr uint64_t kTcWaitNs = 500000000ull;
 
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   int* okf = reinterpret_cast<int*>(tslot + 1);
   int* pend = okf + 1;  // copies issued whose completion has not been seen yet
   int* len_s = reinterpret_cast<int*>(sm + kLens);
+  int* next_s = reinterpret_cast<int*>(sm + kNext);
   const int nrb = (n + 15) >> 4;
   const int qbox = min(16, batch * n);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -190,6 +192,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     if (!*okf) break;
     const int valid = cur.valid;
+    if (tid == kIssuer) {  // decode the next item now, off the path from the PV product to its copies
+      TcItem nx;
+      next_s[0] = tc_next(t + gridDim.x, nitems, nkv, nrb, batch, n, causal, capacity, len_s, nx);
+      next_s[1] = nx.c, next_s[2] = nx.hk, next_s[3] = nx.b, next_s[4] = nx.rb;
+      next_s[5] = nx.P, next_s[6] = nx.k_begin, next_s[7] = nx.valid;
+    }
 
     // ---- S = Q K^T per key half
     if (tid == 0) {
@@ -335,10 +343,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---- the tiles are dead: start the next item's loads.  The issuing lane
     // belongs to the last warp, which holds padding rows whenever 16 G <= 96, so
     // the copies go out while the other warps write the partial.
-    TcItem nxt;
-    const int t2 = tc_next(t + gridDim.x, nitems, nkv, nrb, batch, n, causal, capacity, len_s, nxt);
-    if (tid == kIssuer && t2 < nitems && good) {
-      issue_loads(nxt);
+    if (tid == kIssuer && next_s[0] < nitems && good) {
+      const TcItem nx{next_s[1], next_s[2], next_s[3], next_s[4], next_s[5], next_s[6], next_s[7]};
+      issue_loads(nx);
       *pend = 1;
     }
 
@@ -378,8 +385,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const size_t prow = ((size_t)(cur.b * n + qi) * nq + cur.hk * G + hl) * nchunk + cur.c;
       *reinterpret_cast<float2*>(part_ml + prow * 2) = make_float2(M, L);
     }
-    cur = nxt;
-    t = t2;
+    t = next_s[0];  // written before the syncs above
+    cur = TcItem{next_s[1], next_s[2], next_s[3], next_s[4], next_s[5], next_s[6], next_s[7]};
     ph ^= 1;
   }
   __syncthreads();
