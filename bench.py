@@ -302,7 +302,12 @@ def run_reference(args, dist: Dist):
         return
     wl = synth.WORKLOADS[args.workload]
     B = wl.block
-    k, _ = synth.acceptance_draws(max(args.steps, 1), wl.target.vocab, batch=wl.batch)
+    # the acceptance draws of the GPU arm's timed steps for the same --steps/--warmup
+    # (its first, eager step takes draw 0, the warm-up replays draws 1..W), so that
+    # both arms divide by the same emitted tokens per step
+    K, W = max(args.steps, 1), args.warmup
+    k, _ = synth.acceptance_draws(1 + W + K, wl.target.vocab, batch=wl.batch)
+    k = k[1 + W:]
     tau = float(np.mean(np.sum(np.minimum(k, B - 1) + 1, axis=1)))
     P = int(round(np.mean(synth.prompt_lengths(wl))))
     for _ in range(args.warmup):
