@@ -664,6 +664,7 @@ int dflash_attention(const dflash_model_desc* d, const void* q, int32_t batch, i
                      dflash_cache* c, int32_t layer, void* out, dflash_workspace* ws, dflash_stream_t stream) {
   REQ(desc_ok(d) && q && out && ws && batch > 0 && n > 0 && batch * n <= ws->max_rows);
   REQ(cache_matches(c, *d, layer + 1) && layer >= 0 && batch <= c->batch && c->capacity <= ws->max_ctx);
+  REQ((reinterpret_cast<uintptr_t>(q) & 15) == 0);  // the bf16 path reads q by TMA
   if (!desc_shapes_ok(d)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
   const uint8_t* kc = c->k + (size_t)layer * c->layer_stride * c->elem;
   const uint8_t* vc = c->v + (size_t)layer * c->layer_stride * c->elem;

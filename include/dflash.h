@@ -287,7 +287,12 @@ int dflash_argmax_noalloc(const float *logits, int32_t rows, int32_t V, int32_t 
 /* Attention of q [batch][n][nq][hd] (dtype, RoPE applied) against layer
  * `layer` of `cache` (positions 0 .. len[b] + n - 1, the block's own keys
  * already written at len[b] ..), causal (row j sees 0..len+j) or not (every
- * row sees 0..len+n-1).  out [batch][n][nq * hd] dtype. */
+ * row sees 0..len+n-1).  out [batch][n][nq * hd] dtype.  q, out: device
+ * pointers owned by the caller; q must be 16-byte aligned (the bf16 path
+ * loads it by TMA), else DFLASH_ERR_INVALID_ARG before any CUDA call.
+ * Every score and softmax sum is exact per fixed 256-position chunk and the
+ * chunks merge in order (the scaled dot-product attention of "DFlash 深度解析",
+ * §2.2 draft_inference, evaluated chunkwise). */
 int dflash_attention(const dflash_model_desc *d, const void *q, int32_t batch, int32_t n,
                      int32_t causal, dflash_cache *cache, int32_t layer, void *out,
                      dflash_workspace *ws, dflash_stream_t stream);

@@ -132,6 +132,10 @@ ATT_CASES = [
     ("bf16", 8, 2, 128, [300, 17], 1),
     ("bf16", 4, 1, 128, [200, 513], 37),
     ("bf16", 8, 4, 128, [1024], 128),
+    # G = 8: no padding rows, the copy/PV issuing lane sits in a live warp
+    ("bf16", 64, 8, 128, [700], 16),
+    # G = 1 with several work items per persistent CTA (512 items)
+    ("bf16", 8, 8, 128, [8000, 3000], 16),
 ]
 
 
@@ -164,6 +168,24 @@ def test_attention(ws, dt, nq, nkv, hd, lens, n, causal):
             for h in range(nq):
                 ref = O.attention(q[b, :, h], ks[b][h // G], vs[b][h // G], allowed)
                 assert_close(got[b, :, h], ref, dt, f"attention b={b} h={h} P={P} n={n} causal={causal}")
+        assert capi.dflash_status(ws) == 0
+    finally:
+        capi.dflash_cache_free(cache)
+
+
+def test_attention_rejects_misaligned_query(ws):
+    """The bf16 path reads the query by TMA: a query pointer off a 16-byte
+    boundary is an argument error, reported before any launch."""
+    d = _desc(H=4 * 128, nq=4, nkv=1, hd=128, F=256, V=256, dt=capi.BF16)
+    cache = capi.dflash_cache_alloc(d, 1, 1, 256)
+    try:
+        capi.dflash_cache_set_lengths(cache, [16])
+        buf = torch.zeros(16 * 4 * 128 + 8, dtype=torch.bfloat16, device=dev())
+        q = buf[1:1 + 16 * 4 * 128]  # 2 bytes past an aligned base
+        out = torch.empty(1, 16, 4 * 128, dtype=torch.bfloat16, device=dev())
+        with pytest.raises(capi.DFlashError) as e:
+            capi.dflash_attention(d, q, 1, 16, 1, cache, 0, out, ws)
+        assert e.value.code == capi.ERR_INVALID_ARG
         assert capi.dflash_status(ws) == 0
     finally:
         capi.dflash_cache_free(cache)
