@@ -439,22 +439,29 @@ def run_ours(args, dist: Dist):
     # ---------------------------------------------------------------- end to end (host buffers)
     pin_k = torch.from_numpy(k_draw.astype(np.int32)).pin_memory()
     pin_r = torch.from_numpy(r_draw.astype(np.int32)).pin_memory()
-    out_acc = torch.zeros(nb, dtype=torch.int32).pin_memory()
-    out_tok = torch.zeros(nb * B, dtype=torch.int32).pin_memory()
+    # results come back into two pinned buffers: step i+1 is queued before the
+    # host waits for step i's copy, as a serving loop streaming tokens one step
+    # behind would do (the step itself needs nothing from the host)
+    out_acc = [torch.zeros(nb, dtype=torch.int32).pin_memory() for _ in range(2)]
+    out_tok = [torch.zeros(nb * B, dtype=torch.int32).pin_memory() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
     st_host = int(sess.step_ctr.item())
     torch.cuda.synchronize()
     e2e_tokens = 0
     t_e2e = time.perf_counter()
-    for i in range(K):
-        si = st_host + i
-        # this step's inputs from pinned host memory, its emitted tokens back
-        sess.k_draw[si].copy_(pin_k[si], non_blocking=True)
-        sess.r_draw[si].copy_(pin_r[si], non_blocking=True)
-        graph.replay()
-        out_acc.copy_(sess.accept_len, non_blocking=True)
-        out_tok.copy_(sess.argmax[:nb * B], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        e2e_tokens += int(out_acc.sum()) + nb
+    for i in range(K + 1):
+        if i < K:
+            si = st_host + i
+            # this step's inputs from pinned host memory, its emitted tokens back
+            sess.k_draw[si].copy_(pin_k[si], non_blocking=True)
+            sess.r_draw[si].copy_(pin_r[si], non_blocking=True)
+            graph.replay()
+            out_acc[i % 2].copy_(sess.accept_len, non_blocking=True)
+            out_tok[i % 2].copy_(sess.argmax[:nb * B], non_blocking=True)
+            done[i % 2].record()
+        if i >= 1:  # the previous step's results, read on the host
+            done[(i - 1) % 2].synchronize()
+            e2e_tokens += int(out_acc[(i - 1) % 2].sum()) + nb
     e2e_s = time.perf_counter() - t_e2e
     h2d = 2 * 4 * nb
     d2h = 4 * nb + 4 * nb * B
