@@ -93,6 +93,22 @@ def step_bytes(wl: synth.Workload, P_mean: float, batch=1):
     return weights + kv, weights, kv
 
 
+def stage_bytes(wl: synth.Workload, P_mean: float, batch=1):
+    """Algorithmic bytes of each stage of one step (the terms of step_bytes):
+    fuse reads W_fc; inject the drafter's K/V projections; draft every drafter
+    layer, the LM head and the drafter's keys/values; verify every target
+    layer, the LM head and the target's keys/values.  Teacher forcing and
+    accept move bytes per row only (counted 0)."""
+    s = wl.target
+    Wl = layer_weight_bytes(s)
+    lm = 2 * s.vocab * s.hidden
+    kv_pos = 2 * 2 * s.n_kv * s.head_dim
+    return {"fuse": 2 * s.hidden * 5 * s.hidden,
+            "inject": 2 * wl.draft_layers * 2 * s.n_kv * s.head_dim * s.hidden,
+            "draft": wl.draft_layers * Wl + lm + batch * wl.draft_layers * P_mean * kv_pos,
+            "teacher": 0, "verify": s.n_layers * Wl + lm + batch * s.n_layers * P_mean * kv_pos, "accept": 0}
+
+
 # ---------------------------------------------------------------------------
 # clocks
 # ---------------------------------------------------------------------------
@@ -505,6 +521,9 @@ def run_ours(args, dist: Dist):
     # ---------------------------------------------------------------- results
     P_mean = 0.5 * (float(np.mean(P_before)) + float(np.mean(P_after)))
     bytes_step, w_bytes, kv_bytes = step_bytes(wl, P_mean, batch=nb)
+    stage_med = {k: statistics.median(v) for k, v in stage_ms.items()}
+    stage_by = stage_bytes(wl, P_mean, batch=nb)
+    assert abs(sum(stage_by.values()) - bytes_step) < 1e-6 * bytes_step
     ms_step = statistics.median(step_ms)
     peak, peak_kind = measured_peaks()
     step_gbs = bytes_step / (ms_step / 1e3) / 1e9
@@ -537,8 +556,11 @@ def run_ours(args, dist: Dist):
                    "l2": "inputs larger than L2 (weights+KV read per step >> 129 MB)", "graph": "one CUDA graph per step"},
         "tau": tau,
         "bytes_per_step": bytes_step, "weight_bytes_per_step": w_bytes, "kv_bytes_per_step": kv_bytes,
-        "step_roofline": {"achieved_gbs": step_gbs, "peak_gbs": peak, "frac": step_gbs / peak, "peak_kind": peak_kind},
-        "stage_ms": {k: statistics.median(v) for k, v in stage_ms.items()},
+        "step_roofline": {"achieved_gbs": step_gbs, "peak_gbs": peak, "frac": step_gbs / peak, "peak_kind": peak_kind,
+                          "frac_of_8tbs": step_gbs / 8000.0},
+        "stage_ms": stage_med,
+        "stage_gbs": {k: (stage_by[k] / (stage_med[k] / 1e3) / 1e9 if stage_by[k] and stage_med[k] > 0 else None)
+                      for k in stage_med},
         "ar_tokens_per_s": ar_tok_s,
         "roofline": {"bound": "hbm", "kernel": "gemm_cl_kernel", "achieved": gemm_gbs, "peak": peak,
                      "unit": "GB/s", "frac": (gemm_gbs / peak) if gemm_gbs else None,
