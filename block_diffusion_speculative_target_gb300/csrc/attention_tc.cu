@@ -135,6 +135,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nrb = (n + 15) >> 4;
   const int qbox = min(16, batch * n);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {  // the descriptors are kernel parameters: fetch them while the previous kernel drains
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
   pdl_launch();
   pdl_wait();
 
