@@ -313,18 +313,24 @@ def _blas_threads():
 # ---------------------------------------------------------------------------
 
 
+def timed_tau(wl: synth.Workload, steps: int, warmup: int, rank: int = 0) -> float:
+    """Emitted tokens per step (summed over the batch) of the GPU arm's timed
+    steps for the same --steps/--warmup: its first, eager step takes draw 0 and
+    the warm-up replays draws 1..warmup, so the timed steps take the next
+    `steps` draws; a step emits min(k, B - 1) + 1 tokens per sequence.  The
+    reference arm divides by this, so both arms count the same tokens."""
+    k, _ = synth.acceptance_draws(1 + warmup + steps, wl.target.vocab, batch=wl.batch,
+                                  seed=synth.ACCEPT_SEED + rank)
+    k = k[1 + warmup:]
+    return float(np.mean(np.sum(np.minimum(k, wl.block - 1) + 1, axis=1)))
+
+
 def run_reference(args, dist: Dist):
     if dist.rank != 0:
         return
     wl = synth.WORKLOADS[args.workload]
     B = wl.block
-    # the acceptance draws of the GPU arm's timed steps for the same --steps/--warmup
-    # (its first, eager step takes draw 0, the warm-up replays draws 1..W), so that
-    # both arms divide by the same emitted tokens per step
-    K, W = max(args.steps, 1), args.warmup
-    k, _ = synth.acceptance_draws(1 + W + K, wl.target.vocab, batch=wl.batch)
-    k = k[1 + W:]
-    tau = float(np.mean(np.sum(np.minimum(k, B - 1) + 1, axis=1)))
+    tau = timed_tau(wl, max(args.steps, 1), args.warmup)
     P = int(round(np.mean(synth.prompt_lengths(wl))))
     for _ in range(args.warmup):
         oracle_step_sample(wl, 0.0, tau, P, repeats=1, batch=wl.batch)
