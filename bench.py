@@ -36,12 +36,12 @@ import synth  # noqa: E402
 METRIC = "emitted tokens/s per step (draft block+verify) at 4K/36K ctx; % of HBM roofline"
 UNIT = "tokens/s"
 
-# DRAM bytes (read + write) per gemm_cl_kernel launch, averaged over the 168
-# weight-product launches of one step of the 4K workload, from the ncu launch
-# list in profiles/launches__bench_qwen3-8b-4k.md.  Set to None whenever the
-# kernel changes until a new capture is taken.
-GEMM_TRAFFIC = {"workload": "qwen3-8b-4k", "bytes_per_launch": 111039901,
-                "source": "profiles/launches__bench_qwen3-8b-4k.md"}
+# DRAM bytes (read + write) per gemm_cl_kernel launch, averaged over the
+# weight-product launches of one step of the 4K workload, from an ncu launch
+# list of this command (gpu__time_duration.sum, dram__bytes_read.sum,
+# dram__bytes_write.sum over the timed graph replays).  None whenever the
+# kernel has changed since the counters were taken.
+GEMM_TRAFFIC = {"workload": "qwen3-8b-4k", "bytes_per_launch": None}
 
 
 def parse():
@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the CPU-baseline sample")
+    ap.add_argument("--also", nargs="*", default=["dense27b-36k"],
+                    help="further workloads measured after the main one (one GPU only); empty to skip")
     return ap.parse_args()
 
 
@@ -77,25 +79,28 @@ def layer_weight_bytes(s, es=2):
 
 
 def step_bytes(wl: synth.Workload, P_mean: float, batch=1):
-    """Weights read once per step plus keys/values read, bf16.
+    """Algorithmic bytes of one step: every weight matrix once plus the
+    keys/values read, bf16.
 
     verify: every target layer + LM head; draft: every drafter layer + LM head;
-    fuse: W_fc; inject: the drafter's K/V projections; attention: target and
-    drafter keys+values for P positions (per sequence)."""
+    fuse: W_fc; attention: target and drafter keys+values for P positions (per
+    sequence).  The injection projects with the drafter layers' own W_k/W_v,
+    which the drafter layers already count, so it adds no bytes (the library
+    streams a packed copy of them, which the roofline does not credit)."""
     s = wl.target
     Wl = layer_weight_bytes(s)
     lm = 2 * s.vocab * s.hidden
     fc = 2 * s.hidden * 5 * s.hidden
-    inj = 2 * wl.draft_layers * 2 * s.n_kv * s.head_dim * s.hidden
     kv_pos = 2 * 2 * s.n_kv * s.head_dim  # K and V, bf16, per layer per position
-    weights = s.n_layers * Wl + lm + wl.draft_layers * Wl + lm + fc + inj
+    weights = s.n_layers * Wl + lm + wl.draft_layers * Wl + lm + fc
     kv = batch * (s.n_layers + wl.draft_layers) * P_mean * kv_pos
     return weights + kv, weights, kv
 
 
 def stage_bytes(wl: synth.Workload, P_mean: float, batch=1):
     """Algorithmic bytes of each stage of one step (the terms of step_bytes):
-    fuse reads W_fc; inject the drafter's K/V projections; draft every drafter
+    fuse reads W_fc; inject nothing of its own (the drafter layers' W_k/W_v
+    are counted with the draft stage); draft every drafter
     layer, the LM head and the drafter's keys/values; verify every target
     layer, the LM head and the target's keys/values.  Teacher forcing and
     accept move bytes per row only (counted 0)."""
@@ -104,7 +109,7 @@ def stage_bytes(wl: synth.Workload, P_mean: float, batch=1):
     lm = 2 * s.vocab * s.hidden
     kv_pos = 2 * 2 * s.n_kv * s.head_dim
     return {"fuse": 2 * s.hidden * 5 * s.hidden,
-            "inject": 2 * wl.draft_layers * 2 * s.n_kv * s.head_dim * s.hidden,
+            "inject": 0,
             "draft": wl.draft_layers * Wl + lm + batch * wl.draft_layers * P_mean * kv_pos,
             "teacher": 0, "verify": s.n_layers * Wl + lm + batch * s.n_layers * P_mean * kv_pos, "accept": 0}
 
@@ -350,7 +355,11 @@ def run_reference(args, dist: Dist):
         "config": {"workload": wl.name, "batch": wl.batch, "block": B, "context": P, "target_layers": wl.target.n_layers,
                    "draft_layers": wl.draft_layers},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+                         "extrapolated": True,
                          "sample": desc + f"; {args.steps} timed samples, wall {wall:.1f} s"},
+        "extrapolated": True,
+        "extrapolation": "ms_per_step is the layer-count extrapolation of one sample per step (see "
+                         "cpu_baseline.sample), not the wall time of a whole step",
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -376,16 +385,18 @@ def build_model(wl, device):
     return m
 
 
-def run_ours(args, dist: Dist):
+def measure_ours(wl: synth.Workload, args, dist: Dist) -> dict:
+    """Build the workload's model, prefill, decode the greedy reference stream,
+    then time K teacher-forced steps replayed from one CUDA graph (device
+    timing), the same steps with host buffers (e2e), and eager passes per
+    stage and per weight product.  Returns the JSON line's fields; every
+    device allocation is released before returning."""
     import torch
 
     from block_diffusion_speculative_target_gb300 import capi
     from block_diffusion_speculative_target_gb300.engine import Session
 
-    torch.cuda.set_device(dist.local)
     dev = torch.device("cuda", dist.local)
-    capi.load()
-    wl = synth.WORKLOADS[args.workload]
     s = wl.target
     B, V, nb = wl.block, s.vocab, wl.batch
     lens0 = synth.prompt_lengths(wl)
@@ -523,6 +534,7 @@ def run_ours(args, dist: Dist):
     gemm_bytes = sum(kb * 1024.0 for _, kb in chains)
     gemm_ms = sum(ms for ms, _ in chains)
     gemm_gbs = gemm_bytes / (gemm_ms / 1e3) / 1e9 if gemm_ms > 0 else None
+    gemm_bytes_step = gemm_bytes / PS
 
     # ---------------------------------------------------------------- results
     P_mean = 0.5 * (float(np.mean(P_before)) + float(np.mean(P_after)))
@@ -546,7 +558,7 @@ def run_ours(args, dist: Dist):
                     + [f"draft.layers.0.{p}" for p in synth.LAYER_PARTS]}
             v, t_step, desc, thr = oracle_step_sample(wl, args.cpu_seconds, tau, int(round(np.mean(lens0))),
                                                       weights_dev=need, batch=nb)
-            cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc}
+            cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle", "extrapolated": True, "sample": desc}
         except Exception as e:  # the baseline is reported, never required
             cpu = {"value": None, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                    "sample": f"failed: {type(e).__name__}: {e}"}
@@ -572,10 +584,14 @@ def run_ours(args, dist: Dist):
                      "unit": "GB/s", "frac": (gemm_gbs / peak) if gemm_gbs else None,
                      "traffic": GEMM_TRAFFIC["bytes_per_launch"] if wl.name == GEMM_TRAFFIC["workload"] else None,
                      "algorithmic_bytes_per_launch": gemm_bytes / len(chains) if chains else None,
-                     "peak_kind": peak_kind,
-                     "note": f"{len(chains)} weight-product launches over {PS} eager steps; achieved = weight "
-                             f"bytes of each launch / its CUDA-event duration, summed; traffic = ncu DRAM read+write "
-                             f"bytes per launch from {GEMM_TRAFFIC['source']}"},
+                     "peak_kind": peak_kind, "timing": "eager",
+                     "frac_in_graph_lower_bound": gemm_bytes_step / (ms_step / 1e3) / 1e9 / peak,
+                     "note": f"{len(chains)} weight-product launches over {PS} eager steps (events around each "
+                             f"launch, so no overlap with its neighbours: an upper bound on the kernel's time in the "
+                             f"graph); achieved = weight bytes of the launches / their summed CUDA-event durations; "
+                             f"frac_in_graph_lower_bound = the products' bytes per step / the whole graph-timed step; "
+                             f"traffic = ncu DRAM read+write bytes per launch (null until recaptured for this "
+                             f"kernel)"},
         "clocks": clk,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(kernels_per_step * K),
@@ -585,6 +601,36 @@ def run_ours(args, dist: Dist):
         "prefill_s": t_prefill,
     }
     sess.close()
+    del graph, sess, m
+    import gc
+
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
+
+
+# Keys of a second workload's measurement carried in the main line.
+SUB_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "tau", "bytes_per_step", "step_roofline",
+            "stage_ms", "stage_gbs", "roofline", "clocks", "e2e", "gpu_launches", "kernels_per_step", "cpu_baseline",
+            "ar_tokens_per_s", "setup_s", "prefill_s")
+
+
+def run_ours(args, dist: Dist):
+    import torch
+
+    from block_diffusion_speculative_target_gb300 import capi
+
+    torch.cuda.set_device(dist.local)
+    capi.load()
+    line = measure_ours(synth.WORKLOADS[args.workload], args, dist)
+    # the metric is quoted at 4K and 36K: one GPU also measures the 27B-class
+    # shapes at a 36K context, after the first model has been released
+    if dist.world == 1:
+        for name in args.also:
+            if name and name != args.workload:
+                sub = measure_ours(synth.WORKLOADS[name], args, dist)
+                line.setdefault("also", {})[name] = {k: sub[k] for k in SUB_KEYS if k in sub}
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -70,6 +70,8 @@ _SIGS = {
     "dflash_workspace_alloc": (_I, [POINTER(ModelDesc), POINTER(ModelDesc), _I, _I, POINTER(c_void_p)]),
     "dflash_workspace_free": (_I, [_P]),
     "dflash_status": (_I, [_P, _P, POINTER(c_int32)]),
+    "dflash_workspace_logits": (c_void_p, [_P]),
+    "dflash_debug_set_wait_limit": (_I, [ctypes.c_int64]),
     "dflash_fuse_features": (_I, [POINTER(DraftC), _P, _I, _P, _P, _P]),
     "dflash_inject_kv": (_I, [POINTER(DraftC), _P, _I, _I, _P, _P, _P, _P]),
     "dflash_draft_block": (_I, [POINTER(DraftC), POINTER(TargetC), _P, _I, _I, _P, _P, _P, _P]),
@@ -206,6 +208,33 @@ def dflash_status(ws, stream=None):
     v = c_int32()
     _check(load().dflash_status(ws, _stream(stream), ctypes.byref(v)), "dflash_status")
     return v.value
+
+
+def dflash_workspace_logits(ws, rows, vocab):
+    """The workspace's float32 logits [rows][vocab] as a torch tensor view
+    (device memory owned by the workspace; valid until the next call)."""
+    import torch
+
+    p = load().dflash_workspace_logits(ws)
+    if not p:
+        raise DFlashError("dflash_workspace_logits: no workspace")
+    return _device_view(p, rows * vocab, torch.float32).view(rows, vocab)
+
+
+def _device_view(ptr, numel, dtype):
+    """A torch tensor over `numel` elements of library-owned device memory."""
+    import torch
+
+    class _Mem:
+        def __init__(self, p, n, dt):
+            self.__cuda_array_interface__ = {"shape": (n,), "typestr": {torch.float32: "<f4", torch.int32: "<i4"}[dt],
+                                             "data": (p, False), "version": 3}
+
+    return torch.as_tensor(_Mem(ptr, numel, dtype), device="cuda")
+
+
+def dflash_debug_set_wait_limit(ns):
+    _check(load().dflash_debug_set_wait_limit(int(ns)), "dflash_debug_set_wait_limit")
 
 
 # ---------------------------------------------------------------- stages

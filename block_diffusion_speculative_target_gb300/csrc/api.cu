@@ -326,6 +326,13 @@ int dflash_workspace_free(dflash_workspace* w) {
   return DFLASH_OK;
 }
 
+float* dflash_workspace_logits(dflash_workspace* w) { return w ? w->logits : nullptr; }
+
+int dflash_debug_set_wait_limit(int64_t ns) {
+  set_gemm_wait_ns((long long)ns);
+  return DFLASH_OK;
+}
+
 int dflash_status(dflash_workspace* w, dflash_stream_t stream, int32_t* status_out) {
   REQ(w && status_out);
   int32_t v = 0;

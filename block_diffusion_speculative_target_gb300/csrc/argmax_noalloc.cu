@@ -21,19 +21,50 @@ static __device__ __align__(256) int g_tickets[kMaxRows];
 
 struct Slot {
   std::atomic<bool> ready{false};
+  std::atomic<unsigned long long> ctx_id{0};  // unique id of the context the addresses belong to
   float4* part = nullptr;
   int* tickets = nullptr;
 };
 Slot g_slot[kMaxDevices];
 std::mutex g_setup_mu;
 
-// Resolves the device addresses of the scratch arrays on the current device,
-// once per device; a failed lookup is not cached, so the next call retries.
+typedef CUresult (*PFN_ctxGetCurrent_t)(CUcontext*);
+typedef CUresult (*PFN_ctxGetId_t)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 when there is none or
+// the driver cannot tell).  A device reset ends the context; the next one gets
+// a new id, so addresses looked up in the old one are never reused.
+unsigned long long current_ctx_id() {
+  static PFN_ctxGetCurrent_t get_cur = nullptr;
+  static PFN_ctxGetId_t get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_ctxGetCurrent_t>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_ctxGetId_t>(p);
+  });
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_cur || !get_id || get_cur(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Resolves the device addresses of the scratch arrays in the current context
+// of device `dev`: once per context (again after the context changes, e.g.
+// after cudaDeviceReset); a failed lookup is not cached, so the next call
+// retries.
 cudaError_t scratch_of(int dev, dfl::ArgmaxScratch* out) {
   Slot& s = g_slot[dev];
-  if (!s.ready.load(std::memory_order_acquire)) {
+  const unsigned long long id = current_ctx_id();
+  if (!s.ready.load(std::memory_order_acquire) || id == 0 || s.ctx_id.load(std::memory_order_acquire) != id) {
     std::lock_guard<std::mutex> lk(g_setup_mu);
-    if (!s.ready.load(std::memory_order_relaxed)) {
+    if (!s.ready.load(std::memory_order_relaxed) || id == 0 || s.ctx_id.load(std::memory_order_relaxed) != id) {
+      s.ready.store(false, std::memory_order_relaxed);
       void* p = nullptr;
       void* t = nullptr;
       cudaError_t e = cudaGetSymbolAddress(&p, g_part);
@@ -42,6 +73,7 @@ cudaError_t scratch_of(int dev, dfl::ArgmaxScratch* out) {
       if (e != cudaSuccess) return e;
       s.part = static_cast<float4*>(p);
       s.tickets = static_cast<int*>(t);
+      s.ctx_id.store(id, std::memory_order_release);
       s.ready.store(true, std::memory_order_release);
     }
   }
@@ -60,7 +92,7 @@ extern "C" int dflash_argmax_noalloc(const float* logits, int32_t rows, int32_t 
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return dfl::record_cuda_error(e);
-  if (dev < 0 || dev >= kMaxDevices) return DFLASH_ERR_TOO_LARGE;
+  if (dev < 0 || dev >= kMaxDevices) return DFLASH_ERR_INVALID_ARG;  // more devices than the table holds
   dfl::ArgmaxScratch sc;
   e = scratch_of(dev, &sc);
   if (e != cudaSuccess) return dfl::record_cuda_error(e);

@@ -75,9 +75,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase with the given parity to complete, giving up after
-// `limit_ns` nanoseconds.  Returns false on time-out.  The clock is read only
-// every 128 polls so that a completing phase is seen without delay.
+// `limit_ns` nanoseconds.  Returns false on time-out; a limit of 0 has expired
+// before the first poll.  The clock is read only every 128 polls so that a
+// completing phase is seen without delay.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns == 0) return false;
 #pragma unroll 1
   for (int i = 0; i < 128; ++i)
     if (mbar_try_wait(bar, parity)) return true;

@@ -24,6 +24,7 @@
 // write at each row's position.
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -32,6 +33,13 @@
 namespace dfl {
 
 constexpr uint64_t kGemmWaitNs = 500000000ull;  // 500 ms per wait
+
+// Limit of the main-loop waits (ring slots, accumulator); the drain after a
+// time-out always waits the full kGemmWaitNs / 4 so that copies and products
+// in flight complete before shared memory and TMEM are released.  Lowered only
+// by dflash_debug_set_wait_limit (failure-path tests).
+static std::atomic<unsigned long long> g_wait_ns{kGemmWaitNs};
+void set_gemm_wait_ns(long long ns) { g_wait_ns.store(ns < 0 ? kGemmWaitNs : (unsigned long long)ns); }
 
 template <int BN, int STAGES>
 struct ClCfg {
@@ -184,7 +192,7 @@ __device__ __forceinline__ void gemm_epi(const GemmEpi& e, int n, int m, float v
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(128)
     gemm_cl_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const GemmEpi epi,
-                   const int rows, const int K, const int S, int* status) {
+                   const int rows, const int K, const int S, int* status, const uint64_t wait_ns) {
   using C = ClCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -251,7 +259,7 @@ __global__ void __launch_bounds__(128)
       issued = pre;
       for (int kb = pre; kb < nkb; ++kb) {
         const int s = kb % STAGES;
-        if (!mbar_wait(&empty[s], (uint32_t)((kb / STAGES) - 1) & 1u, kGemmWaitNs) || flags[0]) {
+        if (!mbar_wait(&empty[s], (uint32_t)((kb / STAGES) - 1) & 1u, wait_ns) || flags[0]) {
           flags[0] = 1;
           set_status(status, DFLASH_STATUS_TIMEOUT);
           break;
@@ -288,7 +296,7 @@ __global__ void __launch_bounds__(128)
       constexpr uint32_t idesc = idesc_bf16_f32(C::BM, BN);
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % STAGES;
-        if (!mbar_wait(&full[s], (uint32_t)(kb / STAGES) & 1u, kGemmWaitNs)) {
+        if (!mbar_wait(&full[s], (uint32_t)(kb / STAGES) & 1u, wait_ns)) {
           flags[0] = 1;
           set_status(status, DFLASH_STATUS_TIMEOUT);
           break;
@@ -306,14 +314,15 @@ __global__ void __launch_bounds__(128)
   }
 
   // ---------------------------------------------------------------- epilogue
-  if (threadIdx.x == 0 && !mbar_wait(accb, 0, kGemmWaitNs)) {
+  if (threadIdx.x == 0 && !mbar_wait(accb, 0, wait_ns)) {
     flags[0] = 1;
     set_status(status, DFLASH_STATUS_TIMEOUT);
   }
   __syncthreads();
-  // Drain: after a time-out, wait (bounded) for loads still in flight before
-  // the ring is reused or released.
+  // Drain: after a time-out, wait (bounded) for the products and the loads
+  // still in flight before the ring and TMEM are reused or released.
   if (flags[0] && warp == 0 && lane == 0) {
+    mbar_wait(accb, 0, kGemmWaitNs / 4);
     const int first = issued > STAGES ? issued - STAGES : 0;
     for (int i = first; i < issued; ++i) mbar_wait(&full[i % STAGES], (uint32_t)(i / STAGES) & 1u, kGemmWaitNs / 4);
   }
@@ -526,7 +535,8 @@ static cudaError_t launch_cl(const CUtensorMap& tw, const CUtensorMap& tx, const
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   count_launch();
-  return cudaLaunchKernelEx(&cfg, gemm_cl_kernel<BN, STAGES>, tw, tx, epi, rows, K, S, status);
+  return cudaLaunchKernelEx(&cfg, gemm_cl_kernel<BN, STAGES>, tw, tx, epi, rows, K, S, status,
+                            (uint64_t)g_wait_ns.load(std::memory_order_relaxed));
 }
 
 cudaError_t gemm_bf16(const void* X, int ldx, int rows, const void* W, int M, int K, const GemmEpi& epi, int* status,

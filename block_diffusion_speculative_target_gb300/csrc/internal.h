@@ -58,6 +58,9 @@ struct GemmEpi {
 // bf16 weight product on tcgen05 with cluster split-K (M % 128 == 0, K % 64 == 0, rows <= 128).
 cudaError_t gemm_bf16(const void* X, int ldx, int rows, const void* W, int M, int K, const GemmEpi& epi, int* status,
                       cudaStream_t s);
+// Limit of the weight product's main-loop waits in nanoseconds (< 0: the
+// default 500 ms); see dflash_debug_set_wait_limit.
+void set_gemm_wait_ns(long long ns);
 // K splits (cluster size) for an [M x K] weight: depends on M, K and the SM count only.
 int gemm_splits(int M, int K);
 

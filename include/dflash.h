@@ -157,6 +157,21 @@ int dflash_workspace_alloc(const dflash_model_desc *target, const dflash_model_d
 int dflash_workspace_free(dflash_workspace *w);
 /* Synchronises `stream`, returns the status bits in *status_out and clears them. */
 int dflash_status(dflash_workspace *w, dflash_stream_t stream, int32_t *status_out);
+/* Device pointer to the workspace's float32 logits, row-major [rows][vocab]:
+ * after target_verify (rows = batch * n) or dflash_draft_block (rows =
+ * batch * block) they hold that call's logits, the last RMSNorm'd residual
+ * times the LM head ([DD] §1.1: the target's next-token scores), until the
+ * next call on the workspace overwrites them.  Owned by the workspace; NULL
+ * for a NULL workspace.  No synchronisation: read it on the same stream. */
+float *dflash_workspace_logits(dflash_workspace *w);
+/* Failure-path testing: sets the limit, in nanoseconds, of the waits in the
+ * main loop of the weight-product kernel (ring slots and accumulator) for
+ * launches enqueued afterwards; a negative value restores the default of
+ * 500 ms.  A limit of 0 expires at once, so the kernel gives up, sets
+ * DFLASH_STATUS_TIMEOUT, still waits (with the default limit) for its copies
+ * and products in flight, writes no result and returns.  Process-wide; not an
+ * operation of the method. */
+int dflash_debug_set_wait_limit(int64_t ns);
 const char *dflash_strerror(int code);
 
 /* Captured layers for a target of n_layers: 5 layers spread uniformly from
@@ -253,7 +268,8 @@ int dflash_linear(int32_t dtype, const void *x, const void *w, float *y, int32_t
 /* y = x / sqrt(mean(x^2) + eps) * gain, x float32 [rows][H] -> y dtype. */
 int dflash_rmsnorm(int32_t dtype, const float *x, const void *gain, void *y, int32_t rows,
                    int32_t H, float eps, dflash_stream_t stream);
-/* Greedy token and top-2 gap of float32 logits [rows][V]. */
+/* Greedy token and top-2 gap of float32 logits [rows][V] ([DD] §1.1 greedy
+ * choice; lowest index on ties). */
 int dflash_argmax(const float *logits, int32_t rows, int32_t V, int32_t *argmax, float *gap,
                   dflash_workspace *ws, dflash_stream_t stream);
 /* dflash_argmax without a workspace.  Not an operation of the method (the
@@ -270,10 +286,13 @@ int dflash_argmax(const float *logits, int32_t rows, int32_t V, int32_t *argmax,
  *   DFLASH_ARGMAX_NOALLOC_MAX_ROWS rows; rows above it return
  *   DFLASH_ERR_TOO_LARGE before any CUDA call.  The library calls no
  *   allocator on this path.
- *   Set-up: the first call on each device, with that device current, resolves
- *   the array's address (cudaGetSymbolAddress, return code checked; a failure
- *   returns DFLASH_ERR_CUDA and the next call retries).  Make that first call
- *   before any stream capture begins.
+ *   Set-up: the first call in each CUDA context (per device, with that device
+ *   current) resolves the array's address (cudaGetSymbolAddress, return code
+ *   checked; a failure returns DFLASH_ERR_CUDA and the next call retries).
+ *   The library remembers the context's unique id and resolves again when it
+ *   changes, e.g. after cudaDeviceReset.  Make the first call in a context
+ *   before any stream capture begins.  Devices with an ordinal of 64 or more
+ *   return DFLASH_ERR_INVALID_ARG.
  *   Each call clears the rows' tickets (an asynchronous memset on `stream`)
  *   and launches one kernel.  All calls on a device share the one array:
  *   calls that overlap in time (other streams, other host threads) race on

@@ -358,7 +358,7 @@ def inject_kv(dr: Draft, fused, positions, rnd):
     return out
 
 
-def draft_forward(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rnd):
+def draft_logits(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rnd):
     """One non-causal drafter forward over the block [anchor, MASK x (B-1)] at
     positions P..P+B-1 (P = drafter cache length): [DD] §5.1 "given [T1] +
     target_model_context -> single forward pass -> [T2,...]", §2.2
@@ -368,7 +368,8 @@ def draft_forward(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rn
     parity unpinned: the sub-layer order of the drafter (pre-norm attention,
     then pre-norm SwiGLU, then a final RMSNorm) is not printed on any page.
 
-    Returns the B drafted tokens, slot 0 holding the anchor itself."""
+    Returns the logits [B-1, V] of slots 1..B-1 (slot 0 holds the anchor,
+    whose logits are not used)."""
     sh = dr.shape
     P = dcache.length()
     toks = np.array([anchor] + [dr.mask_id] * (block - 1), dtype=np.int64)
@@ -376,8 +377,14 @@ def draft_forward(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rn
     for li, lw in enumerate(dr.layers):
         x, _, _ = decoder_layer(x, lw, sh, dcache.k[li], dcache.v[li], P, False, rnd)
     z = rnd(rmsnorm(x, dr.final_norm, sh.eps))
-    logits = linear(z[1:], tg.lm_head)
-    am, gap = argmax_top2(logits)
+    return linear(z[1:], tg.lm_head)
+
+
+def draft_forward(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rnd):
+    """The drafter's greedy block: argmax of each slot's logits
+    (``draft_logits``).  Returns the B drafted tokens, slot 0 holding the
+    anchor itself, and the top-2 gaps of slots 1..B-1."""
+    am, gap = argmax_top2(draft_logits(dr, tg, anchor, block, dcache, rnd))
     return np.concatenate([[anchor], am]).astype(np.int64), gap
 
 

@@ -8,22 +8,28 @@ over the full 36K context, a full-width verify/draft/fuse/inject on a
 synthetic 4K cache.  Greedy losslessness (speculative stream == greedy AR
 stream, accepted lengths == the teacher-forced draws) is a property that
 holds at any size and is checked on the whole 36-layer 4K model and on the
-27B-class widths at a 36K prompt (8 layers).
+full 64-layer 27B-class model at a 36K prompt.
 
 Single-stage outputs (a GEMM, attention, fused features, injected keys and
-values, the first layer's keys and values) are held to the bf16 max-abs bound
-2e-2.  Outputs of a stack of layers carry the bf16 noise floor (see
-gpu_util.assert_close_stack): at these widths it puts about 1e-2 of noise on
-each logit, so greedy tokens must agree where the oracle's top-2 gap exceeds
-twice the logit bound (GAP_TOL), and captured states and deep keys/values are
-checked against the noise-floor bounds."""
+values) are held to the stated bf16 max-abs bound 2e-2.  Outputs of a stack of
+layers (captured states, each layer's keys and values, logits, greedy tokens)
+are held to the stated bounds widened, where needed, to twice the bf16 noise
+floor that the oracle alone reaches at these widths (float64 vs
+float32-accumulated products, tests/golden/noise_floor.json): no
+float32-accumulating implementation can be held tighter.  Every comparison's
+error, and whether it meets the stated bound, goes to the report named by
+DFLASH_PARITY_REPORT when that is set."""
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
 
 from conftest import oracle_models, shrink
-from gpu_util import (GAP_TOL, O, Model, Session, assert_close, assert_close_stack, capi, check_tokens, dev, rounder,
-                      synth, to_dev, to_np)
+from gpu_util import (GAP_TOL, TOL, O, Model, Session, assert_close, capi, check_tokens, dev, oracle_logits_along,
+                      rounder, synth, to_dev, to_np)
+from tolerances import FLOOR_MARGIN, floor_bound, floor_of, token_gap_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -118,16 +124,46 @@ def _device_model(wl):
     return m, tg, dr
 
 
-@pytest.fixture(scope="module")
-def wide():
-    """Qwen3-8B widths (hidden 4096, 32/8 heads, FFN 12288, vocab 151936) with
-    6 target layers (the fewest that hold 5 capture points) and the full 5
-    drafter layers."""
-    wl = shrink(QWEN, n_layers=6)
+@pytest.fixture(scope="module", params=["qwen3-8b-4k", "dense27b-36k"])
+def wide(request):
+    """The workload's widths (Qwen3-8B: hidden 4096, 32/8 heads, FFN 12288;
+    27B-class: hidden 5120, 40/8 heads, FFN 25600; vocab 151936) with 6 target
+    layers (the fewest that hold 5 capture points) and the full 5 drafter
+    layers."""
+    name = request.param
+    wl = shrink(synth.WORKLOADS[name], n_layers=6)
     m, tg, dr = _device_model(wl)
-    yield wl, m, tg, dr
+    yield name, wl, m, tg, dr
     del m
     torch.cuda.empty_cache()
+
+
+def _record(rec):
+    """Append one comparison to the JSON-lines report named by
+    DFLASH_PARITY_REPORT (no report when unset)."""
+    path = os.environ.get("DFLASH_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(rec) + "\n")
+
+
+def _check_float(name, stage, output, got, ref, stated=TOL["bf16"]):
+    """Max-abs and relative-Frobenius error of a full-width output against the
+    floor-derived bounds (the stated bound, widened to FLOOR_MARGIN x the
+    oracle-only floor where the floor exceeds it).  The error against the
+    stated bound is recorded as well, met or not."""
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    d = got - ref
+    err = float(np.max(np.abs(d)))
+    fro = float(np.linalg.norm(d) / max(np.linalg.norm(ref), 1e-300))
+    b_abs = floor_bound(name, stage, output, stated)
+    b_fro = FLOOR_MARGIN * floor_of(name, stage, output, "rel_fro")
+    _record({"workload": name, "stage": stage, "output": output, "max_abs": err, "rel_fro": fro,
+             "floor_max_abs": floor_of(name, stage, output), "floor_rel_fro": floor_of(name, stage, output, "rel_fro"),
+             "bound_max_abs": b_abs, "stated": stated, "meets_stated": err <= stated})
+    assert err <= b_abs, f"{name} {stage} {output}: max-abs {err:.3e} > {b_abs:.3e}"
+    if b_abs > stated:  # held to the floor: the error's spread is bounded by the floor's too
+        assert fro <= b_fro, f"{name} {stage} {output}: rel Frobenius {fro:.3e} > {b_fro:.3e}"
 
 
 def _synthetic_cache(wl, cache, n_layers, P, seed):
@@ -142,38 +178,42 @@ def _synthetic_cache(wl, cache, n_layers, P, seed):
     return kv
 
 
+CTX = 4096  # synthetic context of the full-width stage checks
+
+
 def test_verify_full_width(wide):
-    wl, m, tg, dr = wide
-    sh, B, P = wl.target, wl.block, wl.prompt_len
+    name, wl, m, tg, dr = wide
+    sh, B, P = wl.target, wl.block, CTX
     s = Session(m, batch=1, capacity=P + 64, block=B)
     kv = _synthetic_cache(wl, s.tcache, sh.n_layers, P, seed=64)
     toks = synth.prompt_tokens(B, sh.vocab, stream=65)
     tgc, _ = m.structs()
     capi.target_verify(tgc, to_dev(toks.astype(np.int32), torch.int32), 1, B, 0, s.tcache, s.argmax, s.gap, s.hcap,
                        None, None, None, None, 0, s.ws)
+    logits = to_np(capi.dflash_workspace_logits(s.ws, B, sh.vocab))
     ref = O.target_forward(tg, toks, kv, rounder(wl))
-    check_tokens(s.argmax[:B].cpu().numpy(), ref.argmax, ref.gap, "bf16", "full-width verify argmax",
-                 bound=GAP_TOL["bf16"])
-    assert_close(s.gap[:B].cpu().numpy(), ref.gap, "bf16", "full-width verify top-2 gap", tol=GAP_TOL["bf16"])
-    assert_close_stack(to_np(s.hcap[:B]), ref.hcap, "full-width verify captured states")
+    tb = token_gap_bound(name, "verify")
+    n_tie = check_tokens(s.argmax[:B].cpu().numpy(), ref.argmax, ref.gap, "bf16", "full-width verify argmax", bound=tb)
+    _record({"workload": name, "stage": "verify", "output": "tokens", "token_gap_bound": tb, "exempt": n_tie,
+             "differ_above_stated_1e-2": int(np.sum((s.argmax[:B].cpu().numpy() != ref.argmax) & (ref.gap > 1e-2)))})
+    gap_bound = max(GAP_TOL["bf16"], FLOOR_MARGIN * floor_of(name, "verify", "tokens", "max_gap_change"))
+    assert_close(s.gap[:B].cpu().numpy(), ref.gap, "bf16", "full-width verify top-2 gap", tol=gap_bound)
+    _check_float(name, "verify", "logits", logits, ref.logits)
+    _check_float(name, "verify", "hcap", to_np(s.hcap[:B]), ref.hcap)
     for li in range(sh.n_layers):
         k = torch.empty(sh.n_kv, B, sh.head_dim, dtype=torch.bfloat16, device=dev())
         v = torch.empty_like(k)
         capi.dflash_cache_read(s.tcache, li, 0, P, B, k, v)
         kg, vg = np.transpose(to_np(k), (1, 0, 2)), np.transpose(to_np(v), (1, 0, 2))
-        if li == 0:  # one rounding stage from identical inputs
-            assert_close(kg, ref.new_k[li], "bf16", "verify K layer 0")
-            assert_close(vg, ref.new_v[li], "bf16", "verify V layer 0")
-        else:
-            assert_close_stack(kg, ref.new_k[li], f"verify K layer {li}")
-            assert_close_stack(vg, ref.new_v[li], f"verify V layer {li}")
+        _check_float(name, "verify", f"k{li}", kg, ref.new_k[li])
+        _check_float(name, "verify", f"v{li}", vg, ref.new_v[li])
     assert s.status() == 0
     s.close()
 
 
 def test_draft_full_width(wide):
-    wl, m, tg, dr = wide
-    sh, B, P = wl.target, wl.block, wl.prompt_len
+    name, wl, m, tg, dr = wide
+    sh, B, P = wl.target, wl.block, CTX
     s = Session(m, batch=1, capacity=P + 64, block=B)
     kv = _synthetic_cache(wl, s.dcache, wl.draft_layers, P, seed=66)
     anchor = int(synth.prompt_tokens(1, sh.vocab, stream=67)[0])
@@ -181,16 +221,22 @@ def test_draft_full_width(wide):
     tgc, drc = m.structs()
     capi.dflash_draft_block(drc, tgc, s.anchor, 1, B, s.dcache, s.draft, s.ws)
     got = s.draft.cpu().numpy()[0]
-    ref, gap = O.draft_forward(dr, tg, anchor, B, kv, rounder(wl))
+    logits = to_np(capi.dflash_workspace_logits(s.ws, B, sh.vocab))[1:]
+    ref_logits = O.draft_logits(dr, tg, anchor, B, kv, rounder(wl))
+    ref_tok, gap = O.argmax_top2(ref_logits)
     assert got[0] == anchor
-    check_tokens(got[1:], ref[1:], gap, "bf16", "full-width draft tokens", bound=GAP_TOL["bf16"])
+    tb = token_gap_bound(name, "draft")
+    n_tie = check_tokens(got[1:], ref_tok, gap, "bf16", "full-width draft tokens", bound=tb)
+    _record({"workload": name, "stage": "draft", "output": "tokens", "token_gap_bound": tb, "exempt": n_tie,
+             "differ_above_stated_1e-2": int(np.sum((got[1:] != ref_tok) & (gap > 1e-2)))})
+    _check_float(name, "draft", "logits", logits, ref_logits)
     assert s.status() == 0
     s.close()
 
 
 def test_fuse_inject_full_width(wide):
-    wl, m, tg, dr = wide
-    sh, B, P = wl.target, wl.block, wl.prompt_len
+    name, wl, m, tg, dr = wide
+    sh, B, P = wl.target, wl.block, CTX
     rnd = rounder(wl)
     hcap = synth.to_bf16_f32(synth.gaussian((B, 5 * sh.hidden), seed=68, scale=2.0))
     s = Session(m, batch=1, capacity=P + 64, block=B)
@@ -212,6 +258,40 @@ def test_fuse_inject_full_width(wide):
         assert_close(np.transpose(to_np(v), (1, 0, 2)), inj[li][1], "bf16", f"full-width injected V l={li}")
     assert s.status() == 0
     s.close()
+
+
+def test_greedy_stream_matches_oracle_full_width(wide):
+    """The GPU's greedy stream at full width (6 target layers, 256-token
+    prompt, 40 tokens) against the oracle's greedy choice after the GPU's own
+    prefix, wherever the oracle's top-2 gap exceeds the token bound; and the
+    teacher-forced speculative stream equals it bit for bit."""
+    name, wl, m, tg, dr = wide
+    sh, B = wl.target, wl.block
+    P0, n_tok, steps = 256, 40, 4
+    prompt = synth.prompt_tokens(P0, sh.vocab, stream=68)
+    cap = P0 + (steps + 2) * B + n_tok + 64
+    ar = Session(m, batch=1, capacity=cap, block=B, with_draft=False, stream_cap=cap)
+    ar.prefill([prompt], inject=False)
+    for _ in range(max(n_tok, (steps + 1) * B) - 1):
+        ar.ar_step()
+    G = ar.emitted()[0]
+    assert ar.status() == 0
+    ar.close()
+    exp, gap = oracle_logits_along(tg, prompt, G[:n_tok], rounder(wl))
+    tb = token_gap_bound(name, "verify")
+    n_tie = check_tokens(G[:n_tok], exp, gap, "bf16", f"{name} greedy stream vs oracle", bound=tb)
+    _record({"workload": name, "stage": "greedy-stream", "output": "tokens", "n": n_tok, "token_gap_bound": tb,
+             "exempt": n_tie, "differ_above_stated_1e-2": int(np.sum((G[:n_tok] != exp) & (gap > 1e-2)))})
+    k_draw, r_draw = synth.acceptance_draws(steps + 2, sh.vocab, seed=69)
+    sp = Session(m, batch=1, capacity=cap, block=B, stream_cap=cap)
+    sp.prefill([prompt])
+    sp.set_teacher(G[None, :], k_draw, r_draw)
+    for _ in range(steps):
+        sp.step(teacher=True)
+    E = sp.emitted()[0]
+    assert sp.status() == 0
+    sp.close()
+    assert np.array_equal(E, G[:len(E)])
 
 
 # ------------------------------------------------------------------ losslessness at full size
@@ -262,5 +342,7 @@ def test_lossless_qwen3_8b_4k():
     _lossless(QWEN, steps=12)
 
 
-def test_lossless_dense27b_widths_36k_prompt():
-    _lossless(shrink(DENSE, n_layers=8), steps=6)
+def test_lossless_dense27b_36k():
+    """The full 64-layer 27B-class model (about 62 GB of bf16 weights) at a
+    36864-token prompt."""
+    _lossless(DENSE, steps=6)

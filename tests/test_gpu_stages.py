@@ -106,12 +106,15 @@ def test_draft_block(setup):
     tgc, drc = m.structs()
     capi.dflash_draft_block(drc, tgc, s.anchor, batch, B, s.dcache, s.draft, s.ws)
     got = s.draft.cpu().numpy()
+    lg = to_np(capi.dflash_workspace_logits(s.ws, batch * B, wl.target.vocab)).reshape(batch, B, -1)
     assert s.draft_len() == lens  # the block's keys/values are scratch beyond the length
     rnd = rounder(wl)
     for b in range(batch):
+        ref_logits = O.draft_logits(dr, tg, int(anchors[b]), B, kvs[b], rnd)
         ref, gap = O.draft_forward(dr, tg, int(anchors[b]), B, kvs[b], rnd)
         assert got[b, 0] == anchors[b]
         check_tokens(got[b, 1:], ref[1:], gap, wl.dtype, f"draft tokens b={b}")
+        assert_close(lg[b, 1:], ref_logits, wl.dtype, f"draft logits b={b}")
     assert s.status() == 0
     s.close()
 
@@ -128,6 +131,7 @@ def test_verify_prefill_commit(setup):
                        s.stream_len, s.stream_cap, s.ws)
     rnd = rounder(wl)
     ref = O.target_forward(tg, prompt, O.KV.empty(sh.n_layers, sh.n_kv, sh.head_dim), rnd)
+    assert_close(to_np(capi.dflash_workspace_logits(s.ws, n, sh.vocab)), ref.logits, wl.dtype, "prefill logits")
     check_tokens(s.argmax[:n].cpu().numpy(), ref.argmax, ref.gap, wl.dtype, "prefill argmax")
     assert_close(s.gap[:n].cpu().numpy(), ref.gap, wl.dtype, "prefill top-2 gap", tol=GAP_TOL[wl.dtype])
     assert_close(to_np(s.hcap[:n]), ref.hcap, wl.dtype, "prefill captured states")
@@ -158,10 +162,12 @@ def test_verify_block_on_context(setup):
     rnd = rounder(wl)
     am = s.argmax.cpu().numpy()[:batch * B].reshape(batch, B)
     hc = to_np(s.hcap)[:batch * B].reshape(batch, B, -1)
+    lg = to_np(capi.dflash_workspace_logits(s.ws, batch * B, sh.vocab)).reshape(batch, B, -1)
     for b in range(batch):
         ref = O.target_forward(tg, toks[b], kvs[b], rnd)
         check_tokens(am[b], ref.argmax, ref.gap, wl.dtype, f"verify argmax b={b}")
         assert_close(hc[b], ref.hcap, wl.dtype, f"verify hcap b={b}")
+        assert_close(lg[b], ref.logits, wl.dtype, f"verify logits b={b}")
     assert s.status() == 0
     s.close()
 

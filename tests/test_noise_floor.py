@@ -50,3 +50,36 @@ def test_two_emulations_diverge_to_the_bf16_floor(monkeypatch):
         assert fro <= STACK_FRO and peak <= STACK_PEAK, (fro, peak)
     # and the top-2 gaps move by less than twice the bf16 logit bound
     assert np.max(np.abs(a.gap - b.gap)) < 4e-2
+
+
+def test_floor_at_qwen3_8b_widths_reproduces_the_stored_bounds():
+    """Re-measure the floor at the Qwen3-8B widths (hidden 4096, 32/8 x 128,
+    FFN 12288, vocab 151936; 6 target layers, the 5 drafter layers, a 4096-
+    position synthetic cache) with the oracle alone, and check the stored
+    floors that the full-width GPU bounds derive from: same order of magnitude
+    (float32 products may differ between BLAS builds), and every derived bound
+    above the floor measured here."""
+    import importlib.util
+    import os
+
+    from tolerances import FLOOR_MARGIN, FLOORS
+
+    here = os.path.dirname(os.path.abspath(__file__))
+    spec = importlib.util.spec_from_file_location("noise_floor", os.path.join(here, "golden", "noise_floor.py"))
+    nf = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(nf)
+    now = nf.measure(synth.WORKLOADS["qwen3-8b-4k"])
+    stored = FLOORS["qwen3-8b-4k"]
+    for stage in ("verify", "draft"):
+        for out, st in now[stage].items():
+            key = "max_gap_change" if out == "tokens" else "max_abs"
+            a, b = st[key], stored[stage][out][key]
+            if b == 0.0:
+                assert a == 0.0, (stage, out, a)
+                continue
+            assert 0.5 * b <= a <= 2.0 * b, (stage, out, a, b)
+            assert FLOOR_MARGIN * b >= a, (stage, out, a, b)
+    # the stack pushes logits past the stated 2e-2 and near-tie tokens past 1e-2 at this width
+    assert stored["verify"]["logits"]["max_abs"] > 1e-2
+    # the first layer's keys sit within one bf16 rounding of each other
+    assert stored["verify"]["k0"]["max_abs"] <= 2e-2
