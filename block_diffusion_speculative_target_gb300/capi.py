@@ -50,7 +50,7 @@ class TargetC(ctypes.Structure):
 
 class DraftC(ctypes.Structure):
     _fields_ = [("d", ModelDesc), ("w_fc", c_void_p), ("fc_norm", c_void_p), ("final_norm", c_void_p),
-                ("layers", POINTER(LayerW)), ("w_kv_all", c_void_p), ("mask_id", c_int32)]
+                ("layers", POINTER(LayerW)), ("w_kv_all", c_void_p), ("mask_id", c_int32), ("cross_ctx", c_int32)]
 
 
 _P = c_void_p
@@ -82,7 +82,7 @@ _SIGS = {
     "dflash_rmsnorm": (_I, [_I, _P, _P, _P, _I, _I, c_float, _P]),
     "dflash_argmax": (_I, [_P, _I, _I, _P, _P, _P, _P]),
     "dflash_argmax_noalloc": (_I, [_P, _I, _I, _P, _P, _P, _P]),
-    "dflash_attention": (_I, [POINTER(ModelDesc), _P, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "dflash_attention": (_I, [POINTER(ModelDesc), _P, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
     "dflash_profile_begin": (_I, [_I]),
     "dflash_launch_count": (ctypes.c_longlong, []),
     "dflash_profile_end": (_I, [POINTER(c_float), POINTER(c_int32), _I, POINTER(c_int32)]),
@@ -299,8 +299,8 @@ def dflash_argmax_noalloc(logits, rows, V, argmax, gap, status=None, stream=None
                                         _stream(stream)), "dflash_argmax_noalloc")
 
 
-def dflash_attention(desc: ModelDesc, q, batch, n, causal, cache, layer, out, ws, stream=None):
-    _check(load().dflash_attention(ctypes.byref(desc), _ptr(q), batch, n, causal, cache, layer, _ptr(out), ws,
+def dflash_attention(desc: ModelDesc, q, batch, n, causal, cache, layer, out, ws, stream=None, window=0):
+    _check(load().dflash_attention(ctypes.byref(desc), _ptr(q), batch, n, causal, window, cache, layer, _ptr(out), ws,
                                    _stream(stream)), "dflash_attention")
 
 

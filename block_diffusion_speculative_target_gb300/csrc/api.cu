@@ -27,6 +27,7 @@ struct dflash_cache {
   CUtensorMap tk, tv;
   int32_t total_batch;    // sequences of the allocation (views share it)
   int32_t seq_base;       // first sequence of this view
+  int32_t attn_gtiles;    // 128-key tiles per attention partial (fixed for the cache's life)
 };
 
 static KvMaps kv_maps(const dflash_cache* c, int layer) {
@@ -152,6 +153,7 @@ int dflash_cache_alloc(const dflash_model_desc* d, int32_t n_layers, int32_t bat
   c->total_batch = batch;
   c->seq_base = 0;
   c->has_maps = false;
+  c->attn_gtiles = attn_group_tiles(capacity, d->n_kv_heads);
   if (d->dtype == DFLASH_BF16 && d->head_dim == 128) {
     if (!make_kv_maps(c->k, c->v, (long long)n_layers * batch * d->n_kv_heads * capacity, &c->tk, &c->tv)) {
       dflash_cache_free(c);
@@ -454,7 +456,7 @@ static bool cache_matches(const dflash_cache* c, const dflash_model_desc& d, int
 }
 
 static int layer_forward_f32(const dflash_model_desc& d, const dflash_layer_w& w, dflash_cache* c, int layer,
-                             int batch, int n, int causal, dflash_workspace* ws, cudaStream_t s) {
+                             int batch, int n, int causal, int window, dflash_workspace* ws, cudaStream_t s) {
   const int rows = batch * n, H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads;
   const int qkvw = (nq + 2 * nkv) * hd, dt = d.dtype;
   uint8_t* kc = c->k + (size_t)layer * c->layer_stride * c->elem;
@@ -463,8 +465,8 @@ static int layer_forward_f32(const dflash_model_desc& d, const dflash_layer_w& w
   CK(gemm_f32(ws->xn, H, rows, w.wqkv, qkvw, H, Epi{EPI_F32, ws->f32buf, qkvw}, s));
   CK(rope_qkv(dt, ws->f32buf, batch, n, nq, nkv, hd, ws->q, kc, vc, c->seq_stride, c->head_stride, c->capacity,
               c->len, c->rope, ws->status, s));
-  CK(attention(dt, ws->q, batch, n, nq, nkv, hd, causal, kc, vc, c->seq_stride, c->head_stride, c->capacity, c->len,
-               nullptr, ws->as, ws->attn, ws->status, s));
+  CK(attention(dt, ws->q, batch, n, nq, nkv, hd, causal, window, kc, vc, c->seq_stride, c->head_stride, c->capacity,
+               c->attn_gtiles, c->len, nullptr, ws->as, ws->attn, ws->status, s));
   CK(gemm_f32(ws->attn, nq * hd, rows, w.wo, H, nq * hd, Epi{EPI_RESID, ws->x, H}, s));
   CK(rmsnorm(dt, ws->x, w.ffn_norm, ws->xn, rows, H, d.rms_eps, s));
   CK(gemm_f32(ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, Epi{EPI_SWIGLU, ws->act, d.ffn}, s));
@@ -476,10 +478,11 @@ static int layer_forward_f32(const dflash_model_desc& d, const dflash_layer_w& w
 // QKV product (bf16: RoPE and the KV-cache write fused in its epilogue),
 // attention, O product + residual, RMSNorm, gate/up product + SwiGLU, down
 // product + residual.  Captured states (hcap != null) after the layers in
-// capture[].
+// capture[].  window > 0 limits attention to the last `window` cached
+// positions (the drafter's cross-context window).
 static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layers, dflash_cache* c, int batch, int n,
-                         int causal, const int32_t* capture, void* hcap, const void* final_norm, const void* lm_head,
-                         dflash_workspace* ws, cudaStream_t s) {
+                         int causal, int window, const int32_t* capture, void* hcap, const void* final_norm,
+                         const void* lm_head, dflash_workspace* ws, cudaStream_t s) {
   const int rows = batch * n, H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, L = d.n_layers;
   for (int l = 0; l < L; ++l) {
     const dflash_layer_w& w = layers[l];
@@ -487,7 +490,7 @@ static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layer
   }
   if (d.dtype != DFLASH_BF16) {
     for (int l = 0; l < L; ++l) {
-      int rc = layer_forward_f32(d, layers[l], c, l, batch, n, causal, ws, s);
+      int rc = layer_forward_f32(d, layers[l], c, l, batch, n, causal, window, ws, s);
       if (rc != DFLASH_OK) return rc;
       if (hcap)
         for (int si = 0; si < 5; ++si)
@@ -505,8 +508,8 @@ static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layer
     CK(rmsnorm(d.dtype, ws->x, w.attn_norm, ws->xn, rows, H, d.rms_eps, s));
     CK(gemm_b16(ws->xn, H, rows, w.wqkv, qkvw, H, epi_cache(GE_QKV, ws->q, nq * hd, c, l, nq, n, nullptr), ws, s));
     const KvMaps maps = kv_maps(c, l);
-    CK(attention(d.dtype, ws->q, batch, n, nq, nkv, hd, causal, kc, vc, c->seq_stride, c->head_stride, c->capacity,
-                 c->len, &maps, ws->as, ws->attn, ws->status, s));
+    CK(attention(d.dtype, ws->q, batch, n, nq, nkv, hd, causal, window, kc, vc, c->seq_stride, c->head_stride, c->capacity,
+                 c->attn_gtiles, c->len, &maps, ws->as, ws->attn, ws->status, s));
     CK(gemm_b16(ws->attn, nq * hd, rows, w.wo, H, nq * hd, epi_of(GE_RESID, ws->x, H), ws, s));
     CK(rmsnorm(d.dtype, ws->x, w.ffn_norm, ws->xn, rows, H, d.rms_eps, s));
     CK(gemm_b16(ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, epi_of(GE_SWIGLU, ws->act, d.ffn), ws, s));
@@ -541,7 +544,7 @@ int target_verify(const dflash_target* tg, const int32_t* tokens, int32_t batch,
   cudaStream_t s = (cudaStream_t)cuda_stream;
   const int rows = batch * n, H = d.hidden;
   CK(embed(d.dtype, tg->embed, d.vocab, H, tokens, nullptr, 0, batch, n, 0, nullptr, ws->x, ws->status, s));
-  int rc = decoder_stack(d, tg->layers, tc, batch, n, 1, tg->capture, hcap, tg->final_norm, tg->lm_head, ws, s);
+  int rc = decoder_stack(d, tg->layers, tc, batch, n, 1, 0, tg->capture, hcap, tg->final_norm, tg->lm_head, ws, s);
   if (rc != DFLASH_OK) return rc;
   CK(argmax(ws->logits, rows, d.vocab, argmax_out, top2_gap, 0, ws->am, ws->status, s));
   if (commit)
@@ -602,12 +605,13 @@ int dflash_draft_block(const dflash_draft* dr, const dflash_target* tg, const in
   REQ(d.hidden == tg->d.hidden && d.vocab == tg->d.vocab && d.dtype == tg->d.dtype);
   REQ(block >= 2 && block <= 16 && batch > 0 && batch * block <= ws->max_rows);
   REQ(cache_matches(dc, d, d.n_layers) && batch <= dc->batch && dc->capacity <= ws->max_ctx);
-  REQ(dr->mask_id >= 0 && dr->mask_id < d.vocab);
+  REQ(dr->mask_id >= 0 && dr->mask_id < d.vocab && dr->cross_ctx >= 0);
   cudaStream_t s = (cudaStream_t)stream;
   const int rows = batch * block, H = d.hidden;
   CK(embed(d.dtype, tg->embed, d.vocab, H, nullptr, anchor, dr->mask_id, batch, block, 1, draft_tokens, ws->x,
            ws->status, s));
-  int rc = decoder_stack(d, dr->layers, dc, batch, block, 0, nullptr, nullptr, dr->final_norm, tg->lm_head, ws, s);
+  int rc = decoder_stack(d, dr->layers, dc, batch, block, 0, dr->cross_ctx, nullptr, nullptr, dr->final_norm,
+                         tg->lm_head, ws, s);
   if (rc != DFLASH_OK) return rc;
   CK(argmax(ws->logits, rows, d.vocab, draft_tokens, nullptr, block, ws->am, ws->status, s));
   return DFLASH_OK;
@@ -668,16 +672,17 @@ int dflash_argmax(const float* logits, int32_t rows, int32_t V, int32_t* argmax_
 }
 
 int dflash_attention(const dflash_model_desc* d, const void* q, int32_t batch, int32_t n, int32_t causal,
-                     dflash_cache* c, int32_t layer, void* out, dflash_workspace* ws, dflash_stream_t stream) {
-  REQ(desc_ok(d) && q && out && ws && batch > 0 && n > 0 && batch * n <= ws->max_rows);
+                     int32_t window, dflash_cache* c, int32_t layer, void* out, dflash_workspace* ws,
+                     dflash_stream_t stream) {
+  REQ(desc_ok(d) && q && out && ws && batch > 0 && n > 0 && batch * n <= ws->max_rows && window >= 0);
   REQ(cache_matches(c, *d, layer + 1) && layer >= 0 && batch <= c->batch && c->capacity <= ws->max_ctx);
   REQ((reinterpret_cast<uintptr_t>(q) & 15) == 0);  // the bf16 path reads q by TMA
   if (!desc_shapes_ok(d)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
   const uint8_t* kc = c->k + (size_t)layer * c->layer_stride * c->elem;
   const uint8_t* vc = c->v + (size_t)layer * c->layer_stride * c->elem;
   const KvMaps maps = kv_maps(c, layer);
-  CK(attention(d->dtype, q, batch, n, d->n_q_heads, d->n_kv_heads, d->head_dim, causal ? 1 : 0, kc, vc,
-               c->seq_stride, c->head_stride, c->capacity, c->len, c->has_maps ? &maps : nullptr, ws->as, out,
+  CK(attention(d->dtype, q, batch, n, d->n_q_heads, d->n_kv_heads, d->head_dim, causal ? 1 : 0, window, kc, vc,
+               c->seq_stride, c->head_stride, c->capacity, c->attn_gtiles, c->len, c->has_maps ? &maps : nullptr, ws->as, out,
                ws->status, (cudaStream_t)stream));
   return DFLASH_OK;
 }

@@ -10,7 +10,8 @@
 // P+j sees keys 0..P+j; full (drafter block) -- every row sees 0..P+n-1 (the
 // injected context plus the whole block).
 //
-// bf16 path (head_dim 128): the tcgen05 chunk kernel (attention_tc.cu).
+// bf16 path (head_dim 128): the pipelined tcgen05 kernel (attention_fa.cu),
+// one partial per group of `gtiles` 128-key tiles (a property of the cache).
 // fp32 path: CUDA-core dot products, one CTA per (chunk, head, row).  This
 // file also holds the chunk combine and the TMA maps over a cache.
 #include <algorithm>
@@ -27,8 +28,8 @@ template <int NT>
 __global__ void __launch_bounds__(NT)
     attn_f32_kernel(const float* __restrict__ q, int n, int nq, int nkv, int hd, int causal,
                     const float* __restrict__ kc, const float* __restrict__ vc, size_t seq_stride,
-                    size_t head_stride, int capacity, const int32_t* __restrict__ len, float* __restrict__ part_o,
-                    float* __restrict__ part_ml, int nchunk, float scale_log2) {
+                    size_t head_stride, int capacity, int window, const int32_t* __restrict__ len,
+                    float* __restrict__ part_o, float* __restrict__ part_ml, int nchunk, float scale_log2) {
   __shared__ float qs[kHD];
   __shared__ float sc[kAttnChunk];
   __shared__ float red[NT / 32];
@@ -39,9 +40,10 @@ __global__ void __launch_bounds__(NT)
   pdl_wait();
   const int P = len[b];
   const int lim = min(causal ? P + j + 1 : P + n, capacity);
-  const int kb = c * kAttnChunk;
-  if (kb >= lim) return;
-  const int ke = min(kb + kAttnChunk, lim);
+  const int lo = window > 0 ? max(0, P - window) : 0;  // first key of a cross-context window
+  const int kb = max(c * kAttnChunk, lo);
+  if (kb >= lim || kb >= (c + 1) * kAttnChunk) return;
+  const int ke = min((c + 1) * kAttnChunk, lim);
   const float* kbase = kc + (size_t)b * seq_stride + (size_t)hk * head_stride;
   const float* vbase = vc + (size_t)b * seq_stride + (size_t)hk * head_stride;
   for (int i = threadIdx.x; i < hd; i += NT) qs[i] = q[((size_t)r * nq + hq) * hd + i];
@@ -95,7 +97,8 @@ constexpr int kCombineUnroll = 8;  // float2 partial loads in flight per thread
 template <typename T>
 __global__ void __launch_bounds__(kCombineGroups * 64)
     attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int n, int nq, int hd,
-                        int causal, int capacity, const int32_t* __restrict__ len, int nchunk, T* __restrict__ out) {
+                        int causal, int capacity, int window, int gk, const int32_t* __restrict__ len, int nchunk,
+                        T* __restrict__ out) {
   __shared__ float w[kCombineMaxChunks];
   __shared__ float lsum[kCombineMaxChunks];
   __shared__ float slice[kCombineGroups][kHD];
@@ -107,9 +110,11 @@ __global__ void __launch_bounds__(kCombineGroups * 64)
   pdl_wait();
   const int P = len[b];
   const int lim = min(causal ? P + j + 1 : P + n, capacity);
-  const int nch = min((lim + kAttnChunk - 1) / kAttnChunk, kCombineMaxChunks);
+  const int nch = min((lim + gk - 1) / gk, kCombineMaxChunks);
+  // chunks below a cross-context window hold no partial
+  const int clo = window > 0 ? min(max(0, P - window) / gk, nch) : 0;
   const size_t row0 = ((size_t)r * nq + hq) * nchunk;
-  for (int c = tid; c < nch; c += blockDim.x) {
+  for (int c = clo + tid; c < nch; c += blockDim.x) {
     const float2 ml = *reinterpret_cast<const float2*>(part_ml + (row0 + c) * 2);
     w[c] = ml.x;
     lsum[c] = ml.y;
@@ -117,24 +122,24 @@ __global__ void __launch_bounds__(kCombineGroups * 64)
   __syncthreads();
   if (tid < 32) {
     float m = -INFINITY;
-    for (int c = lane; c < nch; c += 32) m = fmaxf(m, w[c]);
+    for (int c = clo + lane; c < nch; c += 32) m = fmaxf(m, w[c]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (lane == 0) Msh = m;
   }
   __syncthreads();
   const float M = Msh;
-  for (int c = tid; c < nch; c += blockDim.x) w[c] = (w[c] == -INFINITY) ? 0.f : exp2f(w[c] - M);
+  for (int c = clo + tid; c < nch; c += blockDim.x) w[c] = (w[c] == -INFINITY) ? 0.f : exp2f(w[c] - M);
   __syncthreads();
   if (tid < 32) {
     float l = 0.f;
-    for (int c = lane; c < nch; c += 32) l += w[c] * lsum[c];
+    for (int c = clo + lane; c < nch; c += 32) l += w[c] * lsum[c];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     if (lane == 0) Lsh = l;
   }
   const int d2 = tid & 63, g = tid >> 6;
-  const int c0 = nch * g / kCombineGroups, c1 = nch * (g + 1) / kCombineGroups;
+  const int c0 = clo + (nch - clo) * g / kCombineGroups, c1 = clo + (nch - clo) * (g + 1) / kCombineGroups;
   float2 acc = make_float2(0.f, 0.f);
   {
     const float* po = part_o + row0 * kHD + 2 * d2;
@@ -201,6 +206,15 @@ bool make_kv_maps(const void* k, const void* v, long long rows_total, CUtensorMa
   return true;
 }
 
+int attn_group_tiles(int capacity, int nkv) {
+  // units of one sequence at full capacity ~ the SM count: tiles = cap/128 * nkv / SMs,
+  // rounded to the nearest power of two
+  const double x = (double)((capacity + 127) / 128) * nkv / (double)num_sms();
+  int g = 2;
+  while (g < 64 && (double)g * 1.41421356 < x) g *= 2;
+  return g;
+}
+
 bool make_q_map(const void* q, int rows, int nq, int G, CUtensorMap* out) {
   struct Entry {
     const void* q;
@@ -235,9 +249,10 @@ bool make_q_map(const void* q, int rows, int nq, int G, CUtensorMap* out) {
   return true;
 }
 
-cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nkv, int hd, int causal, const void* kc,
-                      const void* vc, size_t seq_stride, size_t head_stride, int capacity, const int32_t* len,
-                      const KvMaps* maps, const AttnScratch& sc, void* out, int* status, cudaStream_t s) {
+cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nkv, int hd, int causal, int window,
+                      const void* kc, const void* vc, size_t seq_stride, size_t head_stride, int capacity, int gtiles,
+                      const int32_t* len, const KvMaps* maps, const AttnScratch& sc, void* out, int* status,
+                      cudaStream_t s) {
   if (batch * n <= 0) return cudaSuccess;
   const int nchunk_launch = (capacity + kAttnChunk - 1) / kAttnChunk;
   if (nchunk_launch > sc.nchunk || nchunk_launch > kCombineMaxChunks || hd > kHD) return cudaErrorInvalidValue;
@@ -247,17 +262,17 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
     const int G = nq / nkv;
     CUtensorMap qmap;
     if (!make_q_map(q, batch * n, nq, G, &qmap)) return cudaErrorInvalidValue;
-    DFL_RET(attention_tc(G, *maps, qmap, batch, n, nq, nkv, causal, capacity, len, sc, nchunk_launch,
-                         scale_log2, status, s));
+    DFL_RET(attention_fa(G, *maps, qmap, batch, n, nq, nkv, causal, window, capacity, gtiles, len, sc, scale_log2,
+                         status, s));
     DFL_RET(launch_pdl(attn_combine_kernel<bf16>, dim3(batch * n, nq), dim3(kCombineGroups * 64), 0, s, sc.o,
-                       sc.ml, n, nq, hd, causal, capacity, len, sc.nchunk, (bf16*)out));
+                       sc.ml, n, nq, hd, causal, capacity, window, gtiles * 128, len, sc.nchunk, (bf16*)out));
   } else {
     const dim3 grid(nchunk_launch, nq, batch * n);
     DFL_RET(launch_pdl(attn_f32_kernel<128>, grid, dim3(128), 0, s, (const float*)q, n, nq, nkv, hd, causal,
-                       (const float*)kc, (const float*)vc, seq_stride, head_stride, capacity, len, sc.o, sc.ml,
-                       sc.nchunk, scale_log2));
+                       (const float*)kc, (const float*)vc, seq_stride, head_stride, capacity, window, len, sc.o,
+                       sc.ml, sc.nchunk, scale_log2));
     DFL_RET(launch_pdl(attn_combine_kernel<float>, dim3(batch * n, nq), dim3(kCombineGroups * 64), 0, s, sc.o,
-                       sc.ml, n, nq, hd, causal, capacity, len, sc.nchunk, (float*)out));
+                       sc.ml, n, nq, hd, causal, capacity, window, kAttnChunk, len, sc.nchunk, (float*)out));
   }
   count_launch(2);
   return cudaSuccess;

@@ -1,0 +1,456 @@
+// Block-vs-cache attention on the 5th-generation tensor cores (bf16, head_dim
+// 128), warp-specialised and pipelined over 128-key tiles.
+//
+// Work unit (one CTA): KV head hk, 16-row block rb of sequence b, key group gi
+// = `gtiles` consecutive 128-key tiles at absolute positions
+// [gi * gtiles * 128, (gi + 1) * gtiles * 128).  The group size is a property
+// of the cache (fixed when it is allocated), so the reduction below depends
+// only on absolute positions: a row's result is the same whether it is
+// computed alone or in a block, and in any batch.
+//
+// The G query heads that share the KV head are stacked into one M = 128 tile
+// (row r = block row r / G, head r % G; rows past 16 G are padding), so one
+// tcgen05.mma serves the whole GQA group.  Per tile t of the unit:
+//   S_t = Q K_t^T (tensor cores, fp32 in TMEM, double-buffered)
+//   m_t = max of the row's visible scores (log2 units), p = 2^(s - m_t),
+//         0 for keys outside the row's visible range [lo, lim)
+//   P_t = p as a bf16 hi/lo pair written over S_t in TMEM (p = hi + lo to
+//         about 2^-17), O_t = P_hi V_t + P_lo V_t (tensor cores, A operand
+//         from TMEM, double-buffered O)
+//   fold (in registers, tiles in order; tiles with no visible key skipped):
+//         M' = max(M, m_t), a = 2^(M - M'), c = 2^(m_t - M'),
+//         O = O a + O_t c, L = L a + l_t c  (l_t: sum of p, per half-row)
+// and the unit writes one partial (M, L, O) per (row, head); the combine
+// kernel merges the groups of a row in group order.
+//
+// Roles (320 threads): warp 0 lane 0 streams Q and the K/V tiles through a
+// 3-stage TMA ring; warp 1 owns TMEM and its lane 0 issues the products
+// (QK^T of tile t+1 is issued while tile t's P is computed); warps 2..9 each
+// own TMEM lane quarter (warp & 3) and one half of the key columns
+// ((warp - 2) >> 2): they compute P for their half and fold their half of O.
+// The row max needs all 128 scores: each thread also reads the other half's
+// scores from TMEM for the max alone, so the two halves never synchronise.
+// Every wait is bounded; a wait that gives up sets DFLASH_STATUS_TIMEOUT,
+// the unit writes nothing, and the CTA drains its copies and products before
+// releasing TMEM.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dfl {
+
+namespace {
+constexpr int kFaThreads = 320;
+constexpr int kStages = 3;
+constexpr uint32_t kTileBytes = 128 * 256;           // 128 keys x 128 dims bf16, two 64-dim halves
+constexpr uint32_t kStageBytes = 2 * kTileBytes;     // keys then values
+constexpr uint32_t kQ = kStages * kStageBytes;       // query [d-half][128 rows][128 B]
+constexpr uint32_t kBar = kQ + 32768;                // barriers, TMEM slot, abort flag
+constexpr int kFaSmem = kBar + 256 + 1024;           // + alignment slack
+constexpr uint32_t kTmemCols = 512;                  // S0 S1 (P aliased) | O0 O1
+constexpr uint64_t kFaWaitNs = 500000000ull;
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A (M = 128 rows = TMEM lanes,
+// K along the columns, two bf16 per 32-bit column) read from TMEM.
+__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// MN-major operand in 128-byte swizzled rows (a TMA load of [key][64 x bf16]
+// boxes): 8-row groups 1024 B apart, 64-element column blocks `block_stride`
+// bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t addr, uint32_t block_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((block_stride >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+}  // namespace
+
+template <int G>
+__global__ void __launch_bounds__(kFaThreads, 1)
+    attn_fa_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmQ, int batch, int n, int nq, int nkv, int causal, int window,
+                   long long row0, int capacity, int gtiles, int ngroups, const int32_t* __restrict__ len,
+                   float* __restrict__ part_o, float* __restrict__ part_ml, float scale_log2, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kBar);
+  uint64_t* kv_full = bar;        // [3] a tile's keys and values landed
+  uint64_t* kv_empty = bar + 3;   // [3] its products completed
+  uint64_t* q_full = bar + 6;
+  uint64_t* s_full = bar + 7;     // [2] S_t in TMEM
+  uint64_t* p_full = bar + 9;     // [2] P_t in TMEM (one arrival per softmax warp)
+  uint64_t* o_full = bar + 11;    // [2] O_t in TMEM
+  uint64_t* o_free = bar + 13;    // [2] O_t read out (one arrival per softmax warp)
+  uint64_t* drain = bar + 15;     // every issued product completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(tslot + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {  // the descriptors are kernel parameters: fetch them while the previous kernel drains
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  pdl_launch();
+  pdl_wait();
+
+  // ---- the unit
+  const int nrb = (n + 15) >> 4;
+  int u = blockIdx.x;
+  const int hk = u % nkv;
+  u /= nkv;
+  const int rb = u % nrb;
+  u /= nrb;
+  const int b = u % batch;
+  const int gi = u / batch;
+  const int P = len[b];
+  const int r_last = min(rb * 16 + 15, n - 1);
+  const int kmax = min(causal ? P + r_last + 1 : P + n, capacity);
+  const int lo = window > 0 ? max(0, P - window) : 0;
+  const int ta = max(gi * gtiles, lo >> 7);
+  const int tb = min((gi + 1) * gtiles, (kmax + 127) >> 7);
+  const int nt = tb - ta;
+  if (nt <= 0) return;  // uniform over the CTA: no key of this group is visible
+
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 8);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_free[i], 8);
+    }
+    mbar_init(drain, 1);
+    *abort_f = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  int issued = 0;  // producer: tiles whose copies were issued
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const int qbox = min(16, batch * n);
+      mbar_arrive_expect_tx(q_full, 2 * 128 * G * qbox);
+      for (int dh = 0; dh < 2; ++dh)
+        tma_load_3d(sm + kQ + dh * 16384, &tmQ, q_full, dh * 64, hk * G, b * n + rb * 16);
+      const int rowb = (int)(row0 + ((long long)b * nkv + hk) * capacity);
+      for (int t = 0; t < nt; ++t) {
+        const int s = t % kStages;
+        if (t >= kStages && !mbar_wait(&kv_empty[s], (uint32_t)((t / kStages) - 1) & 1u, kFaWaitNs)) {
+          *abort_f = 1;
+          set_status(status, DFLASH_STATUS_TIMEOUT);
+          break;
+        }
+        if (*abort_f) break;
+        uint8_t* st = sm + s * kStageBytes;
+        const int key0 = rowb + (ta + t) * 128;
+        mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
+        for (int dh = 0; dh < 2; ++dh) tma_load_2d(st + dh * 16384, &tmK, &kv_full[s], dh * 64, key0);
+        for (int dh = 0; dh < 2; ++dh) tma_load_2d(st + kTileBytes + dh * 16384, &tmV, &kv_full[s], dh * 64, key0);
+        issued = t + 1;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ products
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16_f32(128, 128);
+      const uint32_t idO = idesc_bf16_f32(128, 128) | (1u << 16);  // B (values) MN-major
+      bool ok = mbar_wait(q_full, 0, kFaWaitNs);
+      for (int t = 0; ok && t <= nt; ++t) {
+        if (t < nt) {  // S_t = Q K_t^T into S[t & 1], once P_{t-2} (same buffer) has been consumed
+          const int s = t % kStages, sb = t & 1;
+          ok = mbar_wait(&kv_full[s], (uint32_t)(t / kStages) & 1u, kFaWaitNs);
+          if (ok && t >= 2) ok = mbar_wait(&o_full[sb], (uint32_t)((t - 2) >> 1) & 1u, kFaWaitNs);
+          if (!ok || *abort_f) break;
+          tc_fence_after();
+          const uint8_t* kt = sm + s * kStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const int dh = kk >> 2;
+            const uint64_t a = smem_desc_sw128(sm + kQ + dh * 16384) + (uint64_t)(((kk & 3) * 32) >> 4);
+            const uint64_t bk = smem_desc_sw128(kt + dh * 16384) + (uint64_t)(((kk & 3) * 32) >> 4);
+            tc_mma_f16(tmem + sb * 128, a, bk, idS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&s_full[sb]);
+        }
+        if (t >= 1) {  // O_{t-1} = P_hi V + P_lo V into O[(t-1) & 1], once O_{t-3} has been read out
+          const int w = t - 1, wb = w & 1, s = w % kStages;
+          ok = mbar_wait(&p_full[wb], (uint32_t)(w >> 1) & 1u, kFaWaitNs);
+          if (ok && w >= 2) ok = mbar_wait(&o_free[wb], (uint32_t)((w - 2) >> 1) & 1u, kFaWaitNs);
+          if (!ok || *abort_f) break;
+          tc_fence_after();
+          const uint32_t vt = smem_u32(sm + s * kStageBytes + kTileBytes);
+#pragma unroll
+          for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              tc_mma_f16_tmem_a(tmem + 256 + wb * 128, tmem + wb * 128 + pass * 64 + kk * 8,
+                                smem_desc_mn(vt + kk * 2048, 16384), idO, (pass | kk) != 0 ? 1u : 0u);
+          tc_commit(&o_full[wb]);
+          tc_commit(&kv_empty[s]);
+        }
+      }
+      if (!ok) {
+        *abort_f = 1;
+        set_status(status, DFLASH_STATUS_TIMEOUT);
+      }
+      tc_commit(drain);  // arrives once every product issued above has completed
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + fold
+    const int q4 = warp & 3, h = (warp - 2) >> 2;
+    const int r = q4 * 32 + lane;
+    const int ri = r / G;
+    const int qi = rb * 16 + ri;
+    const bool live = q4 * 32 < 16 * G;  // warp-uniform: the quarter holds real rows
+    const bool row_ok = r < 16 * G && qi < n;
+    const int lim = row_ok ? min(causal ? P + qi + 1 : P + n, capacity) : 0;  // visible keys [lo, lim)
+    const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
+    float acc[64];
+#pragma unroll
+    for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+    float M = -INFINITY, Lh = 0.f;
+    float m_prev = -INFINITY, l_prev = 0.f;
+    bool ok = true;
+    for (int t = 0; t <= nt; ++t) {
+      float m_cur = -INFINITY, l_cur = 0.f;
+      if (t < nt) {
+        const int sb = t & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (uint32_t)(t >> 1) & 1u, kFaWaitNs));
+        if (__any_sync(0xffffffffu, !ok || *abort_f)) break;  // warp-uniform
+        tc_fence_after();
+        if (live) {
+          const int k0 = (ta + t) * 128;
+          const uint32_t sbase = tmem + lrow + sb * 128;
+          // the tile max over all 128 scores (both halves), 32 columns at a time
+          float mraw = -INFINITY;
+#pragma unroll 1
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t v[32];
+            tmem_ld32(sbase + c4 * 32, v);
+            tmem_ld_wait();
+            const int kb = k0 + c4 * 32;
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (kb + e >= lo && kb + e < lim) mraw = fmaxf(mraw, __uint_as_float(v[e]));
+          }
+          // the tile max in log2 units (scale > 0: max(s) * scale = max(s * scale))
+          m_cur = mraw * scale_log2;
+          const float negm = mraw == -INFINITY ? 0.f : -m_cur;
+          // P of this thread's half, 32 keys at a time, written over the scores
+#pragma unroll 1
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t v[32], hi[16], lo_[16];
+            tmem_ld32(sbase + h * 64 + c2 * 32, v);
+            tmem_ld_wait();
+            const int kb = k0 + h * 64 + c2 * 32;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int k = kb + 2 * e;
+              const float p0 =
+                  (k >= lo && k < lim) ? ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm)) : 0.f;
+              const float p1 =
+                  (k + 1 >= lo && k + 1 < lim) ? ex2f(fmaf(__uint_as_float(v[2 * e + 1]), scale_log2, negm)) : 0.f;
+              l_cur += p0;
+              l_cur += p1;
+              pack_bf16_hilo(p0, p1, hi[e], lo_[e]);
+            }
+            tmem_st16(sbase + h * 32 + c2 * 16, hi);
+            tmem_st16(sbase + 64 + h * 32 + c2 * 16, lo_);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);
+      }
+      if (t >= 1) {  // fold O_{t-1}
+        const int w = t - 1, wb = w & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&o_full[wb], (uint32_t)(w >> 1) & 1u, kFaWaitNs));
+        if (__any_sync(0xffffffffu, !ok || *abort_f)) break;  // warp-uniform
+        tc_fence_after();
+        // fold factors of this row (tiles with no visible key are skipped)
+        const bool fold = m_prev != -INFINITY;
+        const float Mn = fmaxf(M, m_prev);
+        const float fa = (M == -INFINITY || !fold) ? 0.f : ex2f(M - Mn);
+        const float fc = fold ? ex2f(m_prev - Mn) : 0.f;
+        if (live) {
+          const uint32_t obase = tmem + lrow + 256 + wb * 128 + h * 64;
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t o[32];
+            tmem_ld32(obase + c2 * 32, o);
+            tmem_ld_wait();
+            if (c2 == 1) {  // O_{t-1} fully read: release its buffer
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&o_free[wb]);
+            }
+            if (fold) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) acc[c2 * 32 + e] = fmaf(__uint_as_float(o[e]), fc, acc[c2 * 32 + e] * fa);
+            }
+          }
+        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&o_free[wb]);
+        }
+        if (fold) {
+          Lh = fmaf(l_prev, fc, Lh * fa);
+          M = Mn;
+        }
+      }
+      m_prev = m_cur;
+      l_prev = l_cur;
+    }
+    if (!ok) {
+      *abort_f = 1;
+      set_status(status, DFLASH_STATUS_TIMEOUT);
+    }
+    __syncthreads();
+    // ---- the unit's partial, staged through the (dead) ring so that each
+    // row leaves as one contiguous 512-byte store: row r at r * 512, its
+    // 16-byte chunks XOR-swizzled by (r & 7).  Row sums of the two halves at
+    // 64 KB, row maxima after them.
+    float* stg = reinterpret_cast<float*>(sm);
+    float* stg_l = stg + 128 * 128;
+    float* stg_m = stg_l + 256;
+    const bool good = !*abort_f;
+    if (good && live) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int ch = h * 16 + c;
+        *reinterpret_cast<float4*>(stg + r * 128 + ((ch ^ (r & 7)) << 2)) =
+            make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+      }
+      stg_l[2 * r + h] = Lh;
+      if (h == 0) stg_m[r] = M;
+    }
+    __syncthreads();
+    if (good) {
+      const int rows_live = min(16 * G, 128);
+      for (int rr = warp - 2; rr < rows_live; rr += 8) {
+        const int ir = rr / G, hr = rr - ir * G, qr = rb * 16 + ir;
+        if (qr >= n) continue;  // warp-uniform
+        const size_t prow = ((size_t)(b * n + qr) * nq + hk * G + hr) * ngroups + gi;
+        *reinterpret_cast<float4*>(part_o + prow * 128 + lane * 4) =
+            *reinterpret_cast<const float4*>(stg + rr * 128 + ((lane ^ (rr & 7)) << 2));
+        if (lane == 0)
+          *reinterpret_cast<float2*>(part_ml + prow * 2) = make_float2(stg_m[rr], stg_l[2 * rr] + stg_l[2 * rr + 1]);
+      }
+    }
+  }
+  if (warp < 2) {  // match the softmax warps' two block-wide barriers
+    __syncthreads();
+    __syncthreads();
+  }
+  // ---- teardown: copies and products still in flight complete before the
+  // ring and TMEM are released
+  if (warp == 0 && lane == 0 && *abort_f) {
+    const int first = issued > kStages ? issued - kStages : 0;
+    for (int t = first; t < issued; ++t)
+      mbar_wait(&kv_full[t % kStages], (uint32_t)(t / kStages) & 1u, kFaWaitNs / 4);
+  }
+  if (warp == 1 && lane == 0) mbar_wait(drain, 0, kFaWaitNs / 4);
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+cudaError_t attention_fa(int G, const KvMaps& maps, const CUtensorMap& qmap, int batch, int n, int nq, int nkv,
+                         int causal, int window, int capacity, int gtiles, const int32_t* len, const AttnScratch& sc,
+                         float scale_log2, int* status, cudaStream_t s) {
+  if (gtiles < 2 || batch > kMaxRows) return cudaErrorInvalidValue;
+  const int ngroups = (capacity + gtiles * 128 - 1) / (gtiles * 128);
+  if (ngroups > sc.nchunk) return cudaErrorInvalidValue;  // partial slots per (row, head)
+  const long long units = (long long)ngroups * nkv * batch * ((n + 15) / 16);
+  if (units <= 0) return cudaSuccess;
+  if (units > INT32_MAX) return cudaErrorInvalidValue;
+#define DFL_FA_CASE(GG)                                                                                         \
+  case GG: {                                                                                                     \
+    static bool set = false;                                                                                     \
+    if (!set) {                                                                                                  \
+      DFL_RET(cudaFuncSetAttribute(attn_fa_kernel<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFaSmem));   \
+      set = true;                                                                                                \
+    }                                                                                                            \
+    DFL_RET(launch_pdl(attn_fa_kernel<GG>, dim3((unsigned)units), dim3(kFaThreads), kFaSmem, s, maps.k, maps.v,  \
+                       qmap, batch, n, nq, nkv, causal, window, maps.row0, capacity, gtiles, sc.nchunk, len, sc.o, \
+                       sc.ml, scale_log2, status));                                                              \
+    return cudaSuccess;                                                                                          \
+  }
+  switch (G) {
+    DFL_FA_CASE(1)
+    DFL_FA_CASE(2)
+    DFL_FA_CASE(4)
+    DFL_FA_CASE(5)
+    DFL_FA_CASE(8)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef DFL_FA_CASE
+}
+
+}  // namespace dfl

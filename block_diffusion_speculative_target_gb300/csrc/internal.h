@@ -137,19 +137,26 @@ struct KvMaps {
   long long row0;
 };
 bool make_kv_maps(const void* k, const void* v, long long rows_total, CUtensorMap* mk, CUtensorMap* mv);
-cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nkv, int hd, int causal,
-                      const void* kc, const void* vc, size_t seq_stride, size_t head_stride, int capacity,
+// window > 0: keys below len[b] - window (a cross-context window) are not attended.
+// gtiles: 128-key tiles per partial of the bf16 path (a property of the cache).
+cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nkv, int hd, int causal, int window,
+                      const void* kc, const void* vc, size_t seq_stride, size_t head_stride, int capacity, int gtiles,
                       const int32_t* len, const KvMaps* maps, const AttnScratch& sc, void* out, int* status,
                       cudaStream_t s);
+// The tiles per partial for a cache of `capacity` positions and nkv heads:
+// about one unit per SM for one sequence at full capacity, a power of two in
+// [2, 64]; depends on nothing else, so results do not depend on the batch.
+int attn_group_tiles(int capacity, int nkv);
 
 // 3-D map over a bf16 query buffer [rows][nq][128]: boxes of 64 head-dim
 // elements (128 B, swizzled) x G heads x min(16, rows) rows.  Encoded maps are cached by
 // (pointer, rows, nq, G).
 bool make_q_map(const void* q, int rows, int nq, int G, CUtensorMap* out);
-// The bf16 attention chunk kernel on tcgen05 (head_dim 128, G in {1, 2, 4, 5, 8}).
-cudaError_t attention_tc(int G, const KvMaps& maps, const CUtensorMap& qmap, int batch, int n, int nq, int nkv, int causal,
-                         int capacity, const int32_t* len, const AttnScratch& sc, int nchunk_launch, float scale_log2,
-                         int* status, cudaStream_t s);
+// The bf16 attention kernel on tcgen05 (head_dim 128, G in {1, 2, 4, 5, 8}):
+// one partial (max, sum, unnormalised output) per (row, head, tile group).
+cudaError_t attention_fa(int G, const KvMaps& maps, const CUtensorMap& qmap, int batch, int n, int nq, int nkv,
+                         int causal, int window, int capacity, int gtiles, const int32_t* len, const AttnScratch& sc,
+                         float scale_log2, int* status, cudaStream_t s);
 
 // Greedy token and top-2 gap per row.  If skip_first_of (>0), rows with
 // (r % skip_first_of) == 0 are not written to argmax_out.

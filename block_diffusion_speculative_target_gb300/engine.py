@@ -34,8 +34,9 @@ class Model:
     hidden, n_q, n_kv, head_dim, ffn, vocab, rope_theta, eps; the drafter has
     the target's width and ``draft_layers`` layers."""
 
-    def __init__(self, shape, draft_layers: int, dtype: str, device="cuda"):
+    def __init__(self, shape, draft_layers: int, dtype: str, device="cuda", cross_ctx: int = 0):
         self.shape, self.draft_layers, self.dtype = shape, draft_layers, dtype
+        self.cross_ctx = cross_ctx  # the drafter's cross-context window (0: whole context)
         self.device = torch.device(device)
         tdt = _DT[dtype][1]
         s = shape
@@ -86,6 +87,11 @@ class Model:
             v.copy_(t.reshape(v.shape))
         self.finalize()
 
+    def set_cross_ctx(self, window: int):
+        """Set the drafter's cross-context window (0: whole context)."""
+        self.cross_ctx = int(window)
+        self._structs = None
+
     def finalize(self):
         """Gather the drafter's k/v rows for the injection product and build
         the C structs.  Call after every change of the weights."""
@@ -119,7 +125,8 @@ class Model:
                                (ctypes.c_int32 * 5)(*self.capture))
             dr = capi.DraftC(desc_of(self.shape, self.dtype, self.draft_layers), self.w_fc.data_ptr(),
                              self.fc_norm.data_ptr(), self.d_final_norm.data_ptr(),
-                             ctypes.cast(dl, ctypes.POINTER(capi.LayerW)), self.w_kv_all.data_ptr(), self.mask_id)
+                             ctypes.cast(dl, ctypes.POINTER(capi.LayerW)), self.w_kv_all.data_ptr(), self.mask_id,
+                             self.cross_ctx)
             self._structs = (tgt, dr, tl, dl)  # keep the layer arrays alive
         return self._structs[0], self._structs[1]
 

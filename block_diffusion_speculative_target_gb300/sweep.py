@@ -58,22 +58,26 @@ def fill_cache(cache, n_layers, P, shape, seed):
     capi.dflash_cache_set_lengths(cache, [P])
 
 
-def step_bytes(shape, draft_layers, P):
+def step_bytes(shape, draft_layers, P, window=0):
+    """Weights once (the injection's W_k/W_v are the drafter layers' own) plus
+    the keys/values read: the target's over P positions, the drafter's over
+    min(P, window) positions when a cross-context window is set."""
     d = shape.head_dim
     layer = 2 * (shape.hidden * (shape.n_q + 2 * shape.n_kv) * d + shape.n_q * d * shape.hidden
                  + 3 * shape.hidden * shape.ffn)
     lm = 2 * shape.vocab * shape.hidden
     fc = 2 * shape.hidden * 5 * shape.hidden
-    inj = 2 * draft_layers * 2 * shape.n_kv * d * shape.hidden
-    kv = (shape.n_layers + draft_layers) * P * 2 * 2 * shape.n_kv * d
-    return shape.n_layers * layer + lm + draft_layers * layer + lm + fc + inj + kv
+    Pd = min(P, window) if window > 0 else P
+    kv = (shape.n_layers * P + draft_layers * Pd) * 2 * 2 * shape.n_kv * d
+    return shape.n_layers * layer + lm + draft_layers * layer + lm + fc + kv
 
 
-def run(contexts, blocks, steps, warmup, stage_passes, peak):
+def run(contexts, blocks, steps, warmup, stage_passes, peak, window=0):
     wl = synth.WORKLOADS["qwen3-8b-4k"]
     s = wl.target
     dev = torch.device("cuda", 0)
     m = build_model(wl, dev)
+    m.set_cross_ctx(window)
     tgc, drc = m.structs()
     Bmax = max(blocks)
     n_steps = 2 + warmup + steps + stage_passes
@@ -148,8 +152,8 @@ def run(contexts, blocks, steps, warmup, stage_passes, peak):
             E = sess.emitted()[0]
             assert np.array_equal(E, G[:len(E)]), "speculative stream left the greedy stream"
             P_mid = P0 + 0.5 * (len0 + int(sess.stream_len.item())) - 1
-            by = step_bytes(s, wl.draft_layers, P_mid)
-            rec = {"P0": P0, "block": B, "ms_per_step": ms, "tokens_per_s": tokens / total, "tau": tokens / steps,
+            by = step_bytes(s, wl.draft_layers, P_mid, window)
+            rec = {"P0": P0, "block": B, "cross_ctx": window, "ms_per_step": ms, "tokens_per_s": tokens / total, "tau": tokens / steps,
                    "bytes_per_step": by, "roofline_frac": by / (ms / 1e3) / (peak * 1e9),
                    "stage_ms": {k: statistics.median(v) for k, v in stage.items()}}
             print(json.dumps(rec), flush=True)
@@ -177,11 +181,12 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--stage-passes", type=int, default=2)
+    ap.add_argument("--cross-ctx", type=int, default=0, help="the drafter's cross-context window (0: whole context)")
     args = ap.parse_args()
     capi.load()
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     peak = json.load(open(p)).get("hbm_gbs", 6800.0) if os.path.exists(p) else 6800.0
-    recs = run(args.contexts, args.blocks, args.steps, args.warmup, args.stage_passes, peak)
+    recs = run(args.contexts, args.blocks, args.steps, args.warmup, args.stage_passes, peak, args.cross_ctx)
     print(table(recs, peak), flush=True)
 
 

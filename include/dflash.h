@@ -97,7 +97,11 @@ typedef struct dflash_target {
  * ([DD] §3.3).  w_kv_all packs, for every drafter layer l in order, that
  * layer's k rows then v rows of wqkv: [Ld * 2 * nkv * hd][H]; it holds the
  * same values as the layers' wqkv and lets one product project the fused
- * feature for all layers ([DD] §5.2 dflash_feature_injection). */
+ * feature for all layers ([DD] §5.2 dflash_feature_injection).
+ * cross_ctx: the drafter's cross-context window W ("如何使用 DFlash 试探式解码
+ * 加速本地 LLM", §7, --spec-dflash-cross-ctx): W > 0 makes every drafter layer
+ * attend only to the W most recent injected positions P-W..P-1 (all of them
+ * when P <= W) plus the block's own rows; 0 attends to the whole context. */
 typedef struct dflash_draft {
   dflash_model_desc d;
   const void *w_fc;       /* [H][5H] fusion Linear ([DD] §2.2 feature_fusion) */
@@ -106,6 +110,7 @@ typedef struct dflash_draft {
   const dflash_layer_w *layers; /* HOST array of d.n_layers entries */
   const void *w_kv_all;
   int32_t mask_id;
+  int32_t cross_ctx;
 } dflash_draft;
 
 /* ------------------------------------------------------------------ caches
@@ -306,14 +311,16 @@ int dflash_argmax_noalloc(const float *logits, int32_t rows, int32_t V, int32_t 
 /* Attention of q [batch][n][nq][hd] (dtype, RoPE applied) against layer
  * `layer` of `cache` (positions 0 .. len[b] + n - 1, the block's own keys
  * already written at len[b] ..), causal (row j sees 0..len+j) or not (every
- * row sees 0..len+n-1).  out [batch][n][nq * hd] dtype.  q, out: device
+ * row sees 0..len+n-1).  window > 0 drops the keys below len - window (the
+ * drafter's cross-context window, see dflash_draft.cross_ctx); 0 keeps all.
+ * out [batch][n][nq * hd] dtype.  q, out: device
  * pointers owned by the caller; q must be 16-byte aligned (the bf16 path
  * loads it by TMA), else DFLASH_ERR_INVALID_ARG before any CUDA call.
  * Every score and softmax sum is exact per fixed 256-position chunk and the
  * chunks merge in order (the scaled dot-product attention of "DFlash 深度解析",
  * §2.2 draft_inference, evaluated chunkwise). */
 int dflash_attention(const dflash_model_desc *d, const void *q, int32_t batch, int32_t n,
-                     int32_t causal, dflash_cache *cache, int32_t layer, void *out,
+                     int32_t causal, int32_t window, dflash_cache *cache, int32_t layer, void *out,
                      dflash_workspace *ws, dflash_stream_t stream);
 
 /* Kernel timing for measurement passes (not for graph capture): between

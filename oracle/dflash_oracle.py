@@ -358,12 +358,24 @@ def inject_kv(dr: Draft, fused, positions, rnd):
     return out
 
 
-def draft_logits(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rnd):
+def cross_window(P: int, window: int) -> int:
+    """First injected context position the drafter attends to.  The tutorial
+    page ("如何使用 DFlash 试探式解码加速本地 LLM", §7) runs the drafter with
+    ``--spec-dflash-cross-ctx 1024`` and says nothing more; the reading taken
+    here: with a cross-context window W > 0 the drafter's attention keeps only
+    the W most recent injected positions P-W..P-1 (all of them when P <= W),
+    and always the block's own B rows.  W = 0 keeps the whole context."""
+    return max(0, P - window) if window > 0 else 0
+
+
+def draft_logits(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rnd, window: int = 0):
     """One non-causal drafter forward over the block [anchor, MASK x (B-1)] at
     positions P..P+B-1 (P = drafter cache length): [DD] §5.1 "given [T1] +
     target_model_context -> single forward pass -> [T2,...]", §2.2
     draft_inference.  Tokens are embedded with the target's embedding and
-    decoded with the target's LM head ([DD] §3.3).
+    decoded with the target's LM head ([DD] §3.3).  ``window``: the
+    cross-context window (``cross_window``); the kept keys carry their
+    absolute positions, so only which keys are attended changes.
 
     parity unpinned: the sub-layer order of the drafter (pre-norm attention,
     then pre-norm SwiGLU, then a final RMSNorm) is not printed on any page.
@@ -372,19 +384,20 @@ def draft_logits(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rnd
     whose logits are not used)."""
     sh = dr.shape
     P = dcache.length()
+    lo = cross_window(P, window)
     toks = np.array([anchor] + [dr.mask_id] * (block - 1), dtype=np.int64)
     x = f64(tg.embed)[toks]
     for li, lw in enumerate(dr.layers):
-        x, _, _ = decoder_layer(x, lw, sh, dcache.k[li], dcache.v[li], P, False, rnd)
+        x, _, _ = decoder_layer(x, lw, sh, dcache.k[li][:, lo:], dcache.v[li][:, lo:], P, False, rnd)
     z = rnd(rmsnorm(x, dr.final_norm, sh.eps))
     return linear(z[1:], tg.lm_head)
 
 
-def draft_forward(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rnd):
+def draft_forward(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rnd, window: int = 0):
     """The drafter's greedy block: argmax of each slot's logits
     (``draft_logits``).  Returns the B drafted tokens, slot 0 holding the
     anchor itself, and the top-2 gaps of slots 1..B-1."""
-    am, gap = argmax_top2(draft_logits(dr, tg, anchor, block, dcache, rnd))
+    am, gap = argmax_top2(draft_logits(dr, tg, anchor, block, dcache, rnd, window))
     return np.concatenate([[anchor], am]).astype(np.int64), gap
 
 
@@ -465,7 +478,7 @@ class StepRecord:
 
 
 def spec_decode(tg: Target, dr: Draft, prompt, n_tokens, block, rnd, forcing=None, ref=None,
-                max_steps=None):
+                max_steps=None, window=0):
     """DFlash speculative decoding, greedy ([DD] §1.2, §2.2, §5.1; [LC]).
 
     prefill : target forward over the prompt, cache its keys/values, capture
@@ -477,7 +490,8 @@ def spec_decode(tg: Target, dr: Draft, prompt, n_tokens, block, rnd, forcing=Non
               leave those rows' captured states pending for the next step.
 
     forcing: optional (k[steps], r[steps]) teacher-forcing draws; ``ref`` is
-    the reference greedy stream they index (length >= n_tokens + block)."""
+    the reference greedy stream they index (length >= n_tokens + block).
+    window: the drafter's cross-context window (``cross_window``)."""
     sh, dsh = tg.shape, dr.shape
     tcache = KV.empty(sh.n_layers, sh.n_kv, sh.head_dim)
     dcache = KV.empty(dsh.n_layers, dsh.n_kv, dsh.head_dim)
@@ -498,7 +512,7 @@ def spec_decode(tg: Target, dr: Draft, prompt, n_tokens, block, rnd, forcing=Non
         for li, (k, v) in enumerate(inject_kv(dr, fused, np.arange(P - m, P), rnd)):
             dcache.append(li, k, v)
         # draft
-        d, _ = draft_forward(dr, tg, anchor, block, dcache, rnd)
+        d, _ = draft_forward(dr, tg, anchor, block, dcache, rnd, window)
         if forcing is not None:
             ks, rs = forcing
             s = len(steps)

@@ -56,6 +56,28 @@ def assert_close(gpu, ref, dtype, what, tol=None):
     return err
 
 
+def bf16_ulp(x):
+    """Spacing of bfloat16 values at |x| (8 significant bits): 2^(e-7) for
+    2^e <= |x| < 2^(e+1)."""
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(x, 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
+def assert_close_rounded(gpu, ref, what, tol=TOL["bf16"]):
+    """A single bf16 rounding of values that the two sides compute with
+    different accumulation order: each element within the stated bound or
+    within one bf16 ulp of the reference value, whichever is larger (two
+    correct results a hair apart can round to adjacent bf16 values, and above
+    |x| = 2.56 one ulp exceeds 2e-2)."""
+    gpu, ref = np.asarray(gpu, dtype=np.float64), np.asarray(ref, dtype=np.float64)
+    d = np.abs(gpu - ref)
+    bound = np.maximum(tol, bf16_ulp(ref))
+    bad = d > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} values off by more than max({tol:.0e}, 1 ulp); worst {d.max():.3e}"
+    return float(d.max()) if d.size else 0.0
+
+
 def assert_close_stack(gpu, ref, what):
     """Stacked outputs: within the bf16 noise-floor bounds (tolerances.py)."""
     fro, peak = stack_error(gpu, ref)

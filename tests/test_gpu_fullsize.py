@@ -11,7 +11,9 @@ holds at any size and is checked on the whole 36-layer 4K model and on the
 full 64-layer 27B-class model at a 36K prompt.
 
 Single-stage outputs (a GEMM, attention, fused features, injected keys and
-values) are held to the stated bf16 max-abs bound 2e-2.  Outputs of a stack of
+values) are held to the stated bf16 max-abs bound 2e-2, or, for a value stored
+in bf16, one bf16 ulp of the reference value where that is larger (above
+|x| = 2.56 a single rounding step exceeds 2e-2).  Outputs of a stack of
 layers (captured states, each layer's keys and values, logits, greedy tokens)
 are held to the stated bounds widened, where needed, to twice the bf16 noise
 floor that the oracle alone reaches at these widths (float64 vs
@@ -27,8 +29,8 @@ import pytest
 import torch
 
 from conftest import oracle_models, shrink
-from gpu_util import (GAP_TOL, TOL, O, Model, Session, assert_close, capi, check_tokens, dev, oracle_logits_along,
-                      rounder, synth, to_dev, to_np)
+from gpu_util import (GAP_TOL, TOL, O, Model, Session, assert_close, assert_close_rounded, capi, check_tokens, dev,
+                      oracle_logits_along, rounder, synth, to_dev, to_np)
 from tolerances import FLOOR_MARGIN, floor_bound, floor_of, token_gap_bound
 
 pytestmark = pytest.mark.gpu
@@ -243,7 +245,7 @@ def test_fuse_inject_full_width(wide):
     _, drc = m.structs()
     capi.dflash_fuse_features(drc, to_dev(hcap, "bf16"), B, s.fused, s.ws)
     ref_f = O.fuse_features(dr, hcap, rnd)
-    assert_close(to_np(s.fused[:B]), ref_f, "bf16", "full-width fused features")
+    assert_close_rounded(to_np(s.fused[:B]), ref_f, "full-width fused features")
     # inject the GPU's fused rows at positions P-B .. P-1 (pending rows of a step)
     capi.dflash_cache_set_lengths(s.dcache, [P - B])
     s.n_pend.fill_(B)
@@ -254,8 +256,8 @@ def test_fuse_inject_full_width(wide):
         k = torch.empty(sh.n_kv, B, sh.head_dim, dtype=torch.bfloat16, device=dev())
         v = torch.empty_like(k)
         capi.dflash_cache_read(s.dcache, li, 0, P - B, B, k, v)
-        assert_close(np.transpose(to_np(k), (1, 0, 2)), inj[li][0], "bf16", f"full-width injected K l={li}")
-        assert_close(np.transpose(to_np(v), (1, 0, 2)), inj[li][1], "bf16", f"full-width injected V l={li}")
+        assert_close_rounded(np.transpose(to_np(k), (1, 0, 2)), inj[li][0], f"full-width injected K l={li}")
+        assert_close_rounded(np.transpose(to_np(v), (1, 0, 2)), inj[li][1], f"full-width injected V l={li}")
     assert s.status() == 0
     s.close()
 

@@ -332,6 +332,74 @@ def test_draft_noncausal_block_sees_all_rows(tiny):
     assert np.array_equal(a[:2], b[:2])
 
 
+# ---------------------------------------------------------------- cross-context window
+
+
+def _injected_cache(dr, fused, positions):
+    dc = O.KV.empty(dr.shape.n_layers, dr.shape.n_kv, dr.shape.head_dim)
+    for li, (k, v) in enumerate(O.inject_kv(dr, fused, positions, NONE)):
+        dc.append(li, k, v)
+    return dc
+
+
+def test_cross_window_bounds():
+    assert O.cross_window(100, 0) == 0          # no window: whole context
+    assert O.cross_window(100, 30) == 70        # the 30 most recent positions 70..99
+    assert O.cross_window(100, 100) == 0
+    assert O.cross_window(20, 1024) == 0        # short context: all of it
+
+
+def test_window_covering_the_context_equals_the_full_drafter(tiny):
+    wl, tg, dr = _tiny_models(tiny)
+    fused = np.random.default_rng(8).standard_normal((40, wl.target.hidden))
+    dc = _injected_cache(dr, fused, np.arange(40))
+    full = O.draft_logits(dr, tg, 7, 16, dc, NONE)
+    for W in (40, 41, 1024):
+        assert np.array_equal(O.draft_logits(dr, tg, 7, 16, dc, NONE, window=W), full)
+
+
+def test_window_edge_is_exactly_w_positions(tiny):
+    """Keys before P-W do not matter at all; the key at P-W does."""
+    wl, tg, dr = _tiny_models(tiny)
+    P, W = 50, 12
+    fused = np.random.default_rng(9).standard_normal((P, wl.target.hidden))
+    base = O.draft_logits(dr, tg, 3, 16, _injected_cache(dr, fused, np.arange(P)), NONE, window=W)
+    outside = fused.copy()
+    outside[: P - W] = np.random.default_rng(10).standard_normal((P - W, wl.target.hidden))
+    got = O.draft_logits(dr, tg, 3, 16, _injected_cache(dr, outside, np.arange(P)), NONE, window=W)
+    assert np.array_equal(got, base)
+    edge = fused.copy()
+    edge[P - W] += 1.0
+    got = O.draft_logits(dr, tg, 3, 16, _injected_cache(dr, edge, np.arange(P)), NONE, window=W)
+    assert not np.allclose(got, base, atol=1e-6)
+
+
+def test_window_equals_full_drafter_on_the_last_w_rows(tiny):
+    """With window W the drafter at P sees the W most recent context rows at
+    positions P-W..P-1 and the block at P..; by RoPE's relative-position
+    invariance that is the full drafter over a context of just those W rows
+    placed at positions 0..W-1 (block at W..)."""
+    wl, tg, dr = _tiny_models(tiny)
+    P, W = 70, 20
+    fused = np.random.default_rng(11).standard_normal((P, wl.target.hidden))
+    win = O.draft_logits(dr, tg, 9, 16, _injected_cache(dr, fused, np.arange(P)), NONE, window=W)
+    short = O.draft_logits(dr, tg, 9, 16, _injected_cache(dr, fused[P - W:], np.arange(W)), NONE)
+    assert np.allclose(win, short, atol=1e-9, rtol=0)
+    full = O.draft_logits(dr, tg, 9, 16, _injected_cache(dr, fused, np.arange(P)), NONE)
+    assert not np.allclose(win, full, atol=1e-6)
+
+
+def test_lossless_with_cross_window(tiny):
+    """The window only changes what the drafter proposes: the emitted stream
+    is still the greedy autoregressive one."""
+    wl, tg, dr = _tiny_models(tiny)
+    prompt = synth.prompt_tokens(wl.prompt_len, wl.target.vocab)
+    n = 24
+    ref, _ = O.greedy_ar(tg, prompt, n, NONE)
+    out, _ = O.spec_decode(tg, dr, prompt, n, 16, NONE, window=32)
+    assert np.array_equal(out, ref)
+
+
 # ---------------------------------------------------------------- losslessness
 
 
