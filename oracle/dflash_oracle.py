@@ -530,6 +530,127 @@ def spec_decode(tg: Target, dr: Draft, prompt, n_tokens, block, rnd, forcing=Non
     return np.array(emitted[:n_tokens], dtype=np.int64), steps
 
 
+# ---------------------------------------------------------------------------
+# Sampling mode (temperature T > 0)
+# ---------------------------------------------------------------------------
+#
+# "DFlash 深度解析" §4.2 reports the speed-up at temperature 1 with the
+# losslessness kept, and prints no rule.  The reading taken here is the
+# standard speculative-sampling rule, which keeps the emitted stream
+# distributed exactly as sampling the target alone:
+#   * the drafter samples slot j >= 1 from q_j = softmax(z_draft_j / T);
+#   * drafted token d_i (i = 1..B-1) is accepted when u_i * q_i(d_i) < p_{i-1}(d_i),
+#     p_{i-1} = softmax(z_target_{i-1} / T) being the target's distribution
+#     after slot i-1 (probability min(1, p/q));
+#   * at the first rejection (slot a+1) the step emits one token drawn from the
+#     residual max(0, p_a - q_{a+1}) (renormalised), and stops;
+#   * when every drafted token is accepted it emits a bonus token drawn from
+#     p_{B-1}.
+# A draw from a distribution w with a uniform v in [0, 1) is the inverse CDF:
+# the smallest t with w_0 + ... + w_t > v * (w_0 + ... + w_{V-1}).  Uniform
+# numbers are inputs (drawn by the caller).
+
+
+def softmax_t(logits, T):
+    """softmax(z / T) over the last axis, float64."""
+    z = f64(logits) / float(T)
+    z = z - np.max(z, axis=-1, keepdims=True)
+    e = np.exp(z)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def sample_inverse_cdf(weights, v):
+    """Index drawn from the non-negative weights with uniform v in [0, 1)."""
+    w = f64(weights)
+    c = np.cumsum(w)
+    return int(np.searchsorted(c, v * c[-1], side="right"))
+
+
+def draft_sample(draft_logits_rows, T, w_draws):
+    """Slots 1..B-1 sampled from q_j (rows of draft_logits_rows) with the
+    uniform draws w_draws[j-1]."""
+    q = softmax_t(draft_logits_rows, T)
+    return np.array([sample_inverse_cdf(q[j], w_draws[j]) for j in range(q.shape[0])], dtype=np.int64)
+
+
+def accept_sampling(draft_tokens, p_rows, q_rows, u, v):
+    """Speculative-sampling verification of one block (see above).
+
+    draft_tokens [B] (slot 0 = anchor); p_rows [B, V] target distributions
+    (row i: after slot i); q_rows [B-1, V] drafter distributions of slots
+    1..B-1; u [B-1] acceptance draws; v the draw of the residual / bonus
+    token.  Returns (a, emitted): a accepted drafts and the a + 1 emitted
+    tokens d_1..d_a, t."""
+    B = len(draft_tokens)
+    a = 0
+    while a < B - 1:
+        d = int(draft_tokens[a + 1])
+        p, q = p_rows[a], q_rows[a]
+        if u[a] * q[d] < p[d]:
+            a += 1
+            continue
+        resid = np.maximum(p - q, 0.0)
+        if not np.sum(resid) > 0.0:  # p == q: nothing left to correct, sample the target
+            resid = p
+        t = sample_inverse_cdf(resid, v)
+        return a, np.array([int(x) for x in draft_tokens[1:a + 1]] + [t], dtype=np.int64)
+    t = sample_inverse_cdf(p_rows[B - 1], v)
+    return a, np.array([int(x) for x in draft_tokens[1:B]] + [t], dtype=np.int64)
+
+
+def sample_ar(tg: Target, prompt, n_tokens, T, v_draws, rnd):
+    """Autoregressive sampling of the target at temperature T ([DD] §1.1 with
+    the argmax replaced by a draw): token k is drawn from softmax(z / T) of the
+    last row with the uniform v_draws[k]."""
+    sh = tg.shape
+    cache = KV.empty(sh.n_layers, sh.n_kv, sh.head_dim)
+    out = target_forward(tg, prompt, cache, rnd)
+    commit(cache, out, len(prompt))
+    toks = [sample_inverse_cdf(softmax_t(out.logits[-1], T), v_draws[0])]
+    while len(toks) < n_tokens:
+        out = target_forward(tg, [toks[-1]], cache, rnd)
+        commit(cache, out, 1)
+        toks.append(sample_inverse_cdf(softmax_t(out.logits[0], T), v_draws[len(toks)]))
+    return np.array(toks, dtype=np.int64)
+
+
+def spec_decode_sampling(tg: Target, dr: Draft, prompt, n_tokens, block, T, draws, rnd, window=0):
+    """DFlash speculative decoding in sampling mode: the loop of
+    ``spec_decode`` with the drafter sampling its block and the target
+    verifying by ``accept_sampling``.  draws = (v0, w[steps, B-1], u[steps,
+    B-1], v[steps]): v0 draws the prefill's first token, then each step uses
+    one row of w (drafting), u (acceptance) and v (residual or bonus).
+    Returns the emitted tokens and the per-step accepted counts."""
+    v0, w_all, u_all, v_all = draws
+    sh, dsh = tg.shape, dr.shape
+    tcache = KV.empty(sh.n_layers, sh.n_kv, sh.head_dim)
+    dcache = KV.empty(dsh.n_layers, dsh.n_kv, dsh.head_dim)
+    prompt = np.asarray(prompt, dtype=np.int64)
+    out = target_forward(tg, prompt, tcache, rnd)
+    commit(tcache, out, len(prompt))
+    pending = out.hcap
+    emitted = [sample_inverse_cdf(softmax_t(out.logits[-1], T), v0)]
+    anchor = emitted[0]
+    accepts = []
+    while len(emitted) < n_tokens:
+        s = len(accepts)
+        P = tcache.length()
+        m = pending.shape[0]
+        fused = fuse_features(dr, pending, rnd)
+        for li, (k, v) in enumerate(inject_kv(dr, fused, np.arange(P - m, P), rnd)):
+            dcache.append(li, k, v)
+        zq = draft_logits(dr, tg, anchor, block, dcache, rnd, window)
+        d = np.concatenate([[anchor], draft_sample(zq, T, w_all[s])]).astype(np.int64)
+        out = target_forward(tg, d, tcache, rnd)
+        a, em = accept_sampling(d, softmax_t(out.logits, T), softmax_t(zq, T), u_all[s], v_all[s])
+        accepts.append(a)
+        emitted.extend(int(t) for t in em)
+        commit(tcache, out, a + 1)
+        pending = out.hcap[: a + 1]
+        anchor = int(em[-1])
+    return np.array(emitted[:n_tokens], dtype=np.int64), accepts
+
+
 def tau(n_emitted_tokens, n_steps):
     """Mean tokens emitted per verification step."""
     return n_emitted_tokens / n_steps

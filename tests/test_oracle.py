@@ -400,6 +400,114 @@ def test_lossless_with_cross_window(tiny):
     assert np.array_equal(out, ref)
 
 
+# ---------------------------------------------------------------- sampling mode
+
+
+def test_inverse_cdf_hand_cases():
+    w = [0.0, 0.25, 0.0, 0.5, 0.25]
+    assert O.sample_inverse_cdf(w, 0.0) == 1           # zero-weight entries are never drawn
+    assert O.sample_inverse_cdf(w, 0.2499) == 1
+    assert O.sample_inverse_cdf(w, 0.25) == 3          # right-open intervals: [0.25, 0.75) -> 3
+    assert O.sample_inverse_cdf(w, 0.7499) == 3
+    assert O.sample_inverse_cdf(w, 0.75) == 4
+    assert O.sample_inverse_cdf(w, 0.999999) == 4
+    assert O.sample_inverse_cdf([3.0, 1.0], 0.74) == 0  # unnormalised weights
+    assert O.sample_inverse_cdf([3.0, 1.0], 0.76) == 1
+
+
+def test_softmax_t_closed_forms():
+    z = np.array([[1.0, 2.0, 4.0]])
+    assert np.allclose(O.softmax_t(z, 1.0), np.exp(z) / np.exp(z).sum())
+    assert np.allclose(O.softmax_t(z, 2.0), np.exp(z / 2) / np.exp(z / 2).sum())
+    assert np.allclose(O.softmax_t(z + 100.0, 0.7), O.softmax_t(z, 0.7))
+    assert O.softmax_t(z, 1e-3)[0, 2] == 1.0                       # T -> 0: the argmax
+
+
+def _emit_distribution(p0, q1, p1, n=4000, rule=None):
+    """Exact-by-quadrature distribution of the first emitted token of a
+    two-slot block (one drafted token d ~ q1): acceptance depends on u alone,
+    the residual on v alone, so each is integrated over its own midpoint grid."""
+    rule = rule or O.accept_sampling
+    V = len(p0)
+    grid = (np.arange(n) + 0.5) / n
+    out = np.zeros(V)
+    p_rows, q_rows = np.stack([p0, p1]), q1[None, :]
+    for d in range(V):
+        draft = [0, d]
+        acc = np.mean([rule(draft, p_rows, q_rows, [u], 0.5)[0] == 1 for u in grid])
+        out[d] += q1[d] * acc
+        if acc < 1.0:
+            firsts = [rule(draft, p_rows, q_rows, [1.0 - 1e-12], v)[1][0] for v in grid]
+            out += q1[d] * (1.0 - acc) * np.bincount(firsts, minlength=V) / n
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_accept_sampling_emits_the_target_distribution(seed):
+    """Speculative sampling is lossless: whatever the drafter's q, the first
+    emitted token is distributed exactly as the target's p."""
+    rng = np.random.default_rng(seed)
+    V = 5
+    p0, p1 = rng.dirichlet(np.ones(V)), rng.dirichlet(np.ones(V))
+    q1 = rng.dirichlet(np.ones(V) * 0.5)
+    dist = _emit_distribution(p0, q1, p1)
+    assert np.allclose(dist, p0, atol=1e-3), (dist, p0)
+    # planted mistake: with the roles of p and q swapped in the verification
+    # (accept with min(1, q/p), residual max(0, q - p)) the output is not p
+    def swapped(d, p, q, u, v):
+        return O.accept_sampling(d, np.stack([q[0], p[1]]), p[:1], u, v)
+    wrong = _emit_distribution(p0, q1, p1, n=1000, rule=swapped)
+    assert np.max(np.abs(wrong - p0)) > 2e-2
+
+
+def test_accept_sampling_bonus_and_residual_structure():
+    V = 4
+    p = np.array([[0.1, 0.2, 0.3, 0.4], [0.25, 0.25, 0.25, 0.25], [0.7, 0.1, 0.1, 0.1]])
+    q = np.array([[0.1, 0.2, 0.3, 0.4], [0.25, 0.25, 0.25, 0.25]])
+    # q == p: always accepted, the bonus comes from the last target row
+    a, em = O.accept_sampling([9, 3, 1], p, q, [0.99, 0.99], 0.05)
+    assert a == 2 and em.tolist() == [3, 1, 0]
+    # q puts all its mass on a token the target gives 0.1: accepted only for u < 0.1
+    q2 = np.array([[0.0, 1.0, 0.0, 0.0], [0.25, 0.25, 0.25, 0.25]])
+    p2 = np.array([[0.4, 0.1, 0.1, 0.4], [0.25, 0.25, 0.25, 0.25], [1.0, 0.0, 0.0, 0.0]])
+    assert O.accept_sampling([9, 1, 2], p2, q2, [0.09, 0.5], 0.0)[0] == 2
+    a, em = O.accept_sampling([9, 1, 2], p2, q2, [0.11, 0.5], 0.6)
+    # residual max(0, p - q) = [0.4, 0, 0.1, 0.4]: v = 0.6 -> 0.54 falls in [0.5, 0.9) -> token 3
+    assert a == 0 and em.tolist() == [3]
+    assert O.accept_sampling([9, 1, 2], p2, q2, [0.11, 0.5], 0.5)[1].tolist() == [2]
+
+
+def test_sampling_at_vanishing_temperature_is_greedy(tiny):
+    """As T -> 0 every distribution collapses onto its argmax: drafting
+    becomes the drafter's argmax, acceptance becomes equality with the
+    target's argmax, the residual and the bonus become the target's argmax --
+    the greedy loop, token for token."""
+    wl, tg, dr = _tiny_models(tiny)
+    prompt = synth.prompt_tokens(wl.prompt_len, wl.target.vocab)
+    n, B = 24, 8
+    rng = np.random.default_rng(12)
+    steps = n
+    draws = (rng.random(), rng.random((steps, B - 1)), rng.random((steps, B - 1)), rng.random(steps))
+    got, accepts = O.spec_decode_sampling(tg, dr, prompt, n, B, 1e-9, draws, NONE)
+    ref, _ = O.spec_decode(tg, dr, prompt, n, B, NONE)
+    assert np.array_equal(got, ref)
+    greedy, _ = O.greedy_ar(tg, prompt, n, NONE)
+    assert np.array_equal(O.sample_ar(tg, prompt, n, 1e-9, rng.random(n), NONE), greedy)
+
+
+def test_sampling_loop_is_consistent_with_its_draws(tiny):
+    """At T = 1 the loop's accepted counts and emitted tokens follow from its
+    own verification of each step (re-derived from the recorded draws)."""
+    wl, tg, dr = _tiny_models(tiny)
+    prompt = synth.prompt_tokens(wl.prompt_len, wl.target.vocab)
+    n, B = 40, 16
+    rng = np.random.default_rng(13)
+    draws = (rng.random(), rng.random((n, B - 1)), rng.random((n, B - 1)), rng.random(n))
+    got, accepts = O.spec_decode_sampling(tg, dr, prompt, n, B, 1.0, draws, NONE)
+    assert len(got) == n and sum(a + 1 for a in accepts) + 1 >= n
+    assert all(0 <= a <= B - 1 for a in accepts)
+
+
 # ---------------------------------------------------------------- losslessness
 
 
