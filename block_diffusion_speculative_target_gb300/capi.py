@@ -70,7 +70,10 @@ _SIGS = {
     "dflash_workspace_alloc": (_I, [POINTER(ModelDesc), POINTER(ModelDesc), _I, _I, POINTER(c_void_p)]),
     "dflash_workspace_free": (_I, [_P]),
     "dflash_status": (_I, [_P, _P, POINTER(c_int32)]),
-    "dflash_workspace_logits": (c_void_p, [_P]),
+    "dflash_workspace_logits": (c_void_p, [_P, _I]),
+    "dflash_draft_sample": (_I, [_I, _I, _I, c_float, _P, _P, _P, _P]),
+    "dflash_accept_sample": (_I, [_P, _I, _I, _I, c_float, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P]),
+    "dflash_sample": (_I, [_P, _I, _I, c_float, _P, _P, _P, _P]),
     "dflash_debug_set_wait_limit": (_I, [ctypes.c_int64]),
     "dflash_fuse_features": (_I, [POINTER(DraftC), _P, _I, _P, _P, _P]),
     "dflash_inject_kv": (_I, [POINTER(DraftC), _P, _I, _I, _P, _P, _P, _P]),
@@ -210,12 +213,13 @@ def dflash_status(ws, stream=None):
     return v.value
 
 
-def dflash_workspace_logits(ws, rows, vocab):
+def dflash_workspace_logits(ws, rows, vocab, which=0):
     """The workspace's float32 logits [rows][vocab] as a torch tensor view
-    (device memory owned by the workspace; valid until the next call)."""
+    (which = 0: the target's, 1: the drafter's; device memory owned by the
+    workspace, valid until the next call that writes it)."""
     import torch
 
-    p = load().dflash_workspace_logits(ws)
+    p = load().dflash_workspace_logits(ws, which)
     if not p:
         raise DFlashError("dflash_workspace_logits: no workspace")
     return _device_view(p, rows * vocab, torch.float32).view(rows, vocab)
@@ -275,6 +279,26 @@ def dflash_teacher_force(draft_tokens, batch, block, ref, ref_stride, ref_len, s
     _check(load().dflash_teacher_force(_ptr(draft_tokens), batch, block, _ptr(ref), ref_stride, ref_len,
                                        _ptr(stream_len), _ptr(k_draw), _ptr(r_draw), max_steps, _ptr(step), vocab, ws,
                                        _stream(stream)), "dflash_teacher_force")
+
+
+# ---------------------------------------------------------------- sampling mode
+
+
+def dflash_draft_sample(batch, block, vocab, temperature, w, draft_tokens, ws, stream=None):
+    _check(load().dflash_draft_sample(batch, block, vocab, float(temperature), _ptr(w), _ptr(draft_tokens), ws,
+                                      _stream(stream)), "dflash_draft_sample")
+
+
+def dflash_accept_sample(draft_tokens, batch, block, vocab, temperature, u, v, target_cache, anchor, n_pend,
+                         accept_len, stream_buf, stream_len, stream_cap, ws, stream=None):
+    _check(load().dflash_accept_sample(_ptr(draft_tokens), batch, block, vocab, float(temperature), _ptr(u), _ptr(v),
+                                       target_cache, _ptr(anchor), _ptr(n_pend), _ptr(accept_len), _ptr(stream_buf),
+                                       _ptr(stream_len), stream_cap, ws, _stream(stream)), "dflash_accept_sample")
+
+
+def dflash_sample(logits, rows, vocab, temperature, v, out, ws, stream=None):
+    _check(load().dflash_sample(_ptr(logits), rows, vocab, float(temperature), _ptr(v), _ptr(out), ws,
+                                _stream(stream)), "dflash_sample")
 
 
 # ---------------------------------------------------------------- building blocks

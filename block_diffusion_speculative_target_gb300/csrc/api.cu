@@ -47,7 +47,11 @@ struct dflash_workspace {
   void* q;
   void* attn;
   void* act;
-  float* logits;
+  float* logits;   // the target's logits [rows][V] (target_verify)
+  float* dlogits;  // the drafter's logits [rows][V] (dflash_draft_block)
+  float2* tstats;  // sampling: per-row (max, sum) of the target's logits
+  float2* dstats;  // sampling: the same for the drafter's logits
+  int32_t vocab;
   AttnScratch as;
   ArgmaxScratch am;
   int* status;
@@ -290,6 +294,9 @@ int dflash_workspace_alloc(const dflash_model_desc* t, const dflash_model_desc* 
       {(void**)&w->attn, R * qw * es},
       {(void**)&w->act, R * F * es},
       {(void**)&w->logits, R * V * 4},
+      {(void**)&w->dlogits, R * V * 4},
+      {(void**)&w->tstats, R * 8},
+      {(void**)&w->dstats, R * 8},
 
       {(void**)&w->as.o, R * nq * nchunk * 128 * 4},
       {(void**)&w->as.ml, R * nq * nchunk * 2 * 4},
@@ -308,6 +315,7 @@ int dflash_workspace_alloc(const dflash_model_desc* t, const dflash_model_desc* 
     w->allocs.push_back(p);
   }
   w->as.nchunk = nchunk;
+  w->vocab = (int32_t)V;
   w->am.max_rows = (int)R;
   cudaMemset(w->am.tickets, 0, R * 4);
 
@@ -328,7 +336,10 @@ int dflash_workspace_free(dflash_workspace* w) {
   return DFLASH_OK;
 }
 
-float* dflash_workspace_logits(dflash_workspace* w) { return w ? w->logits : nullptr; }
+float* dflash_workspace_logits(dflash_workspace* w, int32_t which) {
+  if (!w || which < 0 || which > 1) return nullptr;
+  return which == 0 ? w->logits : w->dlogits;
+}
 
 int dflash_debug_set_wait_limit(int64_t ns) {
   set_gemm_wait_ns((long long)ns);
@@ -482,7 +493,7 @@ static int layer_forward_f32(const dflash_model_desc& d, const dflash_layer_w& w
 // positions (the drafter's cross-context window).
 static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layers, dflash_cache* c, int batch, int n,
                          int causal, int window, const int32_t* capture, void* hcap, const void* final_norm,
-                         const void* lm_head, dflash_workspace* ws, cudaStream_t s) {
+                         const void* lm_head, float* logits, dflash_workspace* ws, cudaStream_t s) {
   const int rows = batch * n, H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, L = d.n_layers;
   for (int l = 0; l < L; ++l) {
     const dflash_layer_w& w = layers[l];
@@ -497,7 +508,7 @@ static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layer
           if (capture[si] == l) CK(dfl::capture(d.dtype, ws->x, hcap, rows, H, si, s));
     }
     CK(rmsnorm(d.dtype, ws->x, final_norm, ws->xn, rows, H, d.rms_eps, s));
-    CK(gemm_f32(ws->xn, H, rows, lm_head, d.vocab, H, Epi{EPI_F32, ws->logits, d.vocab}, s));
+    CK(gemm_f32(ws->xn, H, rows, lm_head, d.vocab, H, Epi{EPI_F32, logits, d.vocab}, s));
     return DFLASH_OK;
   }
   const int qkvw = (nq + 2 * nkv) * hd;
@@ -523,7 +534,7 @@ static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layer
     CK(gemm_b16(ws->act, d.ffn, rows, w.w_down, H, d.ffn, down, ws, s));
   }
   CK(rmsnorm(d.dtype, ws->x, final_norm, ws->xn, rows, H, d.rms_eps, s));
-  CK(gemm_b16(ws->xn, H, rows, lm_head, d.vocab, H, epi_of(GE_F32, ws->logits, d.vocab), ws, s));
+  CK(gemm_b16(ws->xn, H, rows, lm_head, d.vocab, H, epi_of(GE_F32, logits, d.vocab), ws, s));
   return DFLASH_OK;
 }
 
@@ -544,7 +555,8 @@ int target_verify(const dflash_target* tg, const int32_t* tokens, int32_t batch,
   cudaStream_t s = (cudaStream_t)cuda_stream;
   const int rows = batch * n, H = d.hidden;
   CK(embed(d.dtype, tg->embed, d.vocab, H, tokens, nullptr, 0, batch, n, 0, nullptr, ws->x, ws->status, s));
-  int rc = decoder_stack(d, tg->layers, tc, batch, n, 1, 0, tg->capture, hcap, tg->final_norm, tg->lm_head, ws, s);
+  int rc = decoder_stack(d, tg->layers, tc, batch, n, 1, 0, tg->capture, hcap, tg->final_norm, tg->lm_head,
+                         ws->logits, ws, s);
   if (rc != DFLASH_OK) return rc;
   CK(argmax(ws->logits, rows, d.vocab, argmax_out, top2_gap, 0, ws->am, ws->status, s));
   if (commit)
@@ -611,9 +623,9 @@ int dflash_draft_block(const dflash_draft* dr, const dflash_target* tg, const in
   CK(embed(d.dtype, tg->embed, d.vocab, H, nullptr, anchor, dr->mask_id, batch, block, 1, draft_tokens, ws->x,
            ws->status, s));
   int rc = decoder_stack(d, dr->layers, dc, batch, block, 0, dr->cross_ctx, nullptr, nullptr, dr->final_norm,
-                         tg->lm_head, ws, s);
+                         tg->lm_head, ws->dlogits, ws, s);
   if (rc != DFLASH_OK) return rc;
-  CK(argmax(ws->logits, rows, d.vocab, draft_tokens, nullptr, block, ws->am, ws->status, s));
+  CK(argmax(ws->dlogits, rows, d.vocab, draft_tokens, nullptr, block, ws->am, ws->status, s));
   return DFLASH_OK;
 }
 
@@ -637,6 +649,43 @@ int dflash_teacher_force(int32_t* draft_tokens, int32_t batch, int32_t block, co
       vocab > 1);
   CK(teacher_force(draft_tokens, batch, block, ref, ref_stride, ref_len, stream_len, k_draw, r_draw, max_steps, step,
                    vocab, ws->status, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------ sampling mode
+int dflash_draft_sample(int32_t batch, int32_t block, int32_t vocab, float temperature, const float* w,
+                        int32_t* draft_tokens, dflash_workspace* ws, dflash_stream_t stream) {
+  REQ(ws && w && draft_tokens && batch > 0 && block >= 2 && batch * block <= ws->max_rows);
+  REQ(vocab > 1 && vocab <= ws->vocab && temperature > 0.f && isfinite(temperature));
+  cudaStream_t s = (cudaStream_t)stream;
+  const int rows = batch * block;
+  CK(softmax_stats(ws->dlogits, rows, vocab, temperature, ws->dstats, s));
+  CK(sample_rows(ws->dlogits, rows, vocab, temperature, ws->dstats, w, block, draft_tokens, s));
+  return DFLASH_OK;
+}
+
+int dflash_accept_sample(const int32_t* draft_tokens, int32_t batch, int32_t block, int32_t vocab, float temperature,
+                         const float* u, const float* v, dflash_cache* tc, int32_t* anchor, int32_t* n_pend,
+                         int32_t* accept_len, int32_t* stream, int32_t* stream_len, int32_t stream_cap,
+                         dflash_workspace* ws, dflash_stream_t cuda_stream) {
+  REQ(draft_tokens && u && v && tc && anchor && n_pend && ws);
+  REQ(batch > 0 && batch <= tc->batch && block >= 2 && block <= 32 && batch * block <= ws->max_rows);
+  REQ(vocab > 1 && vocab <= ws->vocab && temperature > 0.f && isfinite(temperature));
+  REQ(!stream || (stream_len && stream_cap > 0));
+  cudaStream_t s = (cudaStream_t)cuda_stream;
+  CK(softmax_stats(ws->logits, batch * block, vocab, temperature, ws->tstats, s));
+  CK(accept_sample(draft_tokens, ws->logits, ws->dlogits, ws->tstats, ws->dstats, batch, block, vocab, temperature, u,
+                   v, tc->len, anchor, n_pend, accept_len, stream, stream_len, stream_cap, ws->status, s));
+  return DFLASH_OK;
+}
+
+int dflash_sample(const float* logits, int32_t rows, int32_t vocab, float temperature, const float* v, int32_t* out,
+                  dflash_workspace* ws, dflash_stream_t stream) {
+  REQ(logits && v && out && ws && rows > 0 && rows <= ws->max_rows && vocab > 1);
+  REQ(temperature > 0.f && isfinite(temperature));
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(softmax_stats(logits, rows, vocab, temperature, ws->tstats, s));
+  CK(sample_rows(logits, rows, vocab, temperature, ws->tstats, v, 0, out, s));
   return DFLASH_OK;
 }
 

@@ -42,13 +42,23 @@ namespace dfl {
 
 namespace {
 constexpr int kFaThreads = 320;
-constexpr int kStages = 3;
 constexpr uint32_t kTileBytes = 128 * 256;           // 128 keys x 128 dims bf16, two 64-dim halves
 constexpr uint32_t kStageBytes = 2 * kTileBytes;     // keys then values
-constexpr uint32_t kQ = kStages * kStageBytes;       // query [d-half][128 rows][128 B]
-constexpr uint32_t kBar = kQ + 32768;                // barriers, TMEM slot, abort flag
-constexpr int kFaSmem = kBar + 256 + 1024;           // + alignment slack
-constexpr uint32_t kTmemCols = 512;                  // S0 S1 (P aliased) | O0 O1
+constexpr uint32_t kTmemCols = 512;                  // S0 S1 (P written over S) | O0 O1
+
+// Shared-memory layout per GQA group size G: a 3-stage ring when the query
+// tile (16 G rows) leaves room in its 128-row region for the two halves'
+// row-maximum exchange [2 buffers][2 halves][128 rows] (G <= 5), else a
+// 2-stage ring with the exchange after the query tile.
+template <int G>
+struct FaLayout {
+  static constexpr int kStages = G <= 5 ? 3 : 2;
+  static constexpr uint32_t kQ = kStages * kStageBytes;                     // query [d-half][128 rows][128 B]
+  static constexpr uint32_t kXch = G <= 5 ? kQ + 16 * G * 128 : kQ + 32768; // exchange, 2 KB
+  static constexpr uint32_t kBar = G <= 5 ? kQ + 32768 : kXch + 2048;       // barriers, TMEM slot, abort flag
+  static constexpr int kSmem = kBar + 256 + 1024;                           // + alignment slack
+  static_assert(G > 5 || 16 * G * 128 + 2048 <= 16384, "exchange must fit in the query tile's padding rows");
+};
 constexpr uint64_t kFaWaitNs = 500000000ull;
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -116,9 +126,13 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                    const __grid_constant__ CUtensorMap tmQ, int batch, int n, int nq, int nkv, int causal, int window,
                    long long row0, int capacity, int gtiles, int ngroups, const int32_t* __restrict__ len,
                    float* __restrict__ part_o, float* __restrict__ part_ml, float scale_log2, int* status) {
+  using Ly = FaLayout<G>;
+  constexpr int kStages = Ly::kStages;
+  constexpr uint32_t kQ = Ly::kQ;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kBar);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Ly::kBar);
+  float* xch = reinterpret_cast<float*>(sm + Ly::kXch);  // [2][2][128] row maxima of each half
   uint64_t* kv_full = bar;        // [3] a tile's keys and values landed
   uint64_t* kv_empty = bar + 3;   // [3] its products completed
   uint64_t* q_full = bar + 6;
@@ -127,7 +141,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   uint64_t* o_full = bar + 11;    // [2] O_t in TMEM
   uint64_t* o_free = bar + 13;    // [2] O_t read out (one arrival per softmax warp)
   uint64_t* drain = bar + 15;     // every issued product completed
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
+  uint64_t* xch_full = bar + 16;  // [2] both halves' maxima written (one arrival per softmax thread)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 18);
   volatile int* abort_f = reinterpret_cast<volatile int*>(tslot + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {  // the descriptors are kernel parameters: fetch them while the previous kernel drains
@@ -157,7 +172,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   if (nt <= 0) return;  // uniform over the CTA: no key of this group is visible
 
   if (tid == 0) {
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
@@ -169,6 +184,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       mbar_init(&o_free[i], 8);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&xch_full[i], 256);
     *abort_f = 0;
     fence_barrier_init();
   }
@@ -241,7 +257,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           for (int pass = 0; pass < 2; ++pass)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              tc_mma_f16_tmem_a(tmem + 256 + wb * 128, tmem + wb * 128 + pass * 64 + kk * 8,
+              tc_mma_f16_tmem_a(tmem + 256 + wb * 128, tmem + wb * 128 + (kk >> 2) * 64 + pass * 32 + (kk & 3) * 8,
                                 smem_desc_mn(vt + kk * 2048, 16384), idO, (pass | kk) != 0 ? 1u : 0u);
           tc_commit(&o_full[wb]);
           tc_commit(&kv_empty[s]);
@@ -277,44 +293,69 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (uint32_t)(t >> 1) & 1u, kFaWaitNs));
         if (__any_sync(0xffffffffu, !ok || *abort_f)) break;  // warp-uniform
         tc_fence_after();
-        if (live) {
-          const int k0 = (ta + t) * 128;
-          const uint32_t sbase = tmem + lrow + sb * 128;
-          // the tile max over all 128 scores (both halves), 32 columns at a time
-          float mraw = -INFINITY;
-#pragma unroll 1
-          for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t v[32];
-            tmem_ld32(sbase + c4 * 32, v);
-            tmem_ld_wait();
-            const int kb = k0 + c4 * 32;
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (kb + e >= lo && kb + e < lim) mraw = fmaxf(mraw, __uint_as_float(v[e]));
-          }
-          // the tile max in log2 units (scale > 0: max(s) * scale = max(s * scale))
-          m_cur = mraw * scale_log2;
-          const float negm = mraw == -INFINITY ? 0.f : -m_cur;
-          // P of this thread's half, 32 keys at a time, written over the scores
+        const int k0 = (ta + t) * 128 + h * 64;            // this half's first key
+        const uint32_t sbase = tmem + lrow + sb * 128 + h * 64;  // this half's 64 score columns
+        float lm = -INFINITY;
+        if (live) {  // this half's maximum over its visible scores
 #pragma unroll 1
           for (int c2 = 0; c2 < 2; ++c2) {
-            uint32_t v[32], hi[16], lo_[16];
-            tmem_ld32(sbase + h * 64 + c2 * 32, v);
+            uint32_t v[32];
+            tmem_ld32(sbase + c2 * 32, v);
             tmem_ld_wait();
-            const int kb = k0 + h * 64 + c2 * 32;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int k = k0 + c2 * 32 + e;
+              if (k >= lo && k < lim) lm = fmaxf(lm, __uint_as_float(v[e]));
+            }
+          }
+          xch[(sb * 2 + h) * 128 + r] = lm;
+        }
+        mbar_arrive(&xch_full[sb]);
+        ok = __all_sync(0xffffffffu, mbar_wait(&xch_full[sb], (uint32_t)(t >> 1) & 1u, kFaWaitNs));
+        if (__any_sync(0xffffffffu, !ok || *abort_f)) break;  // warp-uniform
+        if (live) {
+          // the tile max in log2 units (scale > 0: max(s) * scale = max(s * scale))
+          const float mraw = fmaxf(lm, xch[(sb * 2 + (1 - h)) * 128 + r]);
+          m_cur = mraw * scale_log2;
+          const float negm = mraw == -INFINITY ? 0.f : -m_cur;
+          // P of this half as bf16 hi/lo pairs written over its own score
+          // columns only: hi at +0..31, lo at +32..63.  Keys 0..31 of the half
+          // are read first; their lo pairs wait in registers until keys 32..63
+          // (whose scores the lo pairs overwrite) have been read too.
+          uint32_t hiA[16], loA[16];
+          {
+            uint32_t v[32];
+            tmem_ld32(sbase, v);
+            tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const int k = kb + 2 * e;
-              const float p0 =
-                  (k >= lo && k < lim) ? ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm)) : 0.f;
+              const int k = k0 + 2 * e;
+              const float p0 = (k >= lo && k < lim) ? ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm)) : 0.f;
               const float p1 =
                   (k + 1 >= lo && k + 1 < lim) ? ex2f(fmaf(__uint_as_float(v[2 * e + 1]), scale_log2, negm)) : 0.f;
               l_cur += p0;
               l_cur += p1;
-              pack_bf16_hilo(p0, p1, hi[e], lo_[e]);
+              pack_bf16_hilo(p0, p1, hiA[e], loA[e]);
             }
-            tmem_st16(sbase + h * 32 + c2 * 16, hi);
-            tmem_st16(sbase + 64 + h * 32 + c2 * 16, lo_);
+          }
+          tmem_st16(sbase, hiA);
+          {
+            uint32_t v[32], hiB[16], loB[16];
+            tmem_ld32(sbase + 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int k = k0 + 32 + 2 * e;
+              const float p0 = (k >= lo && k < lim) ? ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm)) : 0.f;
+              const float p1 =
+                  (k + 1 >= lo && k + 1 < lim) ? ex2f(fmaf(__uint_as_float(v[2 * e + 1]), scale_log2, negm)) : 0.f;
+              l_cur += p0;
+              l_cur += p1;
+              pack_bf16_hilo(p0, p1, hiB[e], loB[e]);
+            }
+            tmem_st16(sbase + 16, hiB);
+            tmem_st16(sbase + 32, loA);
+            tmem_st16(sbase + 48, loB);
           }
           tmem_st_wait();
         }
@@ -433,10 +474,12 @@ cudaError_t attention_fa(int G, const KvMaps& maps, const CUtensorMap& qmap, int
   case GG: {                                                                                                     \
     static bool set = false;                                                                                     \
     if (!set) {                                                                                                  \
-      DFL_RET(cudaFuncSetAttribute(attn_fa_kernel<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFaSmem));   \
+      DFL_RET(cudaFuncSetAttribute(attn_fa_kernel<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize,              \
+                                   FaLayout<GG>::kSmem));                                                        \
       set = true;                                                                                                \
     }                                                                                                            \
-    DFL_RET(launch_pdl(attn_fa_kernel<GG>, dim3((unsigned)units), dim3(kFaThreads), kFaSmem, s, maps.k, maps.v,  \
+    DFL_RET(launch_pdl(attn_fa_kernel<GG>, dim3((unsigned)units), dim3(kFaThreads), FaLayout<GG>::kSmem, s,       \
+                       maps.k, maps.v,                                                                             \
                        qmap, batch, n, nq, nkv, causal, window, maps.row0, capacity, gtiles, sc.nchunk, len, sc.o, \
                        sc.ml, scale_log2, status));                                                              \
     return cudaSuccess;                                                                                          \

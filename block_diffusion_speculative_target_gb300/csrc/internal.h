@@ -172,6 +172,17 @@ cudaError_t argmax(const float* logits, int rows, int V, int32_t* argmax_out, fl
 // returns DFLASH_ERR_CUDA.
 int record_cuda_error(cudaError_t e);
 
+// Sampling mode: per-row (max, sum of 2^((z - max) log2e / T)); one inverse-CDF
+// draw per row (rows r % skip_first_of == 0 skipped when skip_first_of > 0);
+// speculative-sampling verification + rollback of one block per sequence.
+cudaError_t softmax_stats(const float* logits, int rows, int V, float temperature, float2* stats, cudaStream_t s);
+cudaError_t sample_rows(const float* logits, int rows, int V, float temperature, const float2* stats, const float* v,
+                        int skip_first_of, int32_t* out, cudaStream_t s);
+cudaError_t accept_sample(const int32_t* draft, const float* zt, const float* zd, const float2* tst, const float2* dst,
+                          int batch, int block, int V, float temperature, const float* u, const float* v, int32_t* len,
+                          int32_t* anchor, int32_t* n_pend, int32_t* accept_len, int32_t* stream, int32_t* stream_len,
+                          int stream_cap, int* status, cudaStream_t s);
+
 cudaError_t commit_rows(int32_t* len, int32_t* n_pend, int32_t* anchor, const int32_t* argmax, int batch, int n,
                         int emit, int32_t* stream, int32_t* stream_len, int stream_cap, int* status,
                         cudaStream_t s);

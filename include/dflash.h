@@ -162,13 +162,14 @@ int dflash_workspace_alloc(const dflash_model_desc *target, const dflash_model_d
 int dflash_workspace_free(dflash_workspace *w);
 /* Synchronises `stream`, returns the status bits in *status_out and clears them. */
 int dflash_status(dflash_workspace *w, dflash_stream_t stream, int32_t *status_out);
-/* Device pointer to the workspace's float32 logits, row-major [rows][vocab]:
- * after target_verify (rows = batch * n) or dflash_draft_block (rows =
- * batch * block) they hold that call's logits, the last RMSNorm'd residual
- * times the LM head ([DD] §1.1: the target's next-token scores), until the
- * next call on the workspace overwrites them.  Owned by the workspace; NULL
- * for a NULL workspace.  No synchronisation: read it on the same stream. */
-float *dflash_workspace_logits(dflash_workspace *w);
+/* Device pointer to one of the workspace's float32 logit buffers, row-major
+ * [rows][vocab]: which = 0 the target's, written by target_verify (rows =
+ * batch * n); which = 1 the drafter's, written by dflash_draft_block (rows =
+ * batch * block).  Each holds the last RMSNorm'd residual times the LM head
+ * ([DD] §1.1 next-token scores; §3.3 the drafter shares the head) until the
+ * next such call on the workspace.  Owned by the workspace; NULL for a NULL
+ * workspace or another `which`.  No synchronisation: read it on the stream. */
+float *dflash_workspace_logits(dflash_workspace *w, int32_t which);
 /* Failure-path testing: sets the limit, in nanoseconds, of the waits in the
  * main loop of the weight-product kernel (ring slots and accumulator) for
  * launches enqueued afterwards; a negative value restores the default of
@@ -262,6 +263,44 @@ int dflash_teacher_force(int32_t *draft_tokens, int32_t batch, int32_t block, co
                          int32_t ref_stride, int32_t ref_len, const int32_t *stream_len,
                          const int32_t *k_draw, const int32_t *r_draw, int32_t max_steps,
                          int32_t *step, int32_t vocab, dflash_workspace *ws, dflash_stream_t stream);
+
+/* ------------------------------------------------------------ sampling mode
+ * "DFlash 深度解析" §4.2: the speed-up holds at temperature 1 with the
+ * output distribution unchanged; the page gives no rule.  These calls take
+ * the standard speculative-sampling rule: with p_i = softmax(target logits of
+ * row i / T) and q_j = softmax(drafter logits of slot j / T),
+ *   - the drafter's slot j >= 1 is drawn from q_j;
+ *   - drafted token d_i (i = 1..block-1) is accepted when u_i q_i(d_i) <
+ *     p_{i-1}(d_i) (probability min(1, p/q)), stopping at the first rejection;
+ *   - after a accepted drafts one more token is drawn: from the residual
+ *     max(0, p_a - q_{a+1}) (renormalised; from p_a when it has no mass) when
+ *     a < block-1, from p_{block-1} otherwise.
+ * A draw from weights w with uniform v in [0, 1) is the smallest index whose
+ * running sum exceeds v * sum(w); uniform numbers are caller-supplied device
+ * float32 arrays.  Softmax statistics and running sums are float32 in a fixed
+ * order.  temperature must be finite and > 0, else DFLASH_ERR_INVALID_ARG. */
+
+/* After dflash_draft_block: draft_tokens[b][j] (j = 1..block-1) drawn from
+ * the drafter's logits (workspace buffer 1) at temperature T with
+ * w[b][j-1] ([batch][block-1]); slot 0 keeps the anchor. */
+int dflash_draft_sample(int32_t batch, int32_t block, int32_t vocab, float temperature, const float *w,
+                        int32_t *draft_tokens, dflash_workspace *ws, dflash_stream_t stream);
+/* After target_verify of the drafted block (commit = 0): verification by the
+ * rule above with u [batch][block-1] and v [batch], then the same rollback as
+ * dflash_accept_rollback: emitted = d_1..d_a and the drawn token (a + 1
+ * tokens) appended to stream; target len += a + 1; anchor = the drawn token;
+ * n_pend = a + 1; accept_len[b] = a (nullable).  Reads both workspace logit
+ * buffers; a drafted id outside [0, vocab) sets DFLASH_STATUS_BOUNDS and stops
+ * that sequence's acceptance there. */
+int dflash_accept_sample(const int32_t *draft_tokens, int32_t batch, int32_t block, int32_t vocab,
+                         float temperature, const float *u, const float *v, dflash_cache *target_cache,
+                         int32_t *anchor, int32_t *n_pend, int32_t *accept_len, int32_t *stream,
+                         int32_t *stream_len, int32_t stream_cap, dflash_workspace *ws,
+                         dflash_stream_t cuda_stream);
+/* One draw per row of float32 logits [rows][vocab] at temperature T with
+ * v[rows]: out[rows] (autoregressive sampling, the prefill's first token). */
+int dflash_sample(const float *logits, int32_t rows, int32_t vocab, float temperature, const float *v,
+                  int32_t *out, dflash_workspace *ws, dflash_stream_t stream);
 
 /* -------------------------------------------------------- building blocks
  * The kernels behind the stages, exposed for unit parity tests. */

@@ -223,7 +223,7 @@ def test_draft_full_width(wide):
     tgc, drc = m.structs()
     capi.dflash_draft_block(drc, tgc, s.anchor, 1, B, s.dcache, s.draft, s.ws)
     got = s.draft.cpu().numpy()[0]
-    logits = to_np(capi.dflash_workspace_logits(s.ws, B, sh.vocab))[1:]
+    logits = to_np(capi.dflash_workspace_logits(s.ws, B, sh.vocab, which=1))[1:]
     ref_logits = O.draft_logits(dr, tg, anchor, B, kv, rounder(wl))
     ref_tok, gap = O.argmax_top2(ref_logits)
     assert got[0] == anchor

@@ -78,7 +78,7 @@ def test_draft_block_with_window(setup, W):
     finally:
         m.set_cross_ctx(0)
     got = s.draft.cpu().numpy()
-    lg = to_np(capi.dflash_workspace_logits(s.ws, batch * B, sh.vocab)).reshape(batch, B, -1)
+    lg = to_np(capi.dflash_workspace_logits(s.ws, batch * B, sh.vocab, which=1)).reshape(batch, B, -1)
     rnd = rounder(wl)
     for b in range(batch):
         ref_logits = O.draft_logits(dr, tg, int(anchors[b]), B, kvs[b], rnd, window=W)
