@@ -209,6 +209,8 @@ class Session:
                 for c0 in range(0, len(p), self.chunk):
                     n = min(self.chunk, len(p) - c0)
                     last = c0 + n == len(p)
+                    if last:
+                        self._last_chunk_rows = n
                     capi.target_verify(tgt, toks[c0:c0 + n], 1, n, 2 if last else 1, tv, self.argmax, self.gap,
                                        self.hcap if dv else None, self.anchor[b:], self.n_pend[b:],
                                        self.stream[b], self.stream_len[b:], self.stream_cap, self.ws)
@@ -266,6 +268,36 @@ class Session:
                            None, None, None, 0, self.ws)
         capi.dflash_accept_rollback(self.draft, self.argmax, self.batch, B, self.tcache, self.anchor, self.n_pend,
                                     self.accept_len, self.stream, self.stream_len, self.stream_cap, self.ws)
+        self.steps_done += 1
+
+    def resample_first(self, temperature, v):
+        """Sampling mode after prefill: replace each sequence's first emitted
+        token (the greedy one) by a draw at `temperature` from the last
+        prompt row's logits with the uniform v[batch].  Needs the prefill's
+        last chunk to be its only call with that sequence's last row, i.e. a
+        single sequence (batch 1)."""
+        if self.batch != 1:
+            raise ValueError("resample_first draws from the last prefill call's logits: batch 1 only")
+        n_last = int(self._last_chunk_rows)
+        logits = capi.dflash_workspace_logits(self.ws, n_last, self.m.shape.vocab)[n_last - 1:]
+        vv = torch.as_tensor(np.asarray(v, dtype=np.float32).reshape(1), device=self.m.device)
+        capi.dflash_sample(logits, 1, self.m.shape.vocab, temperature, vv, self.anchor, self.ws)
+        self.stream[:, 0].copy_(self.anchor)
+
+    def step_sampling(self, temperature, w, u, v):
+        """One DFlash step in sampling mode (asynchronous): the drafter samples
+        its block with w [batch][B-1], the target verifies it by speculative
+        sampling with u [batch][B-1] and v [batch] (device float32 uniforms)."""
+        tgt, dr = self.m.structs()
+        B, rows, V = self.block, self.batch * self.block, self.m.shape.vocab
+        capi.dflash_fuse_features(dr, self.hcap, rows, self.fused, self.ws)
+        capi.dflash_inject_kv(dr, self.fused, self.batch, B, self.n_pend, self.dcache, self.ws)
+        capi.dflash_draft_block(dr, tgt, self.anchor, self.batch, B, self.dcache, self.draft, self.ws)
+        capi.dflash_draft_sample(self.batch, B, V, temperature, w, self.draft, self.ws)
+        capi.target_verify(tgt, self.draft, self.batch, B, 0, self.tcache, self.argmax, self.gap, self.hcap, None,
+                           None, None, None, 0, self.ws)
+        capi.dflash_accept_sample(self.draft, self.batch, B, V, temperature, u, v, self.tcache, self.anchor,
+                                  self.n_pend, self.accept_len, self.stream, self.stream_len, self.stream_cap, self.ws)
         self.steps_done += 1
 
     def ar_step(self):

@@ -531,6 +531,186 @@ def spec_decode(tg: Target, dr: Draft, prompt, n_tokens, block, rnd, forcing=Non
 
 
 # ---------------------------------------------------------------------------
+# Tree verification (DDTree)
+# ---------------------------------------------------------------------------
+#
+# "DFlash 深度解析" §8.2: one target forward explores several branches of the
+# drafter's guesses within a node budget, instead of a single chain; the page
+# sketches the idea and prints no algorithm.  The reading taken here:
+#   * candidates: for each drafted slot j = 1..B-1, the drafter's top-K tokens
+#     by log-probability log q_j (softmax of the slot's logits), ranks 0..K-1
+#     (ties to the lower token id);
+#   * the tree: the `budget` highest-scoring token prefixes (c_1..c_d) under the
+#     score sum_j log q_j(c_j) (the drafter predicts its slots in one pass, so
+#     a prefix's probability under it is the product of the slots'
+#     marginals), found best-first; every prefix's parent prefix scores at
+#     least as high, so the set is a tree rooted at the anchor.  Ties between
+#     equal scores go to the smaller depth, then to the smaller rank at that
+#     depth, then to the earlier parent;
+#   * verification: one causal target forward over [anchor, nodes in creation
+#     order] in which node i sits at position P + depth(i) and attends to the
+#     context and to its ancestors (itself included) only;
+#   * acceptance: from the root, move to the child whose token equals the
+#     target's greedy token after the current node, while there is one; the
+#     step emits the tokens of the accepted path and the target's greedy token
+#     after its last node (the bonus), exactly as linear verification does on
+#     a chain.  With K = 1 and budget B-1 the tree is the drafter's greedy chain
+#     and the step is linear verification.
+
+
+@dataclass
+class Tree:
+    tokens: np.ndarray   # [N+1] node 0 = anchor
+    parent: np.ndarray   # [N+1] parent index (-1 for the root)
+    depth: np.ndarray    # [N+1] 0 for the root
+    score: np.ndarray    # [N+1] sum of log q along the path (0 for the root)
+
+
+def log_softmax(logits):
+    z = f64(logits)
+    z = z - np.max(z, axis=-1, keepdims=True)
+    return z - np.log(np.sum(np.exp(z), axis=-1, keepdims=True))
+
+
+def topk_candidates(draft_logits_rows, k):
+    """Per slot row: the k highest log-probabilities and their tokens (ties
+    to the lower token id)."""
+    lp = log_softmax(draft_logits_rows)
+    toks = np.argsort(-lp, axis=-1, kind="stable")[:, :k]
+    return toks.astype(np.int64), np.take_along_axis(lp, toks, axis=-1)
+
+
+def build_tree(anchor, cand_tok, cand_lp, budget):
+    """The `budget` best prefixes, best-first.  cand_tok/cand_lp [B-1, K]
+    sorted by rank.  A frontier entry (score, depth, rank, parent) stands for
+    the prefix parent + candidate `rank` of slot `depth`; taking one adds its
+    next sibling (rank + 1) and its first child (depth + 1, rank 0)."""
+    D, K = cand_tok.shape
+    tokens, parent, depth, score = [int(anchor)], [-1], [0], [0.0]
+    frontier = [(float(cand_lp[0, 0]), 1, 0, 0)] if D >= 1 and K >= 1 else []
+    while frontier and len(tokens) - 1 < budget:
+        best = min(frontier, key=lambda e: (-e[0], e[1], e[2], e[3]))
+        frontier.remove(best)
+        sc, d, r, par = best
+        node = len(tokens)
+        tokens.append(int(cand_tok[d - 1, r]))
+        parent.append(par)
+        depth.append(d)
+        score.append(sc)
+        if r + 1 < K:
+            frontier.append((score[par] + float(cand_lp[d - 1, r + 1]), d, r + 1, par))
+        if d + 1 <= D:
+            frontier.append((sc + float(cand_lp[d, 0]), d + 1, 0, node))
+    return Tree(np.array(tokens, np.int64), np.array(parent, np.int64), np.array(depth, np.int64),
+                np.array(score, np.float64))
+
+
+def tree_ancestors(tree: Tree):
+    """allowed[i, j]: node j is node i or one of its ancestors."""
+    n = len(tree.tokens)
+    allowed = np.zeros((n, n), dtype=bool)
+    for i in range(n):
+        j = i
+        while j >= 0:
+            allowed[i, j] = True
+            j = int(tree.parent[j])
+    return allowed
+
+
+def target_forward_tree(tg: Target, tree: Tree, cache: KV, rnd):
+    """Target forward of the tree's nodes (see above).  Returns argmax, gap,
+    hcap, new keys/values per node row, like ``target_forward``."""
+    sh = tg.shape
+    P = cache.length()
+    tokens = tree.tokens
+    n = len(tokens)
+    allowed_block = tree_ancestors(tree)
+    d, nq, nkv = sh.head_dim, sh.n_q, sh.n_kv
+    pos = P + tree.depth
+    x = f64(tg.embed)[tokens]
+    caps, new_k, new_v = {}, [], []
+    for li, lw in enumerate(tg.layers):
+        h = rnd(rmsnorm(x, lw.attn_norm, sh.eps))
+        q = rnd(rope(linear(h, lw.wq).reshape(n, nq, d), pos, sh.rope_theta))
+        k = rnd(rope(linear(h, lw.wk).reshape(n, nkv, d), pos, sh.rope_theta))
+        v = rnd(linear(h, lw.wv).reshape(n, nkv, d))
+        allowed = np.concatenate([np.ones((n, P), dtype=bool), allowed_block], axis=1)
+        group = nq // nkv
+        o = np.zeros((n, nq, d))
+        for hq in range(nq):
+            hk = hq // group
+            keys = np.concatenate([cache.k[li][hk], k[:, hk]], axis=0)
+            vals = np.concatenate([cache.v[li][hk], v[:, hk]], axis=0)
+            o[:, hq] = attention(q[:, hq], keys, vals, allowed)
+        o = rnd(o.reshape(n, nq * d))
+        x = x + linear(o, lw.wo)
+        h2 = rnd(rmsnorm(x, lw.ffn_norm, sh.eps))
+        a = rnd(silu(linear(h2, lw.w_gate)) * linear(h2, lw.w_up))
+        x = x + linear(a, lw.w_down)
+        new_k.append(k)
+        new_v.append(v)
+        if li in tg.capture:
+            caps[li] = rnd(x)
+    hcap = np.concatenate([caps[i] for i in tg.capture], axis=-1)
+    z = rnd(rmsnorm(x, tg.final_norm, sh.eps))
+    logits = linear(z, tg.lm_head)
+    am, gap = argmax_top2(logits)
+    return TargetOut(am, gap, logits, hcap, new_k, new_v)
+
+
+def accept_tree(tree: Tree, target_argmax):
+    """Walk from the root along the children that match the target's greedy
+    token.  Returns (path node indices, emitted tokens): a = len(path) - 1
+    drafted tokens plus the bonus."""
+    path = [0]
+    while True:
+        x = path[-1]
+        g = int(target_argmax[x])
+        nxt = [c for c in range(len(tree.tokens)) if tree.parent[c] == x and int(tree.tokens[c]) == g]
+        if not nxt:
+            break
+        path.append(nxt[0])
+    emitted = [int(tree.tokens[c]) for c in path[1:]] + [int(target_argmax[path[-1]])]
+    return np.array(path, np.int64), np.array(emitted, np.int64)
+
+
+def spec_decode_tree(tg: Target, dr: Draft, prompt, n_tokens, block, topk, budget, rnd, window=0):
+    """DFlash speculative decoding with tree verification (greedy): per step
+    fuse + inject the pending rows, one drafter forward, the tree of its top-k
+    candidates, one tree-masked target forward, the walk, and the rollback:
+    the accepted path's keys/values are committed at positions P..P+a and its
+    captured rows become the pending rows.  Returns the emitted tokens and the
+    per-step accepted counts."""
+    sh, dsh = tg.shape, dr.shape
+    tcache = KV.empty(sh.n_layers, sh.n_kv, sh.head_dim)
+    dcache = KV.empty(dsh.n_layers, dsh.n_kv, dsh.head_dim)
+    prompt = np.asarray(prompt, dtype=np.int64)
+    out = target_forward(tg, prompt, tcache, rnd, keep_logits=False)
+    commit(tcache, out, len(prompt))
+    pending = out.hcap
+    emitted = [int(out.argmax[-1])]
+    anchor = emitted[0]
+    accepts = []
+    while len(emitted) < n_tokens:
+        P = tcache.length()
+        m = pending.shape[0]
+        fused = fuse_features(dr, pending, rnd)
+        for li, (k, v) in enumerate(inject_kv(dr, fused, np.arange(P - m, P), rnd)):
+            dcache.append(li, k, v)
+        ct, cl = topk_candidates(draft_logits(dr, tg, anchor, block, dcache, rnd, window), topk)
+        tree = build_tree(anchor, ct, cl, budget)
+        out = target_forward_tree(tg, tree, tcache, rnd)
+        path, em = accept_tree(tree, out.argmax)
+        accepts.append(len(path) - 1)
+        emitted.extend(int(t) for t in em)
+        for li in range(len(tcache.k)):
+            tcache.append(li, out.new_k[li][path], out.new_v[li][path])
+        pending = out.hcap[path]
+        anchor = int(em[-1])
+    return np.array(emitted[:n_tokens], dtype=np.int64), accepts
+
+
+# ---------------------------------------------------------------------------
 # Sampling mode (temperature T > 0)
 # ---------------------------------------------------------------------------
 #

@@ -400,6 +400,100 @@ def test_lossless_with_cross_window(tiny):
     assert np.array_equal(out, ref)
 
 
+# ---------------------------------------------------------------- tree verification
+
+
+def _prefix_of(tree, i):
+    out = []
+    while i > 0:
+        out.append(int(tree.tokens[i]))
+        i = int(tree.parent[i])
+    return tuple(reversed(out))
+
+
+@pytest.mark.parametrize("D,K,budget,seed", [(3, 3, 10, 0), (4, 2, 7, 1), (2, 4, 8, 2), (3, 3, 39, 3), (5, 1, 4, 4)])
+def test_tree_is_the_best_prefixes_by_brute_force(D, K, budget, seed):
+    """Enumerate every prefix of the candidate lattice, score it, and take the
+    `budget` best: exactly the tree's nodes."""
+    rng = np.random.default_rng(seed)
+    lp = np.sort(np.log(rng.dirichlet(np.ones(K + 3), size=D)[:, :K]), axis=1)[:, ::-1]
+    toks = rng.permutation(100)[: D * K].reshape(D, K)
+    tree = O.build_tree(99, toks, lp, budget)
+    prefixes = []
+    for d in range(1, D + 1):
+        for ranks in itertools.product(range(K), repeat=d):
+            prefixes.append((sum(lp[j, r] for j, r in enumerate(ranks)), tuple(toks[j, r] for j, r in enumerate(ranks))))
+    prefixes.sort(key=lambda e: -e[0])
+    want = {p for _, p in prefixes[: min(budget, len(prefixes))]}
+    got = {_prefix_of(tree, i) for i in range(1, len(tree.tokens))}
+    assert got == want
+    # a tree: parents come first, depths step by one, scores never increase in creation order
+    for i in range(1, len(tree.tokens)):
+        assert tree.parent[i] < i and tree.depth[i] == tree.depth[tree.parent[i]] + 1
+    assert np.all(np.diff(tree.score[1:]) <= 1e-12)
+
+
+def test_tree_attention_sees_ancestors_only(tiny):
+    wl, tg, dr = _tiny_models(tiny)
+    sh = tg.shape
+    ct = np.array([[10, 11], [12, 13], [14, 15]])
+    cl = np.log(np.array([[0.5, 0.4], [0.6, 0.3], [0.7, 0.2]]))
+    tree = O.build_tree(3, ct, cl, 8)
+    cache = O.KV.empty(sh.n_layers, sh.n_kv, sh.head_dim)
+    base = O.target_forward(tg, synth.prompt_tokens(20, sh.vocab), cache, NONE)
+    O.commit(cache, base, 20)
+    a = O.target_forward_tree(tg, tree, cache, NONE)
+    anc = O.tree_ancestors(tree)
+    for j in range(1, len(tree.tokens)):
+        t2 = O.Tree(tree.tokens.copy(), tree.parent, tree.depth, tree.score)
+        t2.tokens[j] = (t2.tokens[j] + 7) % sh.vocab
+        b = O.target_forward_tree(tg, t2, cache, NONE)
+        for i in range(len(tree.tokens)):
+            same = np.allclose(a.logits[i], b.logits[i], atol=1e-12)
+            assert same == (not anc[i, j]), (i, j)
+    # a node's row equals the causal forward of its own path
+    for i in range(len(tree.tokens)):
+        path = [3] + list(_prefix_of(tree, i))
+        ref = O.target_forward(tg, path, cache, NONE)
+        assert np.allclose(a.logits[i], ref.logits[-1], atol=1e-9)
+
+
+def test_accept_tree_walks_matching_children():
+    tree = O.Tree(np.array([9, 1, 2, 3, 4, 5]), np.array([-1, 0, 0, 1, 3, 2]), np.array([0, 1, 1, 2, 3, 2]),
+                  np.zeros(6))
+    # root -> 2 (node 2) -> 5 (node 5), then node 5's greedy token 8 has no child
+    am = np.array([2, 0, 5, 0, 0, 8])
+    path, em = O.accept_tree(tree, am)
+    assert path.tolist() == [0, 2, 5] and em.tolist() == [2, 5, 8]
+    am = np.array([1, 3, 0, 4, 6, 0])
+    path, em = O.accept_tree(tree, am)
+    assert path.tolist() == [0, 1, 3, 4] and em.tolist() == [1, 3, 4, 6]
+    path, em = O.accept_tree(tree, np.array([7, 0, 0, 0, 0, 0]))
+    assert path.tolist() == [0] and em.tolist() == [7]
+
+
+def test_chain_tree_is_linear_verification(tiny):
+    """K = 1 and a budget of B - 1: the tree is the drafter's greedy chain and
+    the loop is the linear one, step for step."""
+    wl, tg, dr = _tiny_models(tiny)
+    prompt = synth.prompt_tokens(wl.prompt_len, wl.target.vocab)
+    n, B = 30, 6
+    got, acc = O.spec_decode_tree(tg, dr, prompt, n, B, 1, B - 1, NONE)
+    ref, steps = O.spec_decode(tg, dr, prompt, n, B, NONE)
+    assert np.array_equal(got, ref)
+    assert acc == [st.accept for st in steps][: len(acc)]
+
+
+@pytest.mark.parametrize("topk,budget", [(3, 20), (2, 9)])
+def test_lossless_tree_verification(tiny, topk, budget):
+    wl, tg, dr = _tiny_models(tiny)
+    prompt = synth.prompt_tokens(wl.prompt_len, wl.target.vocab)
+    n = 24
+    ref, _ = O.greedy_ar(tg, prompt, n, NONE)
+    got, _ = O.spec_decode_tree(tg, dr, prompt, n, 16, topk, budget, NONE)
+    assert np.array_equal(got, ref)
+
+
 # ---------------------------------------------------------------- sampling mode
 
 
