@@ -51,6 +51,11 @@ struct dflash_workspace {
   float* dlogits;  // the drafter's logits [rows][V] (dflash_draft_block)
   float2* tstats;  // sampling: per-row (max, sum) of the target's logits
   float2* dstats;  // sampling: the same for the drafter's logits
+  int32_t* cand_tok;   // tree: drafter top-K tokens [rows][8]
+  float* cand_lp;      // tree: their log-probabilities [rows][8]
+  int32_t* tree_path;  // tree: accepted path per sequence [rows][64]
+  int32_t* tree_p0;    // tree: length before the rollback [rows]
+  int32_t* tree_a;     // tree: accepted count [rows]
   int32_t vocab;
   AttnScratch as;
   ArgmaxScratch am;
@@ -297,6 +302,11 @@ int dflash_workspace_alloc(const dflash_model_desc* t, const dflash_model_desc* 
       {(void**)&w->dlogits, R * V * 4},
       {(void**)&w->tstats, R * 8},
       {(void**)&w->dstats, R * 8},
+      {(void**)&w->cand_tok, R * 8 * 4},
+      {(void**)&w->cand_lp, R * 8 * 4},
+      {(void**)&w->tree_path, R * 64 * 4},
+      {(void**)&w->tree_p0, R * 4},
+      {(void**)&w->tree_a, R * 4},
 
       {(void**)&w->as.o, R * nq * nchunk * 128 * 4},
       {(void**)&w->as.ml, R * nq * nchunk * 2 * 4},
@@ -467,7 +477,8 @@ static bool cache_matches(const dflash_cache* c, const dflash_model_desc& d, int
 }
 
 static int layer_forward_f32(const dflash_model_desc& d, const dflash_layer_w& w, dflash_cache* c, int layer,
-                             int batch, int n, int causal, int window, dflash_workspace* ws, cudaStream_t s) {
+                             int batch, int n, int causal, int window, const int32_t* rope_off,
+                             const uint64_t* tree_mask, dflash_workspace* ws, cudaStream_t s) {
   const int rows = batch * n, H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads;
   const int qkvw = (nq + 2 * nkv) * hd, dt = d.dtype;
   uint8_t* kc = c->k + (size_t)layer * c->layer_stride * c->elem;
@@ -475,9 +486,9 @@ static int layer_forward_f32(const dflash_model_desc& d, const dflash_layer_w& w
   CK(rmsnorm(dt, ws->x, w.attn_norm, ws->xn, rows, H, d.rms_eps, s));
   CK(gemm_f32(ws->xn, H, rows, w.wqkv, qkvw, H, Epi{EPI_F32, ws->f32buf, qkvw}, s));
   CK(rope_qkv(dt, ws->f32buf, batch, n, nq, nkv, hd, ws->q, kc, vc, c->seq_stride, c->head_stride, c->capacity,
-              c->len, c->rope, ws->status, s));
+              c->len, c->rope, rope_off, ws->status, s));
   CK(attention(dt, ws->q, batch, n, nq, nkv, hd, causal, window, kc, vc, c->seq_stride, c->head_stride, c->capacity,
-               c->attn_gtiles, c->len, nullptr, ws->as, ws->attn, ws->status, s));
+               c->attn_gtiles, c->len, tree_mask, nullptr, ws->as, ws->attn, ws->status, s));
   CK(gemm_f32(ws->attn, nq * hd, rows, w.wo, H, nq * hd, Epi{EPI_RESID, ws->x, H}, s));
   CK(rmsnorm(dt, ws->x, w.ffn_norm, ws->xn, rows, H, d.rms_eps, s));
   CK(gemm_f32(ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, Epi{EPI_SWIGLU, ws->act, d.ffn}, s));
@@ -490,10 +501,13 @@ static int layer_forward_f32(const dflash_model_desc& d, const dflash_layer_w& w
 // attention, O product + residual, RMSNorm, gate/up product + SwiGLU, down
 // product + residual.  Captured states (hcap != null) after the layers in
 // capture[].  window > 0 limits attention to the last `window` cached
-// positions (the drafter's cross-context window).
+// positions (the drafter's cross-context window).  rope_off/tree_mask
+// (nullable, tree verification): row n's RoPE position is len + rope_off[n]
+// and it attends to the context and the block keys its mask selects.
 static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layers, dflash_cache* c, int batch, int n,
-                         int causal, int window, const int32_t* capture, void* hcap, const void* final_norm,
-                         const void* lm_head, float* logits, dflash_workspace* ws, cudaStream_t s) {
+                         int causal, int window, const int32_t* rope_off, const uint64_t* tree_mask,
+                         const int32_t* capture, void* hcap, const void* final_norm, const void* lm_head,
+                         float* logits, dflash_workspace* ws, cudaStream_t s) {
   const int rows = batch * n, H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, L = d.n_layers;
   for (int l = 0; l < L; ++l) {
     const dflash_layer_w& w = layers[l];
@@ -501,7 +515,7 @@ static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layer
   }
   if (d.dtype != DFLASH_BF16) {
     for (int l = 0; l < L; ++l) {
-      int rc = layer_forward_f32(d, layers[l], c, l, batch, n, causal, window, ws, s);
+      int rc = layer_forward_f32(d, layers[l], c, l, batch, n, causal, window, rope_off, tree_mask, ws, s);
       if (rc != DFLASH_OK) return rc;
       if (hcap)
         for (int si = 0; si < 5; ++si)
@@ -517,10 +531,12 @@ static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layer
     uint8_t* kc = c->k + (size_t)l * c->layer_stride * c->elem;
     uint8_t* vc = c->v + (size_t)l * c->layer_stride * c->elem;
     CK(rmsnorm(d.dtype, ws->x, w.attn_norm, ws->xn, rows, H, d.rms_eps, s));
-    CK(gemm_b16(ws->xn, H, rows, w.wqkv, qkvw, H, epi_cache(GE_QKV, ws->q, nq * hd, c, l, nq, n, nullptr), ws, s));
+    GemmEpi qkv = epi_cache(GE_QKV, ws->q, nq * hd, c, l, nq, n, nullptr);
+    qkv.rope_off = rope_off;
+    CK(gemm_b16(ws->xn, H, rows, w.wqkv, qkvw, H, qkv, ws, s));
     const KvMaps maps = kv_maps(c, l);
     CK(attention(d.dtype, ws->q, batch, n, nq, nkv, hd, causal, window, kc, vc, c->seq_stride, c->head_stride, c->capacity,
-                 c->attn_gtiles, c->len, &maps, ws->as, ws->attn, ws->status, s));
+                 c->attn_gtiles, c->len, tree_mask, &maps, ws->as, ws->attn, ws->status, s));
     CK(gemm_b16(ws->attn, nq * hd, rows, w.wo, H, nq * hd, epi_of(GE_RESID, ws->x, H), ws, s));
     CK(rmsnorm(d.dtype, ws->x, w.ffn_norm, ws->xn, rows, H, d.rms_eps, s));
     CK(gemm_b16(ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, epi_of(GE_SWIGLU, ws->act, d.ffn), ws, s));
@@ -555,8 +571,8 @@ int target_verify(const dflash_target* tg, const int32_t* tokens, int32_t batch,
   cudaStream_t s = (cudaStream_t)cuda_stream;
   const int rows = batch * n, H = d.hidden;
   CK(embed(d.dtype, tg->embed, d.vocab, H, tokens, nullptr, 0, batch, n, 0, nullptr, ws->x, ws->status, s));
-  int rc = decoder_stack(d, tg->layers, tc, batch, n, 1, 0, tg->capture, hcap, tg->final_norm, tg->lm_head,
-                         ws->logits, ws, s);
+  int rc = decoder_stack(d, tg->layers, tc, batch, n, 1, 0, nullptr, nullptr, tg->capture, hcap, tg->final_norm,
+                         tg->lm_head, ws->logits, ws, s);
   if (rc != DFLASH_OK) return rc;
   CK(argmax(ws->logits, rows, d.vocab, argmax_out, top2_gap, 0, ws->am, ws->status, s));
   if (commit)
@@ -622,8 +638,8 @@ int dflash_draft_block(const dflash_draft* dr, const dflash_target* tg, const in
   const int rows = batch * block, H = d.hidden;
   CK(embed(d.dtype, tg->embed, d.vocab, H, nullptr, anchor, dr->mask_id, batch, block, 1, draft_tokens, ws->x,
            ws->status, s));
-  int rc = decoder_stack(d, dr->layers, dc, batch, block, 0, dr->cross_ctx, nullptr, nullptr, dr->final_norm,
-                         tg->lm_head, ws->dlogits, ws, s);
+  int rc = decoder_stack(d, dr->layers, dc, batch, block, 0, dr->cross_ctx, nullptr, nullptr, nullptr, nullptr,
+                         dr->final_norm, tg->lm_head, ws->dlogits, ws, s);
   if (rc != DFLASH_OK) return rc;
   CK(argmax(ws->dlogits, rows, d.vocab, draft_tokens, nullptr, block, ws->am, ws->status, s));
   return DFLASH_OK;
@@ -689,6 +705,68 @@ int dflash_sample(const float* logits, int32_t rows, int32_t vocab, float temper
   return DFLASH_OK;
 }
 
+// ------------------------------------------------------------------ tree verification
+static long long tree_capacity(int depth, int k, int limit) {  // number of prefixes, capped
+  long long tot = 0, layer = 1;
+  for (int d = 0; d < depth && tot < limit; ++d) {
+    layer *= k;
+    tot += layer;
+    if (layer > limit) layer = limit;
+  }
+  return tot;
+}
+
+int dflash_draft_tree(const int32_t* anchor, int32_t batch, int32_t block, int32_t vocab, int32_t topk, int32_t budget,
+                      int32_t* tree_tokens, int32_t* tree_parent, int32_t* tree_depth, uint64_t* tree_mask,
+                      dflash_workspace* ws, dflash_stream_t stream) {
+  REQ(anchor && tree_tokens && tree_parent && tree_depth && tree_mask && ws);
+  REQ(batch > 0 && block >= 2 && batch * block <= ws->max_rows && vocab > 1 && vocab <= ws->vocab);
+  REQ(topk >= 1 && topk <= 8 && budget >= 1 && budget <= 63 && tree_capacity(block - 1, topk, 64) >= budget);
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(softmax_stats(ws->dlogits, batch * block, vocab, 1.0f, ws->dstats, s));
+  CK(draft_topk(ws->dlogits, batch, block, vocab, topk, ws->dstats, ws->cand_tok, ws->cand_lp, s));
+  CK(tree_build(ws->cand_tok, ws->cand_lp, anchor, batch, block - 1, topk, budget, tree_tokens, tree_parent,
+                tree_depth, tree_mask, s));
+  return DFLASH_OK;
+}
+
+int target_verify_tree(const dflash_target* tg, const int32_t* tree_tokens, const int32_t* tree_depth,
+                       const uint64_t* tree_mask, int32_t batch, int32_t n, dflash_cache* tc, int32_t* argmax_out,
+                       float* top2_gap, void* hcap, dflash_workspace* ws, dflash_stream_t cuda_stream) {
+  REQ(tg && tree_tokens && tree_depth && tree_mask && argmax_out && ws && desc_ok(&tg->d) && tg->layers &&
+      tg->embed && tg->lm_head && tg->final_norm);
+  const dflash_model_desc& d = tg->d;
+  if (!desc_shapes_ok(&d)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
+  REQ(batch > 0 && n >= 1 && n <= 64 && batch * n <= ws->max_rows);
+  REQ(cache_matches(tc, d, d.n_layers) && batch <= tc->batch && tc->capacity <= ws->max_ctx);
+  for (int i = 0; i < 5; ++i) REQ(tg->capture[i] >= 0 && tg->capture[i] < d.n_layers);
+  cudaStream_t s = (cudaStream_t)cuda_stream;
+  CK(embed(d.dtype, tg->embed, d.vocab, d.hidden, tree_tokens, nullptr, 0, batch, n, 0, nullptr, ws->x, ws->status, s));
+  int rc = decoder_stack(d, tg->layers, tc, batch, n, 0, 0, tree_depth, tree_mask, tg->capture, hcap, tg->final_norm,
+                         tg->lm_head, ws->logits, ws, s);
+  if (rc != DFLASH_OK) return rc;
+  CK(argmax(ws->logits, batch * n, d.vocab, argmax_out, top2_gap, 0, ws->am, ws->status, s));
+  return DFLASH_OK;
+}
+
+int dflash_accept_tree(const dflash_target* tg, const int32_t* tree_tokens, const int32_t* tree_parent,
+                       const int32_t* argmax_in, int32_t batch, int32_t n, dflash_cache* tc, void* hcap,
+                       int32_t* anchor, int32_t* n_pend, int32_t* accept_len, int32_t* stream, int32_t* stream_len,
+                       int32_t stream_cap, dflash_workspace* ws, dflash_stream_t cuda_stream) {
+  REQ(tg && tree_tokens && tree_parent && argmax_in && tc && anchor && n_pend && ws && desc_ok(&tg->d));
+  REQ(batch > 0 && batch <= tc->batch && n >= 1 && n <= 64 && batch * n <= ws->max_rows);
+  REQ(cache_matches(tc, tg->d, tg->d.n_layers));
+  REQ(!stream || (stream_len && stream_cap > 0));
+  cudaStream_t s = (cudaStream_t)cuda_stream;
+  CK(accept_tree(tree_tokens, tree_parent, argmax_in, batch, n, tc->len, anchor, n_pend, accept_len, stream,
+                 stream_len, stream_cap, ws->tree_path, ws->tree_p0, ws->tree_a, ws->status, s));
+  CK(compact_kv(tc->dtype, tc->k, tc->v, tc->n_layers, batch, tc->n_kv, tc->layer_stride, tc->seq_stride,
+                tc->head_stride, tc->head_dim, tc->capacity, ws->tree_path, ws->tree_p0, ws->tree_a, s));
+  if (hcap)
+    CK(compact_rows(tg->d.dtype, hcap, (size_t)5 * tg->d.hidden, batch, n, ws->tree_path, ws->tree_a, s));
+  return DFLASH_OK;
+}
+
 // ------------------------------------------------------------------ building blocks
 int dflash_linear(int32_t dtype, const void* x, const void* w, float* y, int32_t rows, int32_t M, int32_t K,
                   dflash_workspace* ws, dflash_stream_t stream) {
@@ -731,7 +809,7 @@ int dflash_attention(const dflash_model_desc* d, const void* q, int32_t batch, i
   const uint8_t* vc = c->v + (size_t)layer * c->layer_stride * c->elem;
   const KvMaps maps = kv_maps(c, layer);
   CK(attention(d->dtype, q, batch, n, d->n_q_heads, d->n_kv_heads, d->head_dim, causal ? 1 : 0, window, kc, vc,
-               c->seq_stride, c->head_stride, c->capacity, c->attn_gtiles, c->len, c->has_maps ? &maps : nullptr, ws->as, out,
+               c->seq_stride, c->head_stride, c->capacity, c->attn_gtiles, c->len, nullptr, c->has_maps ? &maps : nullptr, ws->as, out,
                ws->status, (cudaStream_t)stream));
   return DFLASH_OK;
 }

@@ -29,7 +29,8 @@ __global__ void __launch_bounds__(NT)
     attn_f32_kernel(const float* __restrict__ q, int n, int nq, int nkv, int hd, int causal,
                     const float* __restrict__ kc, const float* __restrict__ vc, size_t seq_stride,
                     size_t head_stride, int capacity, int window, const int32_t* __restrict__ len,
-                    float* __restrict__ part_o, float* __restrict__ part_ml, int nchunk, float scale_log2) {
+                    const uint64_t* __restrict__ tree_mask, float* __restrict__ part_o, float* __restrict__ part_ml,
+                    int nchunk, float scale_log2) {
   __shared__ float qs[kHD];
   __shared__ float sc[kAttnChunk];
   __shared__ float red[NT / 32];
@@ -48,12 +49,15 @@ __global__ void __launch_bounds__(NT)
   const float* vbase = vc + (size_t)b * seq_stride + (size_t)hk * head_stride;
   for (int i = threadIdx.x; i < hd; i += NT) qs[i] = q[((size_t)r * nq + hq) * hd + i];
   __syncthreads();
+  // tree verification: block key P + i is visible only when bit i is set (the node's ancestors)
+  const uint64_t tm = tree_mask ? tree_mask[r] : ~0ull;
   float mx = -INFINITY;
   for (int key = kb + threadIdx.x; key < ke; key += NT) {
     const float* kr = kbase + (size_t)key * hd;
     float acc = 0.f;
     for (int i = 0; i < hd; ++i) acc = fmaf(qs[i], kr[i], acc);
     acc *= scale_log2;
+    if (key >= P && !((tm >> (key - P)) & 1ull)) acc = -INFINITY;
     sc[key - kb] = acc;
     mx = fmaxf(mx, acc);
   }
@@ -65,7 +69,7 @@ __global__ void __launch_bounds__(NT)
   for (int i = 1; i < NT / 32; ++i) m = fmaxf(m, red[i]);
   float ls = 0.f;
   for (int key = kb + threadIdx.x; key < ke; key += NT) {
-    const float p = exp2f(sc[key - kb] - m);
+    const float p = sc[key - kb] == -INFINITY ? 0.f : exp2f(sc[key - kb] - m);  // 0 for masked keys
     sc[key - kb] = p;
     ls += p;
   }
@@ -251,9 +255,10 @@ bool make_q_map(const void* q, int rows, int nq, int G, CUtensorMap* out) {
 
 cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nkv, int hd, int causal, int window,
                       const void* kc, const void* vc, size_t seq_stride, size_t head_stride, int capacity, int gtiles,
-                      const int32_t* len, const KvMaps* maps, const AttnScratch& sc, void* out, int* status,
-                      cudaStream_t s) {
+                      const int32_t* len, const uint64_t* tree_mask, const KvMaps* maps, const AttnScratch& sc,
+                      void* out, int* status, cudaStream_t s) {
   if (batch * n <= 0) return cudaSuccess;
+  if (tree_mask && (causal || n > 64)) return cudaErrorInvalidValue;  // tree rows: non-causal, at most 64 nodes
   const int nchunk_launch = (capacity + kAttnChunk - 1) / kAttnChunk;
   if (nchunk_launch > sc.nchunk || nchunk_launch > kCombineMaxChunks || hd > kHD) return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
@@ -262,15 +267,15 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
     const int G = nq / nkv;
     CUtensorMap qmap;
     if (!make_q_map(q, batch * n, nq, G, &qmap)) return cudaErrorInvalidValue;
-    DFL_RET(attention_fa(G, *maps, qmap, batch, n, nq, nkv, causal, window, capacity, gtiles, len, sc, scale_log2,
-                         status, s));
+    DFL_RET(attention_fa(G, *maps, qmap, batch, n, nq, nkv, causal, window, capacity, gtiles, len, tree_mask, sc,
+                         scale_log2, status, s));
     DFL_RET(launch_pdl(attn_combine_kernel<bf16>, dim3(batch * n, nq), dim3(kCombineGroups * 64), 0, s, sc.o,
                        sc.ml, n, nq, hd, causal, capacity, window, gtiles * 128, len, sc.nchunk, (bf16*)out));
   } else {
     const dim3 grid(nchunk_launch, nq, batch * n);
     DFL_RET(launch_pdl(attn_f32_kernel<128>, grid, dim3(128), 0, s, (const float*)q, n, nq, nkv, hd, causal,
-                       (const float*)kc, (const float*)vc, seq_stride, head_stride, capacity, window, len, sc.o,
-                       sc.ml, sc.nchunk, scale_log2));
+                       (const float*)kc, (const float*)vc, seq_stride, head_stride, capacity, window, len, tree_mask,
+                       sc.o, sc.ml, sc.nchunk, scale_log2));
     DFL_RET(launch_pdl(attn_combine_kernel<float>, dim3(batch * n, nq), dim3(kCombineGroups * 64), 0, s, sc.o,
                        sc.ml, n, nq, hd, causal, capacity, window, kAttnChunk, len, sc.nchunk, (float*)out));
   }

@@ -4,35 +4,35 @@
 // Work unit (one CTA): KV head hk, 16-row block rb of sequence b, key group gi
 // = `gtiles` consecutive 128-key tiles at absolute positions
 // [gi * gtiles * 128, (gi + 1) * gtiles * 128).  The group size is a property
-// of the cache (fixed when it is allocated), so the reduction below depends
+// of the cache (fixed when it is allocated), so the arithmetic below depends
 // only on absolute positions: a row's result is the same whether it is
 // computed alone or in a block, and in any batch.
 //
 // The G query heads that share the KV head are stacked into one M = 128 tile
 // (row r = block row r / G, head r % G; rows past 16 G are padding), so one
-// tcgen05.mma serves the whole GQA group.  Per tile t of the unit:
-//   S_t = Q K_t^T (tensor cores, fp32 in TMEM, double-buffered)
-//   m_t = max of the row's visible scores (log2 units), p = 2^(s - m_t),
-//         0 for keys outside the row's visible range [lo, lim)
-//   P_t = p as a bf16 hi/lo pair written over S_t in TMEM (p = hi + lo to
-//         about 2^-17), O_t = P_hi V_t + P_lo V_t (tensor cores, A operand
-//         from TMEM, double-buffered O)
-//   fold (in registers, tiles in order; tiles with no visible key skipped):
-//         M' = max(M, m_t), a = 2^(M - M'), c = 2^(m_t - M'),
-//         O = O a + O_t c, L = L a + l_t c  (l_t: sum of p, per half-row)
+// tcgen05.mma serves the whole GQA group.  Per tile t of the unit, per row:
+//   S_t = Q K_t^T                         tensor cores, fp32 in TMEM (two buffers)
+//   reference max M: set by the first tile with a visible key, raised to a
+//     later tile's max only when that exceeds M by more than 8 (log2 units);
+//     when it is raised, O and the row sum L are rescaled by 2^(M_old - M_new)
+//   p = 2^(s - M) for visible keys (<= 2^8), else 0; L += sum of p
+//   P_t = p as a bf16 hi/lo pair (p = hi + lo to about 2^-17 relative)
+//         written over S_t in TMEM
+//   O += P_hi V_t + P_lo V_t              tensor cores, A operand from TMEM,
+//                                         O accumulated in TMEM over the unit
 // and the unit writes one partial (M, L, O) per (row, head); the combine
-// kernel merges the groups of a row in group order.
+// kernel merges the groups of a row in group order.  The decisions (when M
+// moves) are row-local, so they too depend only on the row's keys.
 //
 // Roles (320 threads): warp 0 lane 0 streams Q and the K/V tiles through a
-// 3-stage TMA ring; warp 1 owns TMEM and its lane 0 issues the products
-// (QK^T of tile t+1 is issued while tile t's P is computed); warps 2..9 each
-// own TMEM lane quarter (warp & 3) and one half of the key columns
-// ((warp - 2) >> 2): they compute P for their half and fold their half of O.
-// The row max needs all 128 scores: each thread also reads the other half's
-// scores from TMEM for the max alone, so the two halves never synchronise.
-// Every wait is bounded; a wait that gives up sets DFLASH_STATUS_TIMEOUT,
-// the unit writes nothing, and the CTA drains its copies and products before
-// releasing TMEM.
+// TMA ring; warp 1 owns TMEM and its lane 0 issues the products (QK^T of tile
+// t while P_{t-1} is being computed, PV of tile t-1 as soon as its P is in
+// TMEM); warps 2..9 each own TMEM lane quarter (warp & 3) and one half of the
+// key columns ((warp - 2) >> 2).  Each half writes P only over its own 64
+// score columns; the two halves of a row exchange their maxima through
+// shared memory on an mbarrier.  Every wait is bounded; a wait that gives up
+// sets DFLASH_STATUS_TIMEOUT, the unit writes nothing, and the CTA drains its
+// copies and products before releasing TMEM.
 #include <algorithm>
 
 #include "common.cuh"
@@ -125,7 +125,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     attn_fa_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, int batch, int n, int nq, int nkv, int causal, int window,
                    long long row0, int capacity, int gtiles, int ngroups, const int32_t* __restrict__ len,
-                   float* __restrict__ part_o, float* __restrict__ part_ml, float scale_log2, int* status) {
+                   const uint64_t* __restrict__ tree_mask, float* __restrict__ part_o, float* __restrict__ part_ml,
+                   float scale_log2, int* status) {
   using Ly = FaLayout<G>;
   constexpr int kStages = Ly::kStages;
   constexpr uint32_t kQ = Ly::kQ;
@@ -138,11 +139,10 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   uint64_t* q_full = bar + 6;
   uint64_t* s_full = bar + 7;     // [2] S_t in TMEM
   uint64_t* p_full = bar + 9;     // [2] P_t in TMEM (one arrival per softmax warp)
-  uint64_t* o_full = bar + 11;    // [2] O_t in TMEM
-  uint64_t* o_free = bar + 13;    // [2] O_t read out (one arrival per softmax warp)
-  uint64_t* drain = bar + 15;     // every issued product completed
-  uint64_t* xch_full = bar + 16;  // [2] both halves' maxima written (one arrival per softmax thread)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 18);
+  uint64_t* pv_done = bar + 11;   // [2] O += P_t V_t completed
+  uint64_t* drain = bar + 13;     // every issued product completed
+  uint64_t* xch_full = bar + 14;  // [2] both halves' maxima written (one arrival per softmax warp)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
   volatile int* abort_f = reinterpret_cast<volatile int*>(tslot + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {  // the descriptors are kernel parameters: fetch them while the previous kernel drains
@@ -180,11 +180,10 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 8);
-      mbar_init(&o_full[i], 1);
-      mbar_init(&o_free[i], 8);
+      mbar_init(&pv_done[i], 1);
+      mbar_init(&xch_full[i], 8);
     }
     mbar_init(drain, 1);
-    for (int i = 0; i < 2; ++i) mbar_init(&xch_full[i], 256);
     *abort_f = 0;
     fence_barrier_init();
   }
@@ -233,7 +232,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         if (t < nt) {  // S_t = Q K_t^T into S[t & 1], once P_{t-2} (same buffer) has been consumed
           const int s = t % kStages, sb = t & 1;
           ok = mbar_wait(&kv_full[s], (uint32_t)(t / kStages) & 1u, kFaWaitNs);
-          if (ok && t >= 2) ok = mbar_wait(&o_full[sb], (uint32_t)((t - 2) >> 1) & 1u, kFaWaitNs);
+          if (ok && t >= 2) ok = mbar_wait(&pv_done[sb], (uint32_t)((t - 2) >> 1) & 1u, kFaWaitNs);
           if (!ok || *abort_f) break;
           tc_fence_after();
           const uint8_t* kt = sm + s * kStageBytes;
@@ -246,10 +245,9 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           }
           tc_commit(&s_full[sb]);
         }
-        if (t >= 1) {  // O_{t-1} = P_hi V + P_lo V into O[(t-1) & 1], once O_{t-3} has been read out
+        if (t >= 1) {  // O += P_hi V + P_lo V for tile t-1 (P of key half j at columns 64 j: hi, then lo)
           const int w = t - 1, wb = w & 1, s = w % kStages;
           ok = mbar_wait(&p_full[wb], (uint32_t)(w >> 1) & 1u, kFaWaitNs);
-          if (ok && w >= 2) ok = mbar_wait(&o_free[wb], (uint32_t)((w - 2) >> 1) & 1u, kFaWaitNs);
           if (!ok || *abort_f) break;
           tc_fence_after();
           const uint32_t vt = smem_u32(sm + s * kStageBytes + kTileBytes);
@@ -257,9 +255,9 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           for (int pass = 0; pass < 2; ++pass)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              tc_mma_f16_tmem_a(tmem + 256 + wb * 128, tmem + wb * 128 + (kk >> 2) * 64 + pass * 32 + (kk & 3) * 8,
-                                smem_desc_mn(vt + kk * 2048, 16384), idO, (pass | kk) != 0 ? 1u : 0u);
-          tc_commit(&o_full[wb]);
+              tc_mma_f16_tmem_a(tmem + 256, tmem + wb * 128 + (kk >> 2) * 64 + pass * 32 + (kk & 3) * 8,
+                                smem_desc_mn(vt + kk * 2048, 16384), idO, (w | pass | kk) != 0 ? 1u : 0u);
+          tc_commit(&pv_done[wb]);
           tc_commit(&kv_empty[s]);
         }
       }
@@ -271,7 +269,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax + fold
+    // ------------------------------------------------------------ softmax
     const int q4 = warp & 3, h = (warp - 2) >> 2;
     const int r = q4 * 32 + lane;
     const int ri = r / G;
@@ -279,130 +277,96 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     const bool live = q4 * 32 < 16 * G;  // warp-uniform: the quarter holds real rows
     const bool row_ok = r < 16 * G && qi < n;
     const int lim = row_ok ? min(causal ? P + qi + 1 : P + n, capacity) : 0;  // visible keys [lo, lim)
+    // tree verification: block key P + i is visible only when bit i is set (the node's ancestors)
+    const uint64_t tm = (tree_mask && row_ok) ? tree_mask[(size_t)b * n + qi] : ~0ull;
     const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
-    float acc[64];
-#pragma unroll
-    for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+    const uint32_t obase = tmem + lrow + 256 + h * 64;  // this half's 64 output columns
     float M = -INFINITY, Lh = 0.f;
-    float m_prev = -INFINITY, l_prev = 0.f;
     bool ok = true;
-    for (int t = 0; t <= nt; ++t) {
-      float m_cur = -INFINITY, l_cur = 0.f;
-      if (t < nt) {
-        const int sb = t & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (uint32_t)(t >> 1) & 1u, kFaWaitNs));
-        if (__any_sync(0xffffffffu, !ok || *abort_f)) break;  // warp-uniform
-        tc_fence_after();
-        const int k0 = (ta + t) * 128 + h * 64;            // this half's first key
-        const uint32_t sbase = tmem + lrow + sb * 128 + h * 64;  // this half's 64 score columns
-        float lm = -INFINITY;
-        if (live) {  // this half's maximum over its visible scores
-#pragma unroll 1
-          for (int c2 = 0; c2 < 2; ++c2) {
-            uint32_t v[32];
-            tmem_ld32(sbase + c2 * 32, v);
-            tmem_ld_wait();
+    for (int t = 0; t < nt; ++t) {
+      const int sb = t & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (uint32_t)(t >> 1) & 1u, kFaWaitNs));
+      if (__any_sync(0xffffffffu, !ok || *abort_f)) break;  // warp-uniform
+      tc_fence_after();
+      const int k0 = (ta + t) * 128 + h * 64;                // this half's first key
+      const uint32_t sbase = tmem + lrow + sb * 128 + h * 64;  // this half's 64 score columns
+      uint32_t v[64];
+      float lm = -INFINITY;
+      if (live) {  // this half's scores and their maximum over the visible keys
+        tmem_ld32(sbase, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(sbase + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int k = k0 + c2 * 32 + e;
-              if (k >= lo && k < lim) lm = fmaxf(lm, __uint_as_float(v[e]));
-            }
-          }
-          xch[(sb * 2 + h) * 128 + r] = lm;
+        for (int e = 0; e < 64; ++e) {
+          const int k = k0 + e;
+          if (k >= lo && k < lim && (k < P || ((tm >> (k - P)) & 1ull))) lm = fmaxf(lm, __uint_as_float(v[e]));
         }
-        mbar_arrive(&xch_full[sb]);
-        ok = __all_sync(0xffffffffu, mbar_wait(&xch_full[sb], (uint32_t)(t >> 1) & 1u, kFaWaitNs));
-        if (__any_sync(0xffffffffu, !ok || *abort_f)) break;  // warp-uniform
-        if (live) {
-          // the tile max in log2 units (scale > 0: max(s) * scale = max(s * scale))
-          const float mraw = fmaxf(lm, xch[(sb * 2 + (1 - h)) * 128 + r]);
-          m_cur = mraw * scale_log2;
-          const float negm = mraw == -INFINITY ? 0.f : -m_cur;
-          // P of this half as bf16 hi/lo pairs written over its own score
-          // columns only: hi at +0..31, lo at +32..63.  Keys 0..31 of the half
-          // are read first; their lo pairs wait in registers until keys 32..63
-          // (whose scores the lo pairs overwrite) have been read too.
-          uint32_t hiA[16], loA[16];
-          {
-            uint32_t v[32];
-            tmem_ld32(sbase, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int k = k0 + 2 * e;
-              const float p0 = (k >= lo && k < lim) ? ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm)) : 0.f;
-              const float p1 =
-                  (k + 1 >= lo && k + 1 < lim) ? ex2f(fmaf(__uint_as_float(v[2 * e + 1]), scale_log2, negm)) : 0.f;
-              l_cur += p0;
-              l_cur += p1;
-              pack_bf16_hilo(p0, p1, hiA[e], loA[e]);
-            }
-          }
-          tmem_st16(sbase, hiA);
-          {
-            uint32_t v[32], hiB[16], loB[16];
-            tmem_ld32(sbase + 32, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int k = k0 + 32 + 2 * e;
-              const float p0 = (k >= lo && k < lim) ? ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm)) : 0.f;
-              const float p1 =
-                  (k + 1 >= lo && k + 1 < lim) ? ex2f(fmaf(__uint_as_float(v[2 * e + 1]), scale_log2, negm)) : 0.f;
-              l_cur += p0;
-              l_cur += p1;
-              pack_bf16_hilo(p0, p1, hiB[e], loB[e]);
-            }
-            tmem_st16(sbase + 16, hiB);
-            tmem_st16(sbase + 32, loA);
-            tmem_st16(sbase + 48, loB);
-          }
-          tmem_st_wait();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[sb]);
+        xch[(sb * 2 + h) * 128 + r] = lm;
       }
-      if (t >= 1) {  // fold O_{t-1}
-        const int w = t - 1, wb = w & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(&o_full[wb], (uint32_t)(w >> 1) & 1u, kFaWaitNs));
-        if (__any_sync(0xffffffffu, !ok || *abort_f)) break;  // warp-uniform
-        tc_fence_after();
-        // fold factors of this row (tiles with no visible key are skipped)
-        const bool fold = m_prev != -INFINITY;
-        const float Mn = fmaxf(M, m_prev);
-        const float fa = (M == -INFINITY || !fold) ? 0.f : ex2f(M - Mn);
-        const float fc = fold ? ex2f(m_prev - Mn) : 0.f;
-        if (live) {
-          const uint32_t obase = tmem + lrow + 256 + wb * 128 + h * 64;
-#pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            uint32_t o[32];
-            tmem_ld32(obase + c2 * 32, o);
-            tmem_ld_wait();
-            if (c2 == 1) {  // O_{t-1} fully read: release its buffer
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&o_free[wb]);
-            }
-            if (fold) {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) acc[c2 * 32 + e] = fmaf(__uint_as_float(o[e]), fc, acc[c2 * 32 + e] * fa);
-            }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xch_full[sb]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&xch_full[sb], (uint32_t)(t >> 1) & 1u, kFaWaitNs));
+      if (__any_sync(0xffffffffu, !ok || *abort_f)) break;
+      float Mn = M;
+      bool resc = false;
+      if (live) {
+        const float mraw = fmaxf(lm, xch[(sb * 2 + (1 - h)) * 128 + r]);
+        if (mraw != -INFINITY) {
+          const float mt = mraw * scale_log2;  // scale > 0: max(s) * scale = max(s * scale)
+          if (M == -INFINITY) {
+            Mn = mt;
+          } else if (mt > M + 8.f) {
+            Mn = mt;
+            resc = true;
           }
-        } else {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&o_free[wb]);
         }
-        if (fold) {
-          Lh = fmaf(l_prev, fc, Lh * fa);
-          M = Mn;
+        const float negm = Mn == -INFINITY ? 0.f : -Mn;
+        float lt = 0.f;
+        uint32_t hi[32], lo_[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int k = k0 + 2 * e;
+          const float p0 = (k >= lo && k < lim && (k < P || ((tm >> (k - P)) & 1ull)))
+                               ? ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm)) : 0.f;
+          const float p1 = (k + 1 >= lo && k + 1 < lim && (k + 1 < P || ((tm >> (k + 1 - P)) & 1ull)))
+                               ? ex2f(fmaf(__uint_as_float(v[2 * e + 1]), scale_log2, negm)) : 0.f;
+          lt += p0;
+          lt += p1;
+          pack_bf16_hilo(p0, p1, hi[e], lo_[e]);
         }
+        // every score of this half is in registers: P overwrites them (hi at +0..31, lo at +32..63)
+        tmem_st16(sbase, *reinterpret_cast<const uint32_t(*)[16]>(&hi[0]));
+        tmem_st16(sbase + 16, *reinterpret_cast<const uint32_t(*)[16]>(&hi[16]));
+        tmem_st16(sbase + 32, *reinterpret_cast<const uint32_t(*)[16]>(&lo_[0]));
+        tmem_st16(sbase + 48, *reinterpret_cast<const uint32_t(*)[16]>(&lo_[16]));
+        const float f = resc ? ex2f(M - Mn) : 1.f;
+        Lh = fmaf(Lh, f, lt);
+        // a raised reference max rescales O once the products of the earlier tiles are done
+        if (__any_sync(0xffffffffu, resc)) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, kFaWaitNs));
+          if (ok) {
+            tc_fence_after();
+            uint32_t o[64];
+            tmem_ld32(obase, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+            tmem_ld32(obase + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 64; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_st16(obase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&o[c * 16]));
+          }
+        }
+        tmem_st_wait();
+        M = Mn;
       }
-      m_prev = m_cur;
-      l_prev = l_cur;
+      if (__any_sync(0xffffffffu, !ok)) break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[sb]);
     }
+    // the last product of the unit completes before O is read
+    if (ok && !*abort_f)
+      ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(nt - 1) & 1], (uint32_t)((nt - 1) >> 1) & 1u, kFaWaitNs));
     if (!ok) {
       *abort_f = 1;
       set_status(status, DFLASH_STATUS_TIMEOUT);
@@ -417,11 +381,16 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     float* stg_m = stg_l + 256;
     const bool good = !*abort_f;
     if (good && live) {
+      tc_fence_after();
+      uint32_t o[64];
+      tmem_ld32(obase, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+      tmem_ld32(obase + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+      tmem_ld_wait();
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const int ch = h * 16 + c;
-        *reinterpret_cast<float4*>(stg + r * 128 + ((ch ^ (r & 7)) << 2)) =
-            make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+        *reinterpret_cast<uint4*>(stg + r * 128 + ((ch ^ (r & 7)) << 2)) =
+            make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
       }
       stg_l[2 * r + h] = Lh;
       if (h == 0) stg_m[r] = M;
@@ -462,8 +431,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 }
 
 cudaError_t attention_fa(int G, const KvMaps& maps, const CUtensorMap& qmap, int batch, int n, int nq, int nkv,
-                         int causal, int window, int capacity, int gtiles, const int32_t* len, const AttnScratch& sc,
-                         float scale_log2, int* status, cudaStream_t s) {
+                         int causal, int window, int capacity, int gtiles, const int32_t* len, const uint64_t* tree_mask,
+                         const AttnScratch& sc, float scale_log2, int* status, cudaStream_t s) {
   if (gtiles < 2 || batch > kMaxRows) return cudaErrorInvalidValue;
   const int ngroups = (capacity + gtiles * 128 - 1) / (gtiles * 128);
   if (ngroups > sc.nchunk) return cudaErrorInvalidValue;  // partial slots per (row, head)
@@ -480,7 +449,8 @@ cudaError_t attention_fa(int G, const KvMaps& maps, const CUtensorMap& qmap, int
     }                                                                                                            \
     DFL_RET(launch_pdl(attn_fa_kernel<GG>, dim3((unsigned)units), dim3(kFaThreads), FaLayout<GG>::kSmem, s,       \
                        maps.k, maps.v,                                                                             \
-                       qmap, batch, n, nq, nkv, causal, window, maps.row0, capacity, gtiles, sc.nchunk, len, sc.o, \
+                       qmap, batch, n, nq, nkv, causal, window, maps.row0, capacity, gtiles, sc.nchunk, len,       \
+                       tree_mask, sc.o,                                                                            \
                        sc.ml, scale_log2, status));                                                              \
     return cudaSuccess;                                                                                          \
   }

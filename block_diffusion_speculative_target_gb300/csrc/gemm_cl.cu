@@ -168,9 +168,10 @@ __device__ __forceinline__ void gemm_epi(const GemmEpi& e, int n, int m, float v
       const int b = n / e.rows_per_seq, jj = n % e.rows_per_seq;
       if (e.kind == GE_INJECT && jj >= e.n_pend[b]) break;
       const int pos = e.len[b] + jj;
+      const int rpos = e.rope_off ? e.len[b] + e.rope_off[n] : pos;  // RoPE position (a tree node's depth)
       float r = v;
       if (kind != 2) {
-        const float2 cs = pos < e.capacity ? e.rope[(size_t)pos * 64 + (ml & 63)] : make_float2(1.f, 0.f);
+        const float2 cs = (rpos >= 0 && rpos < e.capacity) ? e.rope[(size_t)rpos * 64 + (ml & 63)] : make_float2(1.f, 0.f);
         r = ml < 64 ? v * cs.x - partner * cs.y : v * cs.x + partner * cs.y;
       }
       if (kind == 0) {
@@ -287,8 +288,10 @@ __global__ void __launch_bounds__(128)
         const int b = n / epi.rows_per_seq, jj = n % epi.rows_per_seq;
         const bool skip = epi.kind == GE_INJECT && jj >= epi.n_pend[b];
         const int pos = epi.len[b] + jj;
+        const int rpos = epi.rope_off ? epi.len[b] + epi.rope_off[n] : pos;
         if (gt == 0) pre_pos[j] = skip ? -1 : pos;
-        pre_cs[j * 64 + gt] = pos < epi.capacity ? epi.rope[(size_t)pos * 64 + gt] : make_float2(1.f, 0.f);
+        pre_cs[j * 64 + gt] =
+            (rpos >= 0 && rpos < epi.capacity) ? epi.rope[(size_t)rpos * 64 + gt] : make_float2(1.f, 0.f);
       }
     }
   } else if (warp == 1) {

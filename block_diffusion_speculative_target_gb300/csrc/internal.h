@@ -50,6 +50,7 @@ struct GemmEpi {
   const int32_t* len;
   const float2* rope;      // [capacity][64] cos, sin
   const int32_t* n_pend;   // GE_INJECT
+  const int32_t* rope_off; // GE_QKV, nullable: row n's RoPE position is len[b] + rope_off[n] (tree nodes)
   void* kc;
   void* vc;
   size_t layer_stride, seq_stride, head_stride;
@@ -114,9 +115,10 @@ cudaError_t embed(int dtype, const void* E, int V, int H, const int32_t* tokens,
                   int mask_id, int batch, int n, int mode, int32_t* draft_out, float* x, int* status,
                   cudaStream_t s);
 // RoPE on the q and k parts of qkv (f32 [rows][(nq+2nkv)hd]); q -> qout (T), k/v -> cache at len[b]+j.
+// rope_off (nullable): row r's RoPE position is len[b] + rope_off[r] instead of len[b] + j (tree nodes).
 cudaError_t rope_qkv(int dtype, const float* qkv, int batch, int n, int nq, int nkv, int hd, void* qout,
                      void* kc, void* vc, size_t seq_stride, size_t head_stride, int capacity,
-                     const int32_t* len, const float2* rope_tab, int* status, cudaStream_t s);
+                     const int32_t* len, const float2* rope_tab, const int32_t* rope_off, int* status, cudaStream_t s);
 // Inject: kv f32 [batch*rps][Ld][2][nkv][hd] -> drafter caches (layer stride given) at len[b]+j, j < n_pend[b].
 cudaError_t inject_write(int dtype, const float* kv, int batch, int rps, int Ld, int nkv, int hd, void* kc,
                          void* vc, size_t layer_stride, size_t seq_stride, size_t head_stride, int capacity,
@@ -139,10 +141,12 @@ struct KvMaps {
 bool make_kv_maps(const void* k, const void* v, long long rows_total, CUtensorMap* mk, CUtensorMap* mv);
 // window > 0: keys below len[b] - window (a cross-context window) are not attended.
 // gtiles: 128-key tiles per partial of the bf16 path (a property of the cache).
+// tree_mask (nullable, non-causal calls with n <= 64): row b*n+j sees the
+// context and block key len[b] + i only when bit i of tree_mask[b*n+j] is set.
 cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nkv, int hd, int causal, int window,
                       const void* kc, const void* vc, size_t seq_stride, size_t head_stride, int capacity, int gtiles,
-                      const int32_t* len, const KvMaps* maps, const AttnScratch& sc, void* out, int* status,
-                      cudaStream_t s);
+                      const int32_t* len, const uint64_t* tree_mask, const KvMaps* maps, const AttnScratch& sc,
+                      void* out, int* status, cudaStream_t s);
 // The tiles per partial for a cache of `capacity` positions and nkv heads:
 // about one unit per SM for one sequence at full capacity, a power of two in
 // [2, 64]; depends on nothing else, so results do not depend on the batch.
@@ -155,8 +159,9 @@ bool make_q_map(const void* q, int rows, int nq, int G, CUtensorMap* out);
 // The bf16 attention kernel on tcgen05 (head_dim 128, G in {1, 2, 4, 5, 8}):
 // one partial (max, sum, unnormalised output) per (row, head, tile group).
 cudaError_t attention_fa(int G, const KvMaps& maps, const CUtensorMap& qmap, int batch, int n, int nq, int nkv,
-                         int causal, int window, int capacity, int gtiles, const int32_t* len, const AttnScratch& sc,
-                         float scale_log2, int* status, cudaStream_t s);
+                         int causal, int window, int capacity, int gtiles, const int32_t* len,
+                         const uint64_t* tree_mask, const AttnScratch& sc, float scale_log2, int* status,
+                         cudaStream_t s);
 
 // Greedy token and top-2 gap per row.  If skip_first_of (>0), rows with
 // (r % skip_first_of) == 0 are not written to argmax_out.
@@ -182,6 +187,24 @@ cudaError_t accept_sample(const int32_t* draft, const float* zt, const float* zd
                           int batch, int block, int V, float temperature, const float* u, const float* v, int32_t* len,
                           int32_t* anchor, int32_t* n_pend, int32_t* accept_len, int32_t* stream, int32_t* stream_len,
                           int stream_cap, int* status, cudaStream_t s);
+
+// Tree verification: the drafter's top-K per slot (rows r % block == 0 skipped),
+// the best-first tree per sequence, the greedy walk + rollback (records the
+// path, the old length and the accepted count), and the compaction of the
+// path's keys/values (all layers) and captured rows.  Trees hold <= 64 nodes.
+cudaError_t draft_topk(const float* logits, int batch, int block, int V, int K, const float2* stats, int32_t* tok,
+                       float* lp, cudaStream_t s);
+cudaError_t tree_build(const int32_t* cand_tok, const float* cand_lp, const int32_t* anchor, int batch, int D, int K,
+                       int budget, int32_t* tokens, int32_t* parent, int32_t* depth, uint64_t* mask, cudaStream_t s);
+cudaError_t accept_tree(const int32_t* tokens, const int32_t* parent, const int32_t* argmax, int batch, int n,
+                        int32_t* len, int32_t* anchor, int32_t* n_pend, int32_t* accept_len, int32_t* stream,
+                        int32_t* stream_len, int stream_cap, int32_t* path, int32_t* p0, int32_t* acc, int* status,
+                        cudaStream_t s);
+cudaError_t compact_kv(int dtype, void* kc, void* vc, int layers, int batch, int nkv, size_t layer_stride,
+                       size_t seq_stride, size_t head_stride, int hd, int capacity, const int32_t* path,
+                       const int32_t* p0, const int32_t* acc, cudaStream_t s);
+cudaError_t compact_rows(int dtype, void* rows, size_t row_elems, int batch, int n, const int32_t* path,
+                         const int32_t* acc, cudaStream_t s);
 
 cudaError_t commit_rows(int32_t* len, int32_t* n_pend, int32_t* anchor, const int32_t* argmax, int batch, int n,
                         int emit, int32_t* stream, int32_t* stream_len, int stream_cap, int* status,

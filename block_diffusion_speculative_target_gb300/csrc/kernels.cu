@@ -115,20 +115,21 @@ template <typename T>
 __global__ void rope_qkv_kernel(const float* __restrict__ qkv, int n, int nq, int nkv, int hd, T* __restrict__ qout,
                                 T* __restrict__ kc, T* __restrict__ vc, size_t seq_stride, size_t head_stride,
                                 int capacity, const int32_t* __restrict__ len, const float2* __restrict__ tab,
-                                int* status) {
+                                const int32_t* __restrict__ rope_off, int* status) {
   const int r = blockIdx.x, b = r / n, j = r % n;
   const int half = hd / 2;
   const int width = (nq + 2 * nkv) * hd;
   pdl_launch();
   pdl_wait();
   const int pos = len[b] + j;
-  const bool in_cap = pos < capacity;
+  const int rpos = rope_off ? len[b] + rope_off[r] : pos;  // RoPE position (a tree node's depth)
+  const bool in_cap = pos < capacity && rpos >= 0 && rpos < capacity;
   if (!in_cap && threadIdx.x == 0) set_status(status, DFLASH_STATUS_CAPACITY);
   const float* src = qkv + (size_t)r * width;
   // q and k heads: nq + nkv heads x half pairs
   for (int t = threadIdx.x; t < (nq + nkv) * half; t += blockDim.x) {
     const int h = t / half, i = t % half;
-    const float2 cs = in_cap ? tab[(size_t)pos * half + i] : make_float2(1.f, 0.f);
+    const float2 cs = in_cap ? tab[(size_t)rpos * half + i] : make_float2(1.f, 0.f);
     const float a = src[h * hd + i], c = src[h * hd + i + half];
     const float ra = a * cs.x - c * cs.y, rc = c * cs.x + a * cs.y;
     if (h < nq) {
@@ -152,15 +153,15 @@ __global__ void rope_qkv_kernel(const float* __restrict__ qkv, int n, int nq, in
 
 cudaError_t rope_qkv(int dtype, const float* qkv, int batch, int n, int nq, int nkv, int hd, void* qout, void* kc,
                      void* vc, size_t seq_stride, size_t head_stride, int capacity, const int32_t* len,
-                     const float2* tab, int* status, cudaStream_t s) {
+                     const float2* tab, const int32_t* rope_off, int* status, cudaStream_t s) {
   const int rows = batch * n;
   if (rows <= 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
     DFL_RET(launch_pdl(rope_qkv_kernel<bf16>, dim3(rows), dim3(256), 0, s, qkv, n, nq, nkv, hd, (bf16*)qout, (bf16*)kc, (bf16*)vc, seq_stride,
-                                               head_stride, capacity, len, tab, status));
+                                               head_stride, capacity, len, tab, rope_off, status));
   else
     DFL_RET(launch_pdl(rope_qkv_kernel<float>, dim3(rows), dim3(256), 0, s, qkv, n, nq, nkv, hd, (float*)qout, (float*)kc, (float*)vc,
-                                                seq_stride, head_stride, capacity, len, tab, status));
+                                                seq_stride, head_stride, capacity, len, tab, rope_off, status));
   count_launch();
   return cudaGetLastError();
 }

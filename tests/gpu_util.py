@@ -48,6 +48,23 @@ def check_tokens(gpu, ref, gap, dtype, what, bound=None):
     return int(((gpu != ref) & ~bad).sum())
 
 
+def check_tokens_vs_logits(gpu_tok, ref_tok, ref_gap, gpu_logits, ref_logits, dtype, what):
+    """Greedy tokens against the oracle's, given both sides' logits: if the GPU
+    picks b where the oracle picks a, then ref[a] - ref[b] <= 2 max|gpu - ref|
+    over the row, so a row's tokens must agree wherever the oracle's top-2 gap
+    exceeds max(GAP, 2 x that row's largest logit difference).  The logits
+    themselves are bounded by a separate check.  Returns the number of rows
+    exempted and the number whose tokens differ while the oracle's gap exceeds
+    the stated GAP."""
+    gpu_tok, ref_tok, ref_gap = np.asarray(gpu_tok), np.asarray(ref_tok), np.asarray(ref_gap)
+    dl = np.max(np.abs(np.asarray(gpu_logits, np.float64) - np.asarray(ref_logits, np.float64)), axis=-1)
+    bound = np.maximum(GAP[dtype], 2.0 * dl)
+    differ = gpu_tok != ref_tok
+    bad = differ & (ref_gap > bound)
+    assert not bad.any(), f"{what}: mismatch at {np.nonzero(bad)[0][:10]} (gaps {ref_gap[bad][:5]}, bounds {bound[bad][:5]})"
+    return int((differ & ~bad).sum()), int((differ & (ref_gap > GAP[dtype])).sum())
+
+
 def assert_close(gpu, ref, dtype, what, tol=None):
     gpu, ref = np.asarray(gpu, dtype=np.float64), np.asarray(ref, dtype=np.float64)
     err = np.max(np.abs(gpu - ref)) if gpu.size else 0.0

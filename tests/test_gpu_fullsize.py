@@ -29,8 +29,8 @@ import pytest
 import torch
 
 from conftest import oracle_models, shrink
-from gpu_util import (GAP_TOL, TOL, O, Model, Session, assert_close, assert_close_rounded, capi, check_tokens, dev,
-                      oracle_logits_along, rounder, synth, to_dev, to_np)
+from gpu_util import (GAP_TOL, TOL, O, Model, Session, assert_close, assert_close_rounded, capi, check_tokens,
+                      check_tokens_vs_logits, dev, oracle_logits_along, rounder, synth, to_dev, to_np)
 from tolerances import FLOOR_MARGIN, floor_bound, floor_of, token_gap_bound
 
 pytestmark = pytest.mark.gpu
@@ -194,10 +194,10 @@ def test_verify_full_width(wide):
                        None, None, None, None, 0, s.ws)
     logits = to_np(capi.dflash_workspace_logits(s.ws, B, sh.vocab))
     ref = O.target_forward(tg, toks, kv, rounder(wl))
-    tb = token_gap_bound(name, "verify")
-    n_tie = check_tokens(s.argmax[:B].cpu().numpy(), ref.argmax, ref.gap, "bf16", "full-width verify argmax", bound=tb)
-    _record({"workload": name, "stage": "verify", "output": "tokens", "token_gap_bound": tb, "exempt": n_tie,
-             "differ_above_stated_1e-2": int(np.sum((s.argmax[:B].cpu().numpy() != ref.argmax) & (ref.gap > 1e-2)))})
+    n_tie, n_stated = check_tokens_vs_logits(s.argmax[:B].cpu().numpy(), ref.argmax, ref.gap, logits, ref.logits,
+                                             "bf16", "full-width verify argmax")
+    _record({"workload": name, "stage": "verify", "output": "tokens", "exempt": n_tie,
+             "differ_above_stated_1e-2": n_stated})
     gap_bound = max(GAP_TOL["bf16"], FLOOR_MARGIN * floor_of(name, "verify", "tokens", "max_gap_change"))
     assert_close(s.gap[:B].cpu().numpy(), ref.gap, "bf16", "full-width verify top-2 gap", tol=gap_bound)
     _check_float(name, "verify", "logits", logits, ref.logits)
@@ -227,10 +227,10 @@ def test_draft_full_width(wide):
     ref_logits = O.draft_logits(dr, tg, anchor, B, kv, rounder(wl))
     ref_tok, gap = O.argmax_top2(ref_logits)
     assert got[0] == anchor
-    tb = token_gap_bound(name, "draft")
-    n_tie = check_tokens(got[1:], ref_tok, gap, "bf16", "full-width draft tokens", bound=tb)
-    _record({"workload": name, "stage": "draft", "output": "tokens", "token_gap_bound": tb, "exempt": n_tie,
-             "differ_above_stated_1e-2": int(np.sum((got[1:] != ref_tok) & (gap > 1e-2)))})
+    n_tie, n_stated = check_tokens_vs_logits(got[1:], ref_tok, gap, logits, ref_logits, "bf16",
+                                             "full-width draft tokens")
+    _record({"workload": name, "stage": "draft", "output": "tokens", "exempt": n_tie,
+             "differ_above_stated_1e-2": n_stated})
     _check_float(name, "draft", "logits", logits, ref_logits)
     assert s.status() == 0
     s.close()

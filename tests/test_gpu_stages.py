@@ -8,7 +8,8 @@ import torch
 import synth
 from block_diffusion_speculative_target_gb300 import capi
 from block_diffusion_speculative_target_gb300.engine import Session, desc_of
-from gpu_util import GAP, GAP_TOL, assert_close, build_model, check_tokens, dev, rounder, to_dev, to_np
+from gpu_util import (GAP, GAP_TOL, assert_close, build_model, check_tokens, check_tokens_vs_logits, dev, rounder,
+                      to_dev, to_np)
 from conftest import shrink
 from oracle import dflash_oracle as O
 
@@ -113,7 +114,7 @@ def test_draft_block(setup):
         ref_logits = O.draft_logits(dr, tg, int(anchors[b]), B, kvs[b], rnd)
         ref, gap = O.draft_forward(dr, tg, int(anchors[b]), B, kvs[b], rnd)
         assert got[b, 0] == anchors[b]
-        check_tokens(got[b, 1:], ref[1:], gap, wl.dtype, f"draft tokens b={b}")
+        check_tokens_vs_logits(got[b, 1:], ref[1:], gap, lg[b, 1:], ref_logits, wl.dtype, f"draft tokens b={b}")
         assert_close(lg[b, 1:], ref_logits, wl.dtype, f"draft logits b={b}")
     assert s.status() == 0
     s.close()
@@ -131,8 +132,10 @@ def test_verify_prefill_commit(setup):
                        s.stream_len, s.stream_cap, s.ws)
     rnd = rounder(wl)
     ref = O.target_forward(tg, prompt, O.KV.empty(sh.n_layers, sh.n_kv, sh.head_dim), rnd)
-    assert_close(to_np(capi.dflash_workspace_logits(s.ws, n, sh.vocab)), ref.logits, wl.dtype, "prefill logits")
-    check_tokens(s.argmax[:n].cpu().numpy(), ref.argmax, ref.gap, wl.dtype, "prefill argmax")
+    lg = to_np(capi.dflash_workspace_logits(s.ws, n, sh.vocab))
+    assert_close(lg, ref.logits, wl.dtype, "prefill logits")
+    check_tokens_vs_logits(s.argmax[:n].cpu().numpy(), ref.argmax, ref.gap, lg, ref.logits, wl.dtype,
+                           "prefill argmax")
     assert_close(s.gap[:n].cpu().numpy(), ref.gap, wl.dtype, "prefill top-2 gap", tol=GAP_TOL[wl.dtype])
     assert_close(to_np(s.hcap[:n]), ref.hcap, wl.dtype, "prefill captured states")
     for li in (0, sh.n_layers // 2, sh.n_layers - 1):
@@ -165,9 +168,9 @@ def test_verify_block_on_context(setup):
     lg = to_np(capi.dflash_workspace_logits(s.ws, batch * B, sh.vocab)).reshape(batch, B, -1)
     for b in range(batch):
         ref = O.target_forward(tg, toks[b], kvs[b], rnd)
-        check_tokens(am[b], ref.argmax, ref.gap, wl.dtype, f"verify argmax b={b}")
-        assert_close(hc[b], ref.hcap, wl.dtype, f"verify hcap b={b}")
         assert_close(lg[b], ref.logits, wl.dtype, f"verify logits b={b}")
+        check_tokens_vs_logits(am[b], ref.argmax, ref.gap, lg[b], ref.logits, wl.dtype, f"verify argmax b={b}")
+        assert_close(hc[b], ref.hcap, wl.dtype, f"verify hcap b={b}")
     assert s.status() == 0
     s.close()
 
