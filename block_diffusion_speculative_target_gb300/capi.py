@@ -74,6 +74,9 @@ _SIGS = {
     "dflash_draft_sample": (_I, [_I, _I, _I, c_float, _P, _P, _P, _P]),
     "dflash_accept_sample": (_I, [_P, _I, _I, _I, c_float, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P]),
     "dflash_sample": (_I, [_P, _I, _I, c_float, _P, _P, _P, _P]),
+    "dflash_draft_tree": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "target_verify_tree": (_I, [POINTER(TargetC), _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "dflash_accept_tree": (_I, [POINTER(TargetC), _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P]),
     "dflash_debug_set_wait_limit": (_I, [ctypes.c_int64]),
     "dflash_fuse_features": (_I, [POINTER(DraftC), _P, _I, _P, _P, _P]),
     "dflash_inject_kv": (_I, [POINTER(DraftC), _P, _I, _I, _P, _P, _P, _P]),
@@ -279,6 +282,31 @@ def dflash_teacher_force(draft_tokens, batch, block, ref, ref_stride, ref_len, s
     _check(load().dflash_teacher_force(_ptr(draft_tokens), batch, block, _ptr(ref), ref_stride, ref_len,
                                        _ptr(stream_len), _ptr(k_draw), _ptr(r_draw), max_steps, _ptr(step), vocab, ws,
                                        _stream(stream)), "dflash_teacher_force")
+
+
+# ---------------------------------------------------------------- tree verification
+
+
+def dflash_draft_tree(anchor, batch, block, vocab, topk, budget, tree_tokens, tree_parent, tree_depth, tree_mask, ws,
+                      stream=None):
+    _check(load().dflash_draft_tree(_ptr(anchor), batch, block, vocab, topk, budget, _ptr(tree_tokens),
+                                    _ptr(tree_parent), _ptr(tree_depth), _ptr(tree_mask), ws, _stream(stream)),
+           "dflash_draft_tree")
+
+
+def target_verify_tree(target: TargetC, tree_tokens, tree_depth, tree_mask, batch, n, target_cache, argmax, top2_gap,
+                       hcap, ws, stream=None):
+    _check(load().target_verify_tree(ctypes.byref(target), _ptr(tree_tokens), _ptr(tree_depth), _ptr(tree_mask),
+                                     batch, n, target_cache, _ptr(argmax), _ptr(top2_gap), _ptr(hcap), ws,
+                                     _stream(stream)), "target_verify_tree")
+
+
+def dflash_accept_tree(target: TargetC, tree_tokens, tree_parent, argmax, batch, n, target_cache, hcap, anchor, n_pend,
+                       accept_len, stream_buf, stream_len, stream_cap, ws, stream=None):
+    _check(load().dflash_accept_tree(ctypes.byref(target), _ptr(tree_tokens), _ptr(tree_parent), _ptr(argmax), batch,
+                                     n, target_cache, _ptr(hcap), _ptr(anchor), _ptr(n_pend), _ptr(accept_len),
+                                     _ptr(stream_buf), _ptr(stream_len), stream_cap, ws, _stream(stream)),
+           "dflash_accept_tree")
 
 
 # ---------------------------------------------------------------- sampling mode

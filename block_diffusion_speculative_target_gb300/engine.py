@@ -135,9 +135,10 @@ class Session:
     """Caches, workspace and device state for ``batch`` sequences."""
 
     def __init__(self, model: Model, batch=1, capacity=1024, block=16, prefill_chunk=128, stream_cap=None,
-                 with_draft=True):
-        if batch * block > 128 or prefill_chunk > 128:
-            raise ValueError("at most 128 rows per call")
+                 with_draft=True, tree_budget=0):
+        tree_n = tree_budget + 1 if tree_budget else 0
+        if batch * max(block, tree_n) > 128 or prefill_chunk > 128 or tree_n > 64:
+            raise ValueError("at most 128 rows per call and 64 tree nodes")
         self.m, self.batch, self.block, self.capacity = model, batch, block, capacity
         self.chunk = prefill_chunk
         self.stream_cap = stream_cap or capacity
@@ -148,7 +149,7 @@ class Session:
         tdt = _DT[model.dtype][1]
         self.tcache = capi.dflash_cache_alloc(self.tdesc, s.n_layers, batch, capacity)
         self.dcache = capi.dflash_cache_alloc(self.ddesc, model.draft_layers, batch, capacity) if with_draft else None
-        self.max_rows = max(batch * block, prefill_chunk)
+        self.max_rows = max(batch * block, batch * tree_n, prefill_chunk)
         self.ws = capi.dflash_workspace_alloc(self.tdesc, self.ddesc if with_draft else None, self.max_rows, capacity)
         i32 = dict(dtype=torch.int32, device=dev)
         self.anchor = torch.zeros(batch, **i32)
@@ -164,6 +165,13 @@ class Session:
         self.step_ctr = torch.zeros(1, **i32)
         self.ref = self.k_draw = self.r_draw = None
         self.steps_done = 0
+        self.rps = block  # rows per sequence of the last verification (the layout of hcap)
+        if tree_n:
+            self.tree_budget, self.tree_n = tree_budget, tree_n
+            self.tree_tokens = torch.zeros(batch, tree_n, **i32)
+            self.tree_parent = torch.zeros(batch, tree_n, **i32)
+            self.tree_depth = torch.zeros(batch, tree_n, **i32)
+            self.tree_mask = torch.zeros(batch, tree_n, dtype=torch.int64, device=dev)  # uint64 bit masks
 
     def close(self):
         for h, f in ((self.tcache, capi.dflash_cache_free), (self.dcache, capi.dflash_cache_free),
@@ -256,10 +264,11 @@ class Session:
     def step(self, teacher=False):
         """One DFlash step for every sequence (asynchronous)."""
         tgt, dr = self.m.structs()
-        B, rows = self.block, self.batch * self.block
-        capi.dflash_fuse_features(dr, self.hcap, rows, self.fused, self.ws)
-        capi.dflash_inject_kv(dr, self.fused, self.batch, B, self.n_pend, self.dcache, self.ws)
+        B = self.block
+        capi.dflash_fuse_features(dr, self.hcap, self.batch * self.rps, self.fused, self.ws)
+        capi.dflash_inject_kv(dr, self.fused, self.batch, self.rps, self.n_pend, self.dcache, self.ws)
         capi.dflash_draft_block(dr, tgt, self.anchor, self.batch, B, self.dcache, self.draft, self.ws)
+        self.rps = B
         if teacher:
             capi.dflash_teacher_force(self.draft, self.batch, B, self.ref, self.ref.shape[1], self.ref.shape[1],
                                       self.stream_len, self.k_draw, self.r_draw, self.k_draw.shape[0], self.step_ctr,
@@ -289,15 +298,36 @@ class Session:
         its block with w [batch][B-1], the target verifies it by speculative
         sampling with u [batch][B-1] and v [batch] (device float32 uniforms)."""
         tgt, dr = self.m.structs()
-        B, rows, V = self.block, self.batch * self.block, self.m.shape.vocab
-        capi.dflash_fuse_features(dr, self.hcap, rows, self.fused, self.ws)
-        capi.dflash_inject_kv(dr, self.fused, self.batch, B, self.n_pend, self.dcache, self.ws)
+        B, V = self.block, self.m.shape.vocab
+        capi.dflash_fuse_features(dr, self.hcap, self.batch * self.rps, self.fused, self.ws)
+        capi.dflash_inject_kv(dr, self.fused, self.batch, self.rps, self.n_pend, self.dcache, self.ws)
         capi.dflash_draft_block(dr, tgt, self.anchor, self.batch, B, self.dcache, self.draft, self.ws)
+        self.rps = B
         capi.dflash_draft_sample(self.batch, B, V, temperature, w, self.draft, self.ws)
         capi.target_verify(tgt, self.draft, self.batch, B, 0, self.tcache, self.argmax, self.gap, self.hcap, None,
                            None, None, None, 0, self.ws)
         capi.dflash_accept_sample(self.draft, self.batch, B, V, temperature, u, v, self.tcache, self.anchor,
                                   self.n_pend, self.accept_len, self.stream, self.stream_len, self.stream_cap, self.ws)
+        self.steps_done += 1
+
+    def step_tree(self, topk):
+        """One DFlash step with tree verification (asynchronous): the drafter's
+        block, the tree of its top-k candidates within the session's budget,
+        one ancestor-masked target forward over the tree, the walk and the
+        compaction of the accepted path."""
+        tgt, dr = self.m.structs()
+        B, V, n = self.block, self.m.shape.vocab, self.tree_n
+        capi.dflash_fuse_features(dr, self.hcap, self.batch * self.rps, self.fused, self.ws)
+        capi.dflash_inject_kv(dr, self.fused, self.batch, self.rps, self.n_pend, self.dcache, self.ws)
+        capi.dflash_draft_block(dr, tgt, self.anchor, self.batch, B, self.dcache, self.draft, self.ws)
+        capi.dflash_draft_tree(self.anchor, self.batch, B, V, topk, self.tree_budget, self.tree_tokens,
+                               self.tree_parent, self.tree_depth, self.tree_mask, self.ws)
+        capi.target_verify_tree(tgt, self.tree_tokens, self.tree_depth, self.tree_mask, self.batch, n, self.tcache,
+                                self.argmax, self.gap, self.hcap, self.ws)
+        capi.dflash_accept_tree(tgt, self.tree_tokens, self.tree_parent, self.argmax, self.batch, n, self.tcache,
+                                self.hcap, self.anchor, self.n_pend, self.accept_len, self.stream, self.stream_len,
+                                self.stream_cap, self.ws)
+        self.rps = n
         self.steps_done += 1
 
     def ar_step(self):

@@ -264,6 +264,56 @@ int dflash_teacher_force(int32_t *draft_tokens, int32_t batch, int32_t block, co
                          const int32_t *k_draw, const int32_t *r_draw, int32_t max_steps,
                          int32_t *step, int32_t vocab, dflash_workspace *ws, dflash_stream_t stream);
 
+/* ------------------------------------------------------ tree verification
+ * "DFlash 深度解析" §8.2 (DDTree): one target forward explores several
+ * branches of the drafter's guesses within a node budget instead of one
+ * chain; the page prints no algorithm.  These calls take the following
+ * reading (greedy):
+ *   - candidates: per drafted slot j = 1..block-1, the drafter's top-K tokens
+ *     by log-probability log q_j (softmax of the slot's logits; ties to the
+ *     lower id);
+ *   - the tree: the `budget` highest-scoring token prefixes, a prefix scoring
+ *     the sum of its tokens' log q (best-first; every prefix's parent scores at
+ *     least as high, so they form a tree rooted at the anchor); ties to the
+ *     smaller depth, then the smaller rank, then the earlier parent;
+ *   - verification: one target forward over the n = budget + 1 nodes (node 0
+ *     the anchor), node i at position P + depth(i), attending to the context
+ *     and to its own ancestors (itself included);
+ *   - acceptance: from the root, move to the child whose token equals the
+ *     target's greedy token after the current node while there is one; emit
+ *     the path's tokens and the greedy token after its last node.
+ * With K = 1 and budget = block - 1 the tree is the drafter's greedy chain and
+ * the step equals linear verification.  Trees hold at most 64 nodes
+ * (budget <= 63).  Per-sequence arrays are [batch][n], device memory owned by
+ * the caller; tree_mask[b][i] has bit j set for every ancestor j of node i and
+ * for i itself. */
+
+/* After dflash_draft_block: build each sequence's tree from the drafter's
+ * logits (workspace buffer 1).  topk in [1, 8]; budget in [1, 63] and at most
+ * the number of prefixes the candidates allow, else DFLASH_ERR_INVALID_ARG. */
+int dflash_draft_tree(const int32_t *anchor, int32_t batch, int32_t block, int32_t vocab, int32_t topk,
+                      int32_t budget, int32_t *tree_tokens, int32_t *tree_parent, int32_t *tree_depth,
+                      uint64_t *tree_mask, dflash_workspace *ws, dflash_stream_t stream);
+/* Target forward of the trees (n = budget + 1 rows per sequence) at
+ * positions P + depth, ancestor-masked; keys/values are written at the scratch
+ * slots P .. P + n - 1 in node order; argmax [batch][n], top2_gap (nullable),
+ * hcap [batch][n][5H] (nullable); lengths untouched. */
+int target_verify_tree(const dflash_target *tg, const int32_t *tree_tokens, const int32_t *tree_depth,
+                       const uint64_t *tree_mask, int32_t batch, int32_t n, dflash_cache *target_cache,
+                       int32_t *argmax, float *top2_gap, void *hcap, dflash_workspace *ws,
+                       dflash_stream_t cuda_stream);
+/* The walk and the rollback: the accepted path's a drafted tokens and the
+ * bonus are appended to stream; the path's keys/values (every target layer)
+ * move from their node slots to positions P .. P + a and its captured rows
+ * (hcap, nullable, [batch][n][5H]) to rows 0 .. a of the sequence's block;
+ * len += a + 1, anchor = the bonus, n_pend = a + 1, accept_len = a
+ * (nullable). */
+int dflash_accept_tree(const dflash_target *tg, const int32_t *tree_tokens, const int32_t *tree_parent,
+                       const int32_t *argmax, int32_t batch, int32_t n, dflash_cache *target_cache, void *hcap,
+                       int32_t *anchor, int32_t *n_pend, int32_t *accept_len, int32_t *stream,
+                       int32_t *stream_len, int32_t stream_cap, dflash_workspace *ws,
+                       dflash_stream_t cuda_stream);
+
 /* ------------------------------------------------------------ sampling mode
  * "DFlash 深度解析" §4.2: the speed-up holds at temperature 1 with the
  * output distribution unchanged; the page gives no rule.  These calls take
