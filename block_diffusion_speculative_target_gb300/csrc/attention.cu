@@ -50,14 +50,15 @@ __global__ void __launch_bounds__(NT)
   for (int i = threadIdx.x; i < hd; i += NT) qs[i] = q[((size_t)r * nq + hq) * hd + i];
   __syncthreads();
   // tree verification: block key P + i is visible only when bit i is set (the node's ancestors)
-  const uint64_t tm = tree_mask ? tree_mask[r] : ~0ull;
+  // (only then is n <= 64, so key - P < 64 keeps the shift defined)
+  const uint64_t tm = tree_mask ? tree_mask[r] : 0ull;
   float mx = -INFINITY;
   for (int key = kb + threadIdx.x; key < ke; key += NT) {
     const float* kr = kbase + (size_t)key * hd;
     float acc = 0.f;
     for (int i = 0; i < hd; ++i) acc = fmaf(qs[i], kr[i], acc);
     acc *= scale_log2;
-    if (key >= P && !((tm >> (key - P)) & 1ull)) acc = -INFINITY;
+    if (tree_mask && key >= P && !((tm >> (key - P)) & 1ull)) acc = -INFINITY;
     sc[key - kb] = acc;
     mx = fmaxf(mx, acc);
   }

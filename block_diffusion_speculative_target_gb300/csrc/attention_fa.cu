@@ -278,7 +278,9 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     const bool row_ok = r < 16 * G && qi < n;
     const int lim = row_ok ? min(causal ? P + qi + 1 : P + n, capacity) : 0;  // visible keys [lo, lim)
     // tree verification: block key P + i is visible only when bit i is set (the node's ancestors)
-    const uint64_t tm = (tree_mask && row_ok) ? tree_mask[(size_t)b * n + qi] : ~0ull;
+    // (only then is n <= 64, so k - P < 64 keeps the shift defined)
+    const bool tree = tree_mask != nullptr;
+    const uint64_t tm = (tree && row_ok) ? tree_mask[(size_t)b * n + qi] : 0ull;
     const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
     const uint32_t obase = tmem + lrow + 256 + h * 64;  // this half's 64 output columns
     float M = -INFINITY, Lh = 0.f;
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 #pragma unroll
         for (int e = 0; e < 64; ++e) {
           const int k = k0 + e;
-          if (k >= lo && k < lim && (k < P || ((tm >> (k - P)) & 1ull))) lm = fmaxf(lm, __uint_as_float(v[e]));
+          if (k >= lo && k < lim && (!tree || k < P || ((tm >> (k - P)) & 1ull))) lm = fmaxf(lm, __uint_as_float(v[e]));
         }
         xch[(sb * 2 + h) * 128 + r] = lm;
       }
@@ -326,9 +328,9 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int k = k0 + 2 * e;
-          const float p0 = (k >= lo && k < lim && (k < P || ((tm >> (k - P)) & 1ull)))
+          const float p0 = (k >= lo && k < lim && (!tree || k < P || ((tm >> (k - P)) & 1ull)))
                                ? ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm)) : 0.f;
-          const float p1 = (k + 1 >= lo && k + 1 < lim && (k + 1 < P || ((tm >> (k + 1 - P)) & 1ull)))
+          const float p1 = (k + 1 >= lo && k + 1 < lim && (!tree || k + 1 < P || ((tm >> (k + 1 - P)) & 1ull)))
                                ? ex2f(fmaf(__uint_as_float(v[2 * e + 1]), scale_log2, negm)) : 0.f;
           lt += p0;
           lt += p1;
