@@ -294,14 +294,24 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       const uint32_t sbase = tmem + lrow + sb * 128 + h * 64;  // this half's 64 score columns
       uint32_t v[64];
       float lm = -INFINITY;
+      // this row's visible keys of the half: [va, vb) (and, in tree mode, the ancestor bits)
+      const int va = min(64, max(0, lo - k0)), vb = max(0, min(64, lim - k0));
+      const bool wfull = __all_sync(0xffffffffu, !tree && va == 0 && vb == 64);  // warp-uniform fast path
+      auto vis = [&](int e) {
+        const int k = k0 + e;
+        return e >= va && e < vb && (!tree || k < P || ((tm >> (k - P)) & 1ull));
+      };
       if (live) {  // this half's scores and their maximum over the visible keys
         tmem_ld32(sbase, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         tmem_ld32(sbase + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
         tmem_ld_wait();
+        if (wfull) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const int k = k0 + e;
-          if (k >= lo && k < lim && (!tree || k < P || ((tm >> (k - P)) & 1ull))) lm = fmaxf(lm, __uint_as_float(v[e]));
+          for (int e = 0; e < 64; ++e) lm = fmaxf(lm, __uint_as_float(v[e]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (vis(e)) lm = fmaxf(lm, __uint_as_float(v[e]));
         }
         xch[(sb * 2 + h) * 128 + r] = lm;
       }
@@ -325,16 +335,24 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         const float negm = Mn == -INFINITY ? 0.f : -Mn;
         float lt = 0.f;
         uint32_t hi[32], lo_[32];
+        if (wfull) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int k = k0 + 2 * e;
-          const float p0 = (k >= lo && k < lim && (!tree || k < P || ((tm >> (k - P)) & 1ull)))
-                               ? ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm)) : 0.f;
-          const float p1 = (k + 1 >= lo && k + 1 < lim && (!tree || k + 1 < P || ((tm >> (k + 1 - P)) & 1ull)))
-                               ? ex2f(fmaf(__uint_as_float(v[2 * e + 1]), scale_log2, negm)) : 0.f;
-          lt += p0;
-          lt += p1;
-          pack_bf16_hilo(p0, p1, hi[e], lo_[e]);
+          for (int e = 0; e < 32; ++e) {
+            const float p0 = ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm));
+            const float p1 = ex2f(fmaf(__uint_as_float(v[2 * e + 1]), scale_log2, negm));
+            lt += p0;
+            lt += p1;
+            pack_bf16_hilo(p0, p1, hi[e], lo_[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float p0 = vis(2 * e) ? ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm)) : 0.f;
+            const float p1 = vis(2 * e + 1) ? ex2f(fmaf(__uint_as_float(v[2 * e + 1]), scale_log2, negm)) : 0.f;
+            lt += p0;
+            lt += p1;
+            pack_bf16_hilo(p0, p1, hi[e], lo_[e]);
+          }
         }
         // every score of this half is in registers: P overwrites them (hi at +0..31, lo at +32..63)
         tmem_st16(sbase, *reinterpret_cast<const uint32_t(*)[16]>(&hi[0]));

@@ -3,6 +3,8 @@ footprint, suitable for Nsight Compute captures).
 
     python -m block_diffusion_speculative_target_gb300.kernel_bench gemm --M 24576 --K 4096 --rows 16
     python -m block_diffusion_speculative_target_gb300.kernel_bench attention --P 4096 --nq 32 --nkv 8 --n 16
+    python -m block_diffusion_speculative_target_gb300.kernel_bench rmsnorm --rows 16 --H 4096
+    python -m block_diffusion_speculative_target_gb300.kernel_bench argmax --rows 16 --V 151936
 
 Weights rotate over enough copies that every launch streams from HBM, not L2.
 The timed launches are captured in a CUDA graph, so host launch overhead is
@@ -90,13 +92,52 @@ def bench_attention(P, nq, nkv, n, iters, warmup, causal=1):
         capi.dflash_cache_free(c)
     capi.dflash_workspace_free(ws)
     byt = 2 * 2 * nkv * (P + n) * hd
-    return {"kernel": "attn_tc_kernel+attn_combine_kernel", "P": P, "nq": nq, "nkv": nkv, "n": n, "ms": avg,
+    return {"kernel": "attn_fa_kernel+attn_combine_kernel", "P": P, "nq": nq, "nkv": nkv, "n": n, "ms": avg,
             "bytes": byt, "GBps": byt / (avg / 1e3) / 1e9}
+
+
+def bench_rmsnorm(rows, H, iters, warmup):
+    """RMSNorm of float32 rows [rows][H] into bf16 (copies rotate so every
+    launch reads from HBM)."""
+    dev = torch.device("cuda")
+    copies = max(2, -(-3 * L2_BYTES // (4 * rows * H)))
+    g = torch.Generator(device=dev).manual_seed(2)
+    xs = [torch.empty(rows, H, dtype=torch.float32, device=dev).normal_(0, 3, generator=g) for _ in range(copies)]
+    gain = torch.ones(H, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(rows, H, dtype=torch.bfloat16, device=dev)
+    for i in range(warmup):
+        capi.dflash_rmsnorm(capi.BF16, xs[i % copies], gain, y, rows, H, 1e-6)
+    avg = _graph_time(lambda: [capi.dflash_rmsnorm(capi.BF16, xs[i % copies], gain, y, rows, H, 1e-6)
+                               for i in range(iters)], iters)
+    byt = 4 * rows * H + 2 * rows * H + 2 * H
+    return {"kernel": "rmsnorm_kernel", "rows": rows, "H": H, "ms": avg, "bytes": byt,
+            "GBps": byt / (avg / 1e3) / 1e9}
+
+
+def bench_argmax(rows, V, iters, warmup):
+    """Greedy token + top-2 gap of float32 logits [rows][V]."""
+    dev = torch.device("cuda")
+    copies = max(2, -(-3 * L2_BYTES // (4 * rows * V)))
+    g = torch.Generator(device=dev).manual_seed(3)
+    zs = [torch.empty(rows, V, dtype=torch.float32, device=dev).normal_(0, 2, generator=g) for _ in range(copies)]
+    d = capi.ModelDesc(1, 256, 4, 4, 64, 768, V, 1e6, 1e-6, capi.F32)
+    ws = capi.dflash_workspace_alloc(d, None, max(rows, 16), 256)
+    out = torch.empty(rows, dtype=torch.int32, device=dev)
+    gap = torch.empty(rows, dtype=torch.float32, device=dev)
+    for i in range(warmup):
+        capi.dflash_argmax(zs[i % copies], rows, V, out, gap, ws)
+    avg = _graph_time(lambda: [capi.dflash_argmax(zs[i % copies], rows, V, out, gap, ws) for i in range(iters)], iters)
+    assert capi.dflash_status(ws) == 0
+    capi.dflash_workspace_free(ws)
+    byt = 4 * rows * V
+    return {"kernel": "argmax_kernel", "rows": rows, "V": V, "ms": avg, "bytes": byt, "GBps": byt / (avg / 1e3) / 1e9}
 
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["gemm", "attention", "step-gemms"])
+    ap.add_argument("kernel", choices=["gemm", "attention", "step-gemms", "rmsnorm", "argmax"])
+    ap.add_argument("--H", type=int, default=4096)
+    ap.add_argument("--V", type=int, default=151936)
     ap.add_argument("--M", type=int, default=24576)
     ap.add_argument("--K", type=int, default=4096)
     ap.add_argument("--rows", type=int, default=16)
@@ -112,6 +153,10 @@ def main():
         print(json.dumps(bench_gemm(a.M, a.K, a.rows, a.iters, a.warmup)))
     elif a.kernel == "attention":
         print(json.dumps(bench_attention(a.P, a.nq, a.nkv, a.n, a.iters, a.warmup)))
+    elif a.kernel == "rmsnorm":
+        print(json.dumps(bench_rmsnorm(a.rows, a.H, a.iters, a.warmup)))
+    elif a.kernel == "argmax":
+        print(json.dumps(bench_argmax(a.rows, a.V, a.iters, a.warmup)))
     else:
         # every weight-GEMM shape of one Qwen3-8B-shaped step (4096 hidden, 32/8 x 128 heads, FFN 12288)
         for M, K in ((6144, 4096), (4096, 4096), (24576, 4096), (4096, 12288), (151936, 4096), (4096, 20480),
