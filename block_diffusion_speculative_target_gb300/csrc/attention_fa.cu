@@ -296,7 +296,9 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       float lm = -INFINITY;
       // this row's visible keys of the half: [va, vb) (and, in tree mode, the ancestor bits)
       const int va = min(64, max(0, lo - k0)), vb = max(0, min(64, lim - k0));
-      const bool wfull = __all_sync(0xffffffffu, !tree && va == 0 && vb == 64);  // warp-uniform fast path
+      // warp-uniform fast path when every real row of the warp sees the whole half (padding rows -- past
+      // 16 G or past the block -- are never read, so their values may be anything)
+      const bool wfull = __all_sync(0xffffffffu, !row_ok || (!tree && va == 0 && vb == 64));
       auto vis = [&](int e) {
         const int k = k0 + e;
         return e >= va && e < vb && (!tree || k < P || ((tm >> (k - P)) & 1ull));
