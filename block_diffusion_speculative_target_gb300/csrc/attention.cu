@@ -87,93 +87,78 @@ __global__ void __launch_bounds__(NT)
   }
 }
 
-// Merge of the chunk partials of one (row, head): with w_c = 2^(m_c - max m),
-// out[d] = sum_c w_c o_c[d] / sum_c w_c l_c.  kCombineGroups x 64 threads:
-// thread (d2, g) owns columns 2 d2 and 2 d2 + 1 and sums them over the g-th
-// contiguous slice of the chunks (float2 loads, unrolled for memory-level
-// parallelism); the slices are added in group order, and the max and the
-// denominator are reduced by warp 0 over a fixed butterfly.  The result
-// depends only on the row's own chunks.  (256-thread blocks leave room on each
-// SM for the next kernel's CTAs to start early.)
+// Merge of the key-group partials of one (row, head), one warp per pair:
+// with w_c = 2^(m_c - max m), out[d] = sum_c w_c o_c[d] / sum_c w_c l_c, the
+// numerator summed over c in increasing order.  Lane l owns columns 4 l ..
+// 4 l + 3.  The first kCombineBatch groups' partial rows are loaded before
+// the maxima are known, so the maxima and the rows share one trip to memory;
+// the denominator's per-lane terms are added over a fixed butterfly.  The
+// result depends only on the row's own groups.  (128-thread blocks leave room
+// on each SM for the next kernel's CTAs to start early.)
 constexpr int kCombineMaxChunks = 1024;
-constexpr int kCombineGroups = 4;
-constexpr int kCombineUnroll = 8;  // float2 partial loads in flight per thread
+constexpr int kCombineWarps = 4;
+constexpr int kCombineBatch = 16;  // partial rows in flight per lane
 
 template <typename T>
-__global__ void __launch_bounds__(kCombineGroups * 64)
-    attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int n, int nq, int hd,
-                        int causal, int capacity, int window, int gk, const int32_t* __restrict__ len, int nchunk,
-                        T* __restrict__ out) {
-  __shared__ float w[kCombineMaxChunks];
-  __shared__ float lsum[kCombineMaxChunks];
-  __shared__ float slice[kCombineGroups][kHD];
-  __shared__ float Msh, Lsh;
-  const int r = blockIdx.x, hq = blockIdx.y;
-  const int b = r / n, j = r % n;
-  const int tid = threadIdx.x, lane = tid & 31;
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int rows, int n, int nq,
+                        int hd, int causal, int capacity, int window, int gk, const int32_t* __restrict__ len,
+                        int nchunk, T* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   pdl_launch();
   pdl_wait();
+  if (item >= rows * nq) return;  // warp-uniform
+  const int r = item / nq, hq = item - r * nq;
+  const int b = r / n, j = r - b * n;
   const int P = len[b];
   const int lim = min(causal ? P + j + 1 : P + n, capacity);
   const int nch = min((lim + gk - 1) / gk, kCombineMaxChunks);
-  // chunks below a cross-context window hold no partial
+  // groups below a cross-context window hold no partial
   const int clo = window > 0 ? min(max(0, P - window) / gk, nch) : 0;
   const size_t row0 = ((size_t)r * nq + hq) * nchunk;
-  for (int c = clo + tid; c < nch; c += blockDim.x) {
-    const float2 ml = *reinterpret_cast<const float2*>(part_ml + (row0 + c) * 2);
-    w[c] = ml.x;
-    lsum[c] = ml.y;
-  }
-  __syncthreads();
-  if (tid < 32) {
-    float m = -INFINITY;
-    for (int c = clo + lane; c < nch; c += 32) m = fmaxf(m, w[c]);
+  const float2* ml = reinterpret_cast<const float2*>(part_ml) + row0;
+  const float4* po = reinterpret_cast<const float4*>(part_o + row0 * kHD) + lane;  // group c at po[c * kHD / 4]
+  float4 v[kCombineBatch];
+  auto load_batch = [&](int c0) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) Msh = m;
-  }
-  __syncthreads();
-  const float M = Msh;
-  for (int c = clo + tid; c < nch; c += blockDim.x) w[c] = (w[c] == -INFINITY) ? 0.f : exp2f(w[c] - M);
-  __syncthreads();
-  if (tid < 32) {
-    float l = 0.f;
-    for (int c = clo + lane; c < nch; c += 32) l += w[c] * lsum[c];
+    for (int u = 0; u < kCombineBatch; ++u)
+      if (c0 + u < nch) v[u] = po[(size_t)(c0 + u) * (kHD / 4)];
+  };
+  load_batch(clo);
+  float m = -INFINITY;
+  for (int c = clo + lane; c < nch; c += 32) m = fmaxf(m, ml[c].x);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    if (lane == 0) Lsh = l;
-  }
-  const int d2 = tid & 63, g = tid >> 6;
-  const int c0 = clo + (nch - clo) * g / kCombineGroups, c1 = clo + (nch - clo) * (g + 1) / kCombineGroups;
-  float2 acc = make_float2(0.f, 0.f);
-  {
-    const float* po = part_o + row0 * kHD + 2 * d2;
-    int c = c0;
-    for (; c + kCombineUnroll <= c1; c += kCombineUnroll) {
-      float2 v[kCombineUnroll];
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float M = m;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.f;
+  for (int c0 = clo; c0 < nch; c0 += kCombineBatch) {
+    // lane u < kCombineBatch holds group c0 + u's weight
+    const int cu = c0 + (lane & (kCombineBatch - 1));
+    const float2 mlu = (lane < kCombineBatch && cu < nch) ? ml[cu] : make_float2(-INFINITY, 0.f);
+    const float wu = mlu.x == -INFINITY ? 0.f : exp2f(mlu.x - M);
+    lsum += wu * mlu.y;
 #pragma unroll
-      for (int u = 0; u < kCombineUnroll; ++u) v[u] = *reinterpret_cast<const float2*>(po + (size_t)(c + u) * kHD);
-#pragma unroll
-      for (int u = 0; u < kCombineUnroll; ++u) {
-        acc.x += w[c + u] * v[u].x;
-        acc.y += w[c + u] * v[u].y;
+    for (int u = 0; u < kCombineBatch; ++u) {
+      const float w = __shfl_sync(0xffffffffu, wu, u);
+      if (c0 + u < nch) {
+        acc.x += w * v[u].x;
+        acc.y += w * v[u].y;
+        acc.z += w * v[u].z;
+        acc.w += w * v[u].w;
       }
     }
-    for (; c < c1; ++c) {
-      const float2 v = *reinterpret_cast<const float2*>(po + (size_t)c * kHD);
-      acc.x += w[c] * v.x;
-      acc.y += w[c] * v.y;
-    }
+    if (c0 + kCombineBatch < nch) load_batch(c0 + kCombineBatch);
   }
-  slice[g][2 * d2] = acc.x;
-  slice[g][2 * d2 + 1] = acc.y;
-  __syncthreads();
-  if (tid < kHD) {
-    const int d = tid;
-    float sum = slice[0][d];
 #pragma unroll
-    for (int k = 1; k < kCombineGroups; ++k) sum += slice[k][d];
-    if (d < hd) out[((size_t)r * nq + hq) * hd + d] = from_f<T>(sum / Lsh);
+  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+  if (4 * lane < hd) {
+    T* dst = out + ((size_t)r * nq + hq) * hd + 4 * lane;
+    dst[0] = from_f<T>(acc.x / lsum);
+    dst[1] = from_f<T>(acc.y / lsum);
+    dst[2] = from_f<T>(acc.z / lsum);
+    dst[3] = from_f<T>(acc.w / lsum);
   }
 }
 
@@ -263,6 +248,7 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
   const int nchunk_launch = (capacity + kAttnChunk - 1) / kAttnChunk;
   if (nchunk_launch > sc.nchunk || nchunk_launch > kCombineMaxChunks || hd > kHD) return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
+  const unsigned combine_blocks = (unsigned)((batch * n * nq + kCombineWarps - 1) / kCombineWarps);
   if (dtype == DFLASH_BF16) {
     if (hd != kHD || !maps) return cudaErrorInvalidValue;
     const int G = nq / nkv;
@@ -270,15 +256,15 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
     if (!make_q_map(q, batch * n, nq, G, &qmap)) return cudaErrorInvalidValue;
     DFL_RET(attention_fa(G, *maps, qmap, batch, n, nq, nkv, causal, window, capacity, gtiles, len, tree_mask, sc,
                          scale_log2, status, s));
-    DFL_RET(launch_pdl(attn_combine_kernel<bf16>, dim3(batch * n, nq), dim3(kCombineGroups * 64), 0, s, sc.o,
-                       sc.ml, n, nq, hd, causal, capacity, window, gtiles * 128, len, sc.nchunk, (bf16*)out));
+    DFL_RET(launch_pdl(attn_combine_kernel<bf16>, dim3(combine_blocks), dim3(kCombineWarps * 32), 0, s, sc.o, sc.ml,
+                       batch * n, n, nq, hd, causal, capacity, window, gtiles * 128, len, sc.nchunk, (bf16*)out));
   } else {
     const dim3 grid(nchunk_launch, nq, batch * n);
     DFL_RET(launch_pdl(attn_f32_kernel<128>, grid, dim3(128), 0, s, (const float*)q, n, nq, nkv, hd, causal,
                        (const float*)kc, (const float*)vc, seq_stride, head_stride, capacity, window, len, tree_mask,
                        sc.o, sc.ml, sc.nchunk, scale_log2));
-    DFL_RET(launch_pdl(attn_combine_kernel<float>, dim3(batch * n, nq), dim3(kCombineGroups * 64), 0, s, sc.o,
-                       sc.ml, n, nq, hd, causal, capacity, window, kAttnChunk, len, sc.nchunk, (float*)out));
+    DFL_RET(launch_pdl(attn_combine_kernel<float>, dim3(combine_blocks), dim3(kCombineWarps * 32), 0, s, sc.o, sc.ml,
+                       batch * n, n, nq, hd, causal, capacity, window, kAttnChunk, len, sc.nchunk, (float*)out));
   }
   count_launch(2);
   return cudaSuccess;

@@ -145,33 +145,12 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
   volatile int* abort_f = reinterpret_cast<volatile int*>(tslot + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {  // the descriptors are kernel parameters: fetch them while the previous kernel drains
+  // Set-up that needs nothing from the previous kernel (barriers, TMEM, the
+  // descriptors) runs before the wait on it.
+  if (tid == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-  }
-  pdl_launch();
-  pdl_wait();
-
-  // ---- the unit
-  const int nrb = (n + 15) >> 4;
-  int u = blockIdx.x;
-  const int hk = u % nkv;
-  u /= nkv;
-  const int rb = u % nrb;
-  u /= nrb;
-  const int b = u % batch;
-  const int gi = u / batch;
-  const int P = len[b];
-  const int r_last = min(rb * 16 + 15, n - 1);
-  const int kmax = min(causal ? P + r_last + 1 : P + n, capacity);
-  const int lo = window > 0 ? max(0, P - window) : 0;
-  const int ta = max(gi * gtiles, lo >> 7);
-  const int tb = min((gi + 1) * gtiles, (kmax + 127) >> 7);
-  const int nt = tb - ta;
-  if (nt <= 0) return;  // uniform over the CTA: no key of this group is visible
-
-  if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
@@ -195,6 +174,29 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  pdl_launch();
+  pdl_wait();
+
+  // ---- the unit
+  const int nrb = (n + 15) >> 4;
+  int u = blockIdx.x;
+  const int hk = u % nkv;
+  u /= nkv;
+  const int rb = u % nrb;
+  u /= nrb;
+  const int b = u % batch;
+  const int gi = u / batch;
+  const int P = len[b];
+  const int r_last = min(rb * 16 + 15, n - 1);
+  const int kmax = min(causal ? P + r_last + 1 : P + n, capacity);
+  const int lo = window > 0 ? max(0, P - window) : 0;
+  const int ta = max(gi * gtiles, lo >> 7);
+  const int tb = min((gi + 1) * gtiles, (kmax + 127) >> 7);
+  const int nt = tb - ta;
+  if (nt <= 0) {  // uniform over the CTA: no key of this group is visible
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
 
   int issued = 0;  // producer: tiles whose copies were issued
   if (warp == 0) {
