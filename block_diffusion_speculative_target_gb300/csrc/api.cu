@@ -43,6 +43,7 @@ struct dflash_workspace {
   size_t x_elems, xn_elems, f32_elems, q_elems, act_elems, logit_elems;
   float* x;
   void* xn;
+  float* ssq;  // [rows][H / 32] sums of squares of the residual's 32-column slices (fused RMSNorm)
   float* f32buf;
   void* q;
   void* attn;
@@ -294,6 +295,7 @@ int dflash_workspace_alloc(const dflash_model_desc* t, const dflash_model_desc* 
   } reqs[] = {
       {(void**)&w->x, R * H * 4},
       {(void**)&w->xn, R * H * es},
+      {(void**)&w->ssq, R * (H / 32 + 1) * 4},
       {(void**)&w->f32buf, R * f32w * 4},
       {(void**)&w->q, R * qw * es},
       {(void**)&w->attn, R * qw * es},
@@ -525,22 +527,37 @@ static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layer
     CK(gemm_f32(ws->xn, H, rows, lm_head, d.vocab, H, Epi{EPI_F32, logits, d.vocab}, s));
     return DFLASH_OK;
   }
+  // Every RMSNorm sits between a residual-add product and the next product:
+  // the residual-add epilogue hands over bf16(x * gain) (the next operand, in
+  // xn) with the rows' 32-column sums of squares (ssq), and the next product
+  // scales its rows by 1 / rms.  Only the first norm runs on its own.
   const int qkvw = (nq + 2 * nkv) * hd;
+  auto normed = [&](GemmEpi e) {
+    e.in_ssq = ws->ssq;
+    e.in_cols = H;
+    e.in_eps = d.rms_eps;
+    return e;
+  };
+  auto handover = [&](GemmEpi e, const void* gain) {
+    e.norm_gain = gain;
+    e.norm_out = ws->xn;
+    e.norm_ssq = ws->ssq;
+    return e;
+  };
+  CK(norm_prep(ws->x, L > 0 ? layers[0].attn_norm : final_norm, ws->xn, ws->ssq, rows, H, s));
   for (int l = 0; l < L; ++l) {
     const dflash_layer_w& w = layers[l];
     uint8_t* kc = c->k + (size_t)l * c->layer_stride * c->elem;
     uint8_t* vc = c->v + (size_t)l * c->layer_stride * c->elem;
-    CK(rmsnorm(d.dtype, ws->x, w.attn_norm, ws->xn, rows, H, d.rms_eps, s));
     GemmEpi qkv = epi_cache(GE_QKV, ws->q, nq * hd, c, l, nq, n, nullptr);
     qkv.rope_off = rope_off;
-    CK(gemm_b16(ws->xn, H, rows, w.wqkv, qkvw, H, qkv, ws, s));
+    CK(gemm_b16(ws->xn, H, rows, w.wqkv, qkvw, H, normed(qkv), ws, s));
     const KvMaps maps = kv_maps(c, l);
     CK(attention(d.dtype, ws->q, batch, n, nq, nkv, hd, causal, window, kc, vc, c->seq_stride, c->head_stride, c->capacity,
                  c->attn_gtiles, c->len, tree_mask, &maps, ws->as, ws->attn, ws->status, s));
-    CK(gemm_b16(ws->attn, nq * hd, rows, w.wo, H, nq * hd, epi_of(GE_RESID, ws->x, H), ws, s));
-    CK(rmsnorm(d.dtype, ws->x, w.ffn_norm, ws->xn, rows, H, d.rms_eps, s));
-    CK(gemm_b16(ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, epi_of(GE_SWIGLU, ws->act, d.ffn), ws, s));
-    GemmEpi down = epi_of(GE_RESID, ws->x, H);
+    CK(gemm_b16(ws->attn, nq * hd, rows, w.wo, H, nq * hd, handover(epi_of(GE_RESID, ws->x, H), w.ffn_norm), ws, s));
+    CK(gemm_b16(ws->xn, H, rows, w.w_gate_up, 2 * d.ffn, H, normed(epi_of(GE_SWIGLU, ws->act, d.ffn)), ws, s));
+    GemmEpi down = handover(epi_of(GE_RESID, ws->x, H), l + 1 < L ? layers[l + 1].attn_norm : final_norm);
     if (hcap) {
       for (int si = 0; si < 5; ++si)
         if (capture[si] == l) down.cap_mask |= 1 << si;
@@ -549,8 +566,7 @@ static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layer
     }
     CK(gemm_b16(ws->act, d.ffn, rows, w.w_down, H, d.ffn, down, ws, s));
   }
-  CK(rmsnorm(d.dtype, ws->x, final_norm, ws->xn, rows, H, d.rms_eps, s));
-  CK(gemm_b16(ws->xn, H, rows, lm_head, d.vocab, H, epi_of(GE_F32, logits, d.vocab), ws, s));
+  CK(gemm_b16(ws->xn, H, rows, lm_head, d.vocab, H, normed(epi_of(GE_F32, logits, d.vocab)), ws, s));
   return DFLASH_OK;
 }
 

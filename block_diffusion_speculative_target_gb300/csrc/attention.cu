@@ -90,17 +90,20 @@ __global__ void __launch_bounds__(NT)
 // Merge of the key-group partials of one (row, head), one warp per pair:
 // with w_c = 2^(m_c - max m), out[d] = sum_c w_c o_c[d] / sum_c w_c l_c, the
 // numerator summed over c in increasing order.  Lane l owns columns 4 l ..
-// 4 l + 3.  The first kCombineBatch groups' partial rows are loaded before
-// the maxima are known, so the maxima and the rows share one trip to memory;
-// the denominator's per-lane terms are added over a fixed butterfly.  The
-// result depends only on the row's own groups.  (128-thread blocks leave room
-// on each SM for the next kernel's CTAs to start early.)
+// 4 l + 3.  The row's length, the first 32 groups' maxima and sums and the
+// first kCombineBatch groups' partial rows are all requested at once, before
+// the row's group range is known (slots past it are read but never used), so
+// a row with few groups needs one trip to memory.  The denominator's per-lane
+// terms are added over a fixed butterfly.  The result depends only on the
+// row's own groups.  The kernel holds no shared memory and at most 80
+// registers a thread, so one 4-warp block fits beside an attention CTA and
+// waits there for it to finish.
 constexpr int kCombineMaxChunks = 1024;
 constexpr int kCombineWarps = 4;
-constexpr int kCombineBatch = 16;  // partial rows in flight per lane
+constexpr int kCombineBatch = 12;  // partial rows in flight per lane
 
 template <typename T>
-__global__ void __launch_bounds__(kCombineWarps * 32)
+__global__ void __launch_bounds__(kCombineWarps * 32, 6)
     attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int rows, int n, int nq,
                         int hd, int causal, int capacity, int window, int gk, const int32_t* __restrict__ len,
                         int nchunk, T* __restrict__ out) {
@@ -111,45 +114,51 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   if (item >= rows * nq) return;  // warp-uniform
   const int r = item / nq, hq = item - r * nq;
   const int b = r / n, j = r - b * n;
-  const int P = len[b];
-  const int lim = min(causal ? P + j + 1 : P + n, capacity);
-  const int nch = min((lim + gk - 1) / gk, kCombineMaxChunks);
-  // groups below a cross-context window hold no partial
-  const int clo = window > 0 ? min(max(0, P - window) / gk, nch) : 0;
   const size_t row0 = ((size_t)r * nq + hq) * nchunk;
   const float2* ml = reinterpret_cast<const float2*>(part_ml) + row0;
   const float4* po = reinterpret_cast<const float4*>(part_o + row0 * kHD) + lane;  // group c at po[c * kHD / 4]
+  const int P = len[b];
+  const float2 ml0 = lane < nchunk ? ml[lane] : make_float2(-INFINITY, 0.f);  // group `lane`
   float4 v[kCombineBatch];
-  auto load_batch = [&](int c0) {
 #pragma unroll
-    for (int u = 0; u < kCombineBatch; ++u)
-      if (c0 + u < nch) v[u] = po[(size_t)(c0 + u) * (kHD / 4)];
-  };
-  load_batch(clo);
-  float m = -INFINITY;
-  for (int c = clo + lane; c < nch; c += 32) m = fmaxf(m, ml[c].x);
+  for (int u = 0; u < kCombineBatch; ++u)
+    if (u < nchunk) v[u] = po[(size_t)u * (kHD / 4)];
+  const int lim = min(causal ? P + j + 1 : P + n, capacity);
+  const int nch = min((lim + gk - 1) / gk, min(nchunk, kCombineMaxChunks));
+  // groups below a cross-context window hold no partial
+  const int clo = window > 0 ? min(max(0, P - window) / gk, nch) : 0;
+  float m = (lane >= clo && lane < nch) ? ml0.x : -INFINITY;
+  for (int c = 32 + lane; c < nch; c += 32)
+    if (c >= clo) m = fmaxf(m, ml[c].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   const float M = m;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float lsum = 0.f;
-  for (int c0 = clo; c0 < nch; c0 += kCombineBatch) {
-    // lane u < kCombineBatch holds group c0 + u's weight
-    const int cu = c0 + (lane & (kCombineBatch - 1));
-    const float2 mlu = (lane < kCombineBatch && cu < nch) ? ml[cu] : make_float2(-INFINITY, 0.f);
+  for (int c0 = 0; c0 < nch; c0 += kCombineBatch) {
+    if (c0 > 0) {
+#pragma unroll
+      for (int u = 0; u < kCombineBatch; ++u)
+        if (c0 + u < nch) v[u] = po[(size_t)(c0 + u) * (kHD / 4)];
+    }
+    // lane u < kCombineBatch: group c0 + u's weight and its term of the denominator (groups below 32
+    // come from the lane that loaded them)
+    const int cu = c0 + lane;
+    const float sx = __shfl_sync(0xffffffffu, ml0.x, cu & 31), sy = __shfl_sync(0xffffffffu, ml0.y, cu & 31);
+    float2 mlu = make_float2(-INFINITY, 0.f);
+    if (lane < kCombineBatch && cu >= clo && cu < nch) mlu = cu < 32 ? make_float2(sx, sy) : ml[cu];
     const float wu = mlu.x == -INFINITY ? 0.f : exp2f(mlu.x - M);
     lsum += wu * mlu.y;
 #pragma unroll
     for (int u = 0; u < kCombineBatch; ++u) {
       const float w = __shfl_sync(0xffffffffu, wu, u);
-      if (c0 + u < nch) {
+      if (c0 + u >= clo && c0 + u < nch) {
         acc.x += w * v[u].x;
         acc.y += w * v[u].y;
         acc.z += w * v[u].z;
         acc.w += w * v[u].w;
       }
     }
-    if (c0 + kCombineBatch < nch) load_batch(c0 + kCombineBatch);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);

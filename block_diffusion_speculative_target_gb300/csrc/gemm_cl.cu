@@ -22,6 +22,12 @@
 // Epilogues: f32 store, f32 residual add, bf16 store, SwiGLU on interleaved
 // gate/up rows, and QKV / drafter-KV with rotate-half RoPE and the KV-cache
 // write at each row's position.
+//
+// RMSNorm across a product boundary: a residual-add epilogue can hand the next
+// product its operand bf16(x * gain) and each row's sums of x^2 over 32-column
+// slices; that product's idle warps turn the slices into the row's
+// 1 / rms during the main loop, and its epilogue scales the row's results by
+// it.  No separate normalisation kernel runs between the two products.
 #include <string.h>
 
 #include <atomic>
@@ -52,7 +58,8 @@ struct ClCfg {
   static constexpr int RING = STAGES * STAGE_BYTES;
   static constexpr int TAIL = 256;   // barriers, TMEM slot, flags
   static constexpr int PRE = 2048;   // epilogue operands prefetched during the main loop
-  static constexpr int SMEM = (RING > RED_BYTES ? RING : RED_BYTES) + 1024 + TAIL + PRE;
+  static constexpr int RS = kMaxRows * 4;  // rows' 1 / rms of a fused RMSNorm
+  static constexpr int SMEM = (RING > RED_BYTES ? RING : RED_BYTES) + 1024 + TAIL + PRE + RS;
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -98,6 +105,28 @@ __device__ __forceinline__ void sum_partials(uint32_t red_local, uint32_t off, u
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// The new residual x of output (n, m): stored, with its captured bf16 copies.
+__device__ __forceinline__ void resid_store(const GemmEpi& e, int n, int m, float x) {
+  reinterpret_cast<float*>(e.out)[(size_t)n * e.ldo + m] = x;
+  if (e.cap_mask)
+    for (int s = 0; s < 5; ++s)
+      if (e.cap_mask & (1 << s))
+        reinterpret_cast<bf16*>(e.hcap)[(size_t)n * 5 * e.cap_H + (size_t)s * e.cap_H + m] = __float2bfloat16_rn(x);
+}
+
+// The next product's RMSNorm handed over (GE_RESID with norm_out): bf16(x *
+// gain) and the sum of x^2 over the warp's 32 consecutive columns.  Every lane
+// of the warp calls it for the same row; `ok` is false after a time-out.
+__device__ __forceinline__ void norm_handover(const GemmEpi& e, int n, int m, float x, bool ok, int lane) {
+  if (ok)
+    reinterpret_cast<bf16*>(e.norm_out)[(size_t)n * e.ldo + m] =
+        __float2bfloat16_rn(x * __bfloat162float(reinterpret_cast<const bf16*>(e.norm_gain)[m]));
+  float t = x * x;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  if (ok && lane == 0) e.norm_ssq[(size_t)n * (e.ldo >> 5) + (m >> 5)] = t;
+}
+
 // RoPE / KV-cache epilogue of output (n, m) with the row's position and the
 // cos/sin of this column's frequency at that position already at hand.
 __device__ __forceinline__ void gemm_epi_rope(const GemmEpi& e, int n, int m, float v, float partner, int pos,
@@ -135,16 +164,9 @@ __device__ __forceinline__ void gemm_epi(const GemmEpi& e, int n, int m, float v
     case GE_F32:
       reinterpret_cast<float*>(e.out)[(size_t)n * e.ldo + m] = v;
       break;
-    case GE_RESID: {
-      float* px = reinterpret_cast<float*>(e.out) + (size_t)n * e.ldo + m;
-      const float x = *px + v;
-      *px = x;
-      if (e.cap_mask)
-        for (int s = 0; s < 5; ++s)
-          if (e.cap_mask & (1 << s))
-            reinterpret_cast<bf16*>(e.hcap)[(size_t)n * 5 * e.cap_H + (size_t)s * e.cap_H + m] = __float2bfloat16_rn(x);
+    case GE_RESID:
+      resid_store(e, n, m, reinterpret_cast<const float*>(e.out)[(size_t)n * e.ldo + m] + v);
       break;
-    }
     case GE_STORE:
       reinterpret_cast<bf16*>(e.out)[(size_t)n * e.ldo + m] = __float2bfloat16_rn(v);
       break;
@@ -213,6 +235,7 @@ __global__ void __launch_bounds__(128)
   float* pre_x = reinterpret_cast<float*>(pre);
   float2* pre_cs = reinterpret_cast<float2*>(pre);
   int* pre_pos = reinterpret_cast<int*>(tail + 192);  // [4], after the barriers and flags
+  float* rsc = reinterpret_cast<float*>(tail + C::TAIL + C::PRE);  // [rows] 1 / rms of a fused RMSNorm
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = (int)cluster_rank();  // split index
@@ -272,12 +295,12 @@ __global__ void __launch_bounds__(128)
       }
     }
     __syncwarp();
-  } else if (warp >= 2 && pf) {
+  } else if (warp >= 2) {
     // Idle during the main loop: fetch what the epilogue will need for this
     // CTA's rows, so no row waits on global memory there.
     const int gt = threadIdx.x - 64;
-    pdl_wait();
-    for (int j = 0; j * S + r < rows; ++j) {
+    if (pf || epi.in_ssq) pdl_wait();
+    for (int j = 0; pf && j * S + r < rows; ++j) {
       const int n = r + j * S;
       if (epi.kind == GE_RESID) {
         const float2 v = *reinterpret_cast<const float2*>(reinterpret_cast<const float*>(epi.out) +
@@ -292,6 +315,20 @@ __global__ void __launch_bounds__(128)
         if (gt == 0) pre_pos[j] = skip ? -1 : pos;
         pre_cs[j * 64 + gt] =
             (rpos >= 0 && rpos < epi.capacity) ? epi.rope[(size_t)rpos * 64 + gt] : make_float2(1.f, 0.f);
+      }
+    }
+    if (epi.in_ssq) {
+      // a fused RMSNorm: each of this CTA's rows' 1 / rms from its 32-column sums of squares, added in
+      // column order per lane and then over a fixed butterfly (the same value in every CTA)
+      const int nw = epi.in_cols >> 5;
+      for (int n = r + (warp - 2) * S; n < rows; n += 2 * S) {
+        const float* sp = epi.in_ssq + (size_t)n * nw;
+        float t = 0.f;
+#pragma unroll 4
+        for (int c = lane; c < nw; c += 32) t += sp[c];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0) rsc[n] = 1.0f / sqrtf(t / (float)epi.in_cols + epi.in_eps);
       }
     }
   } else if (warp == 1) {
@@ -343,6 +380,10 @@ __global__ void __launch_bounds__(128)
       if (c * 16 >= rows) break;  // uniform
       float v[16];
       tmem_ld16(trow + c * 16, v);
+      if (epi.in_ssq) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= rsc[c * 16 + i];  // rows past `rows` are never stored
+      }
       if (epi.kind == GE_RESID) {
         float* col = reinterpret_cast<float*>(epi.out) + m0 + ml;
         float old[16];
@@ -352,15 +393,11 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int n = c * 16 + i;
-          if (n < rows && !flags[0]) {
-            const float x = old[i] + v[i];
-            col[(size_t)n * epi.ldo] = x;
-            if (epi.cap_mask)
-              for (int c5 = 0; c5 < 5; ++c5)
-                if (epi.cap_mask & (1 << c5))
-                  reinterpret_cast<bf16*>(epi.hcap)[(size_t)n * 5 * epi.cap_H + (size_t)c5 * epi.cap_H + m0 + ml] =
-                      __float2bfloat16_rn(x);
-          }
+          if (n >= rows) break;  // uniform over the CTA
+          const float x = old[i] + v[i];
+          const bool ok = !flags[0];
+          if (ok) resid_store(epi, n, m0 + ml, x);
+          if (epi.norm_out) norm_handover(epi, n, m0 + ml, x, ok, lane);
         }
       } else {
 #pragma unroll
@@ -409,24 +446,30 @@ __global__ void __launch_bounds__(128)
           if (rope) pacc += ld_dsmem(base + poff);
         }
     }
+    if (epi.in_ssq) {
+      acc *= rsc[n];
+      pacc *= rsc[n];
+    }
+    const bool ok = !flags[0];
     if (pf) {  // operands already in shared memory
       const int j = (n - r) / S;
-      if (flags[0]) continue;
       if (epi.kind == GE_RESID) {
         const float x = pre_x[j * 128 + ml] + acc;
-        reinterpret_cast<float*>(epi.out)[(size_t)n * epi.ldo + m0 + ml] = x;
-        if (epi.cap_mask)
-          for (int c5 = 0; c5 < 5; ++c5)
-            if (epi.cap_mask & (1 << c5))
-              reinterpret_cast<bf16*>(epi.hcap)[(size_t)n * 5 * epi.cap_H + (size_t)c5 * epi.cap_H + m0 + ml] =
-                  __float2bfloat16_rn(x);
-      } else if (pre_pos[j] >= 0) {
+        if (ok) resid_store(epi, n, m0 + ml, x);
+        if (epi.norm_out) norm_handover(epi, n, m0 + ml, x, ok, lane);
+      } else if (ok && pre_pos[j] >= 0) {
         gemm_epi_rope(epi, n, m0 + ml, acc, pacc, pre_pos[j], pre_cs[j * 64 + (ml & 63)], status);
       }
       continue;
     }
+    if (epi.kind == GE_RESID && epi.norm_out) {
+      const float x = reinterpret_cast<const float*>(epi.out)[(size_t)n * epi.ldo + m0 + ml] + acc;
+      if (ok) resid_store(epi, n, m0 + ml, x);
+      norm_handover(epi, n, m0 + ml, x, ok, lane);
+      continue;
+    }
     const float partner = rope ? pacc : __shfl_xor_sync(0xffffffffu, acc, 1);
-    if (!flags[0]) gemm_epi(epi, n, m0 + ml, acc, partner, status);
+    if (ok) gemm_epi(epi, n, m0 + ml, acc, partner, status);
   }
   cluster_sync();  // no CTA leaves while its partial may still be read
   if (warp == 2) {

@@ -54,6 +54,19 @@ struct GemmEpi {
   void* kc;
   void* vc;
   size_t layer_stride, seq_stride, head_stride;
+  // GE_RESID, nullable: the next product's RMSNorm handed over -- the new
+  // residual x also leaves as bf16(x * norm_gain) in norm_out [rows][ldo] (that
+  // product's operand) and as sums of x^2 over each 32 consecutive columns in
+  // norm_ssq [rows][ldo / 32]
+  const void* norm_gain;
+  void* norm_out;
+  float* norm_ssq;
+  // Any kind, nullable: this product's operand is such a bf16(x * gain); each
+  // row's result is scaled by 1 / sqrt(sum(x^2) / in_cols + in_eps), the sum
+  // taken over in_ssq [rows][in_cols / 32] in column order, before the epilogue
+  const float* in_ssq;
+  int in_cols;
+  float in_eps;
 };
 
 // bf16 weight product on tcgen05 with cluster split-K (M % 128 == 0, K % 64 == 0, rows <= 128).
@@ -105,6 +118,9 @@ cudaError_t gemm_simt(const float* X, int ldx, int rows, const float* W, int M, 
 bool gemm_shape_ok(int dtype, int M, int K);
 
 // Row-wise RMSNorm: y = T(x * 1/sqrt(mean(x^2)+eps) * g).
+// The first normed product's operand bf16(x * g) [rows][H] and the sums of x^2
+// over each 32 consecutive columns [rows][H / 32] (bf16; H % 32 == 0).
+cudaError_t norm_prep(const float* x, const void* g, void* xg, float* ssq, int rows, int H, cudaStream_t s);
 cudaError_t rmsnorm(int dtype, const float* x, const void* g, void* y, int rows, int H, float eps,
                     cudaStream_t s);
 // Copy T(x) into column block `slot` of hcap [rows][5H].

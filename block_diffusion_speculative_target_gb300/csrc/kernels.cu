@@ -50,6 +50,31 @@ cudaError_t rmsnorm(int dtype, const float* x, const void* g, void* y, int rows,
   return cudaGetLastError();
 }
 
+// One CTA per row; warp w of pass k covers columns 256 k + 32 w .. + 31, so each
+// warp sum is one 32-column slice.
+__global__ void __launch_bounds__(256) norm_prep_kernel(const float* __restrict__ x, const bf16* __restrict__ g,
+                                                        bf16* __restrict__ xg, float* __restrict__ ssq, int H) {
+  const float* xr = x + (size_t)blockIdx.x * H;
+  pdl_launch();
+  pdl_wait();
+  for (int i = threadIdx.x; i < H; i += 256) {
+    const float v = xr[i];
+    xg[(size_t)blockIdx.x * H + i] = __float2bfloat16_rn(v * __bfloat162float(g[i]));
+    float t = v * v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if ((threadIdx.x & 31) == 0) ssq[(size_t)blockIdx.x * (H >> 5) + (i >> 5)] = t;
+  }
+}
+
+cudaError_t norm_prep(const float* x, const void* g, void* xg, float* ssq, int rows, int H, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (H % 32) return cudaErrorInvalidValue;
+  DFL_RET(launch_pdl(norm_prep_kernel, dim3(rows), dim3(256), 0, s, x, (const bf16*)g, (bf16*)xg, ssq, H));
+  count_launch();
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ capture
 template <typename T>
 __global__ void capture_kernel(const float* __restrict__ x, T* __restrict__ hcap, int H, int slot) {

@@ -27,10 +27,11 @@ Sources (page titles as printed on the pages):
 Precision.  ``rounding="none"`` keeps every intermediate in float64 (used for
 the fp32 configuration).  ``rounding="bf16"`` rounds to bfloat16 (round to
 nearest even) exactly at the storage points the bf16 configuration defines:
-every matrix-product input that is an activation (normed hidden states,
-attention output, SwiGLU output, captured hidden states, fused feature), the
-query/key/value entries that attention consumes (after RoPE), and nothing
-else; residual stream and logits stay float64.
+every matrix-product input that is an activation (the gain-weighted hidden
+state entering a normed product -- see ``norm_linear`` --, attention output,
+SwiGLU output, captured hidden states, fused feature), the query/key/value
+entries that attention consumes (after RoPE), and nothing else; residual
+stream and logits stay float64.
 
 Parity pins: every function here is pinned by a test under ``tests/`` against
 values the pages print, closed forms, invariants or brute force.  The one
@@ -166,6 +167,25 @@ def linear(x, w):
     return f64(x) @ f64(w).T
 
 
+def norm_linear(x, gain, eps, ws, rnd):
+    """The products of RMSNorm(x) * gain with each matrix of ``ws`` (the
+    pre-norm sub-layers and the LM head, [DD] §2.2).
+
+    Exactly, RMSNorm(x) * gain = r * (x * gain) with the row scale
+    r = 1 / sqrt(mean(x^2) + eps), so each product equals r * ((x * gain) W^T).
+    With bf16 rounding the operand that is stored and enters the products is
+    x * gain rounded to bf16, and r (from the unrounded x) scales the
+    products' results; without rounding the normed rows are formed first and
+    the arithmetic is plain ``rmsnorm`` then ``linear``."""
+    if rnd.mode == "none":
+        h = rmsnorm(x, gain, eps)
+        return [linear(h, w) for w in ws]
+    x = f64(x)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    hg = rnd(x * f64(gain))
+    return [linear(hg, w) * r for w in ws]
+
+
 def silu(x):
     x = f64(x)
     return x / (1.0 + np.exp(-x))
@@ -263,10 +283,10 @@ def decoder_layer(x, lw: Layer, shape: Shape, ctx_k, ctx_v, pos0, causal, rnd):
     n = x.shape[0]
     d, nq, nkv = shape.head_dim, shape.n_q, shape.n_kv
     pos = pos0 + np.arange(n)
-    h = rnd(rmsnorm(x, lw.attn_norm, shape.eps))
-    q = rope(linear(h, lw.wq).reshape(n, nq, d), pos, shape.rope_theta)
-    k = rope(linear(h, lw.wk).reshape(n, nkv, d), pos, shape.rope_theta)
-    v = linear(h, lw.wv).reshape(n, nkv, d)
+    yq, yk, yv = norm_linear(x, lw.attn_norm, shape.eps, (lw.wq, lw.wk, lw.wv), rnd)
+    q = rope(yq.reshape(n, nq, d), pos, shape.rope_theta)
+    k = rope(yk.reshape(n, nkv, d), pos, shape.rope_theta)
+    v = yv.reshape(n, nkv, d)
     q, k, v = rnd(q), rnd(k), rnd(v)
     P = ctx_k.shape[1]
     allowed = np.ones((n, P + n), dtype=bool)
@@ -281,8 +301,8 @@ def decoder_layer(x, lw: Layer, shape: Shape, ctx_k, ctx_v, pos0, causal, rnd):
         o[:, hq] = attention(q[:, hq], keys, vals, allowed)
     o = rnd(o.reshape(n, nq * d))
     x = f64(x) + linear(o, lw.wo)
-    h2 = rnd(rmsnorm(x, lw.ffn_norm, shape.eps))
-    a = rnd(silu(linear(h2, lw.w_gate)) * linear(h2, lw.w_up))
+    yg, yu = norm_linear(x, lw.ffn_norm, shape.eps, (lw.w_gate, lw.w_up), rnd)
+    a = rnd(silu(yg) * yu)
     x = x + linear(a, lw.w_down)
     return x, k, v
 
@@ -320,8 +340,7 @@ def target_forward(tg: Target, tokens, cache: KV, rnd, keep_logits=True):
         if li in tg.capture:
             caps[li] = rnd(x)
     hcap = np.concatenate([caps[i] for i in tg.capture], axis=-1)
-    z = rnd(rmsnorm(x, tg.final_norm, sh.eps))
-    logits = linear(z, tg.lm_head)
+    logits = norm_linear(x, tg.final_norm, sh.eps, (tg.lm_head,), rnd)[0]
     am, gap = argmax_top2(logits)
     return TargetOut(am, gap, logits if keep_logits else None, hcap, new_k, new_v)
 
@@ -389,8 +408,7 @@ def draft_logits(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rnd
     x = f64(tg.embed)[toks]
     for li, lw in enumerate(dr.layers):
         x, _, _ = decoder_layer(x, lw, sh, dcache.k[li][:, lo:], dcache.v[li][:, lo:], P, False, rnd)
-    z = rnd(rmsnorm(x, dr.final_norm, sh.eps))
-    return linear(z[1:], tg.lm_head)
+    return norm_linear(x[1:], dr.final_norm, sh.eps, (tg.lm_head,), rnd)[0]
 
 
 def draft_forward(dr: Draft, tg: Target, anchor: int, block: int, dcache: KV, rnd, window: int = 0):
@@ -630,10 +648,10 @@ def target_forward_tree(tg: Target, tree: Tree, cache: KV, rnd):
     x = f64(tg.embed)[tokens]
     caps, new_k, new_v = {}, [], []
     for li, lw in enumerate(tg.layers):
-        h = rnd(rmsnorm(x, lw.attn_norm, sh.eps))
-        q = rnd(rope(linear(h, lw.wq).reshape(n, nq, d), pos, sh.rope_theta))
-        k = rnd(rope(linear(h, lw.wk).reshape(n, nkv, d), pos, sh.rope_theta))
-        v = rnd(linear(h, lw.wv).reshape(n, nkv, d))
+        yq, yk, yv = norm_linear(x, lw.attn_norm, sh.eps, (lw.wq, lw.wk, lw.wv), rnd)
+        q = rnd(rope(yq.reshape(n, nq, d), pos, sh.rope_theta))
+        k = rnd(rope(yk.reshape(n, nkv, d), pos, sh.rope_theta))
+        v = rnd(yv.reshape(n, nkv, d))
         allowed = np.concatenate([np.ones((n, P), dtype=bool), allowed_block], axis=1)
         group = nq // nkv
         o = np.zeros((n, nq, d))
@@ -644,16 +662,15 @@ def target_forward_tree(tg: Target, tree: Tree, cache: KV, rnd):
             o[:, hq] = attention(q[:, hq], keys, vals, allowed)
         o = rnd(o.reshape(n, nq * d))
         x = x + linear(o, lw.wo)
-        h2 = rnd(rmsnorm(x, lw.ffn_norm, sh.eps))
-        a = rnd(silu(linear(h2, lw.w_gate)) * linear(h2, lw.w_up))
+        yg, yu = norm_linear(x, lw.ffn_norm, sh.eps, (lw.w_gate, lw.w_up), rnd)
+        a = rnd(silu(yg) * yu)
         x = x + linear(a, lw.w_down)
         new_k.append(k)
         new_v.append(v)
         if li in tg.capture:
             caps[li] = rnd(x)
     hcap = np.concatenate([caps[i] for i in tg.capture], axis=-1)
-    z = rnd(rmsnorm(x, tg.final_norm, sh.eps))
-    logits = linear(z, tg.lm_head)
+    logits = norm_linear(x, tg.final_norm, sh.eps, (tg.lm_head,), rnd)[0]
     am, gap = argmax_top2(logits)
     return TargetOut(am, gap, logits, hcap, new_k, new_v)
 

@@ -85,6 +85,38 @@ def test_rmsnorm_closed_forms():
     assert np.allclose(O.rmsnorm(np.ones((1, 4)), np.ones(4), 3.0), 0.5)
 
 
+def test_norm_linear_rounding_point():
+    """The normed products: without rounding they are rmsnorm then linear; with
+    bf16 rounding the stored operand is bf16(x * gain) and the row's 1/rms
+    scales the results."""
+    rng = np.random.default_rng(7)
+    H, M, eps = 64, 24, 1e-6
+    none, bf = O.Rounder("none"), O.Rounder("bf16")
+    x = rng.standard_normal((3, H)) * 3
+    g = 1 + 0.1 * rng.standard_normal(H)
+    W = rng.standard_normal((M, H)) * 0.1
+    assert np.allclose(O.norm_linear(x, g, eps, (W,), none)[0], O.linear(O.rmsnorm(x, g, eps), W),
+                       rtol=1e-13, atol=1e-13)
+    # x * g exactly representable in bf16 (small integers times powers of two): the bf16 reading
+    # then rounds nothing and equals the exact normed product -- it would not if the normed row
+    # (x * g / rms) were the rounded quantity
+    xi = rng.integers(-40, 41, (3, H)).astype(np.float64)
+    gp = 2.0 ** rng.integers(-2, 3, H)
+    exact = O.linear(O.rmsnorm(xi, gp, eps), W)
+    assert np.allclose(O.norm_linear(xi, gp, eps, (W,), bf)[0], exact, rtol=1e-12, atol=1e-12)
+    assert not np.array_equal(O.round_bf16(O.rmsnorm(xi, gp, eps)), O.rmsnorm(xi, gp, eps))
+    # otherwise the operand is rounded: with the identity matrix, result / (1/rms) is bf16(x * g)
+    y = O.norm_linear(x, g, eps, (np.eye(H),), bf)[0]
+    rms = np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    assert np.allclose(y * rms, O.round_bf16(x * g), rtol=1e-14, atol=0)
+    assert not np.allclose(y * rms, x * g, rtol=1e-6, atol=0)
+    # several matrices share the operand and the scale
+    W2 = rng.standard_normal((5, H))
+    a, b = O.norm_linear(x, g, eps, (W, W2), bf)
+    assert np.array_equal(a, O.norm_linear(x, g, eps, (W,), bf)[0])
+    assert np.allclose(b, O.linear(y, W2), rtol=1e-12, atol=1e-12)
+
+
 def test_linear_hand_values():
     x = np.array([[1.0, 2.0, 3.0]])
     w = np.array([[1.0, 0.0, -1.0], [2.0, 1.0, 0.5]])    # [out=2, in=3]
