@@ -89,6 +89,7 @@ class Target:
     final_norm: np.ndarray
     lm_head: np.ndarray
     capture: tuple
+    kv_format: str = "bf16"   # the target's K/V cache: "bf16" or "q8" (``kv_q8_store``)
 
 
 @dataclass
@@ -135,6 +136,49 @@ class Rounder:
 
     def __call__(self, x):
         return round_bf16(x) if self.mode == "bf16" else f64(x)
+
+
+def round_f16(x):
+    """Round to IEEE half precision, nearest even (NumPy's float16 conversion:
+    11 significant bits, largest finite 65504)."""
+    with np.errstate(over="ignore"):
+        return f64(np.asarray(x, dtype=np.float64).astype(np.float16))
+
+
+# ---------------------------------------------------------------------------
+# 8-bit K/V cache
+# ---------------------------------------------------------------------------
+# The pages run the target's cache quantised ([DD] §8.3 "显存优化" 方案3, a
+# 3-bit KV cache; the tutorial's llama.cpp runs, §5 and §7, with 5-bit keys
+# and 4-bit values) but print no format.  Reading: "q8" keeps each cached
+# key or value row of head_dim entries as 8-bit integers q in [-127, 127]
+# with one float32 scale s per row (per position and KV head), the entry
+# being q * s.  A row is quantised from its float32 value (the key after
+# RoPE): s = max|x| / 127 and q = round-half-even(x / s), both in float32
+# arithmetic; a row of zeros keeps s = 0.  Every row the target writes --
+# the block's own rows included -- is stored this way before attention reads
+# it, and the query enters attention in IEEE half precision.
+
+
+def quantize_q8(x):
+    """Quantise rows (last axis) to (q int8, s float32) as stated above."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1, keepdims=True)
+    s = amax / np.float32(127.0)
+    safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    t = np.where(s > 0, x32 / safe, np.float32(0.0)).astype(np.float32)
+    q = np.clip(np.rint(t), -127, 127).astype(np.int8)
+    return q, s[..., 0].astype(np.float32)
+
+
+def dequantize_q8(q, s):
+    """The stored entries q * s (float64, exact)."""
+    return np.asarray(q, dtype=np.float64) * np.asarray(s, dtype=np.float64)[..., None]
+
+
+def kv_q8_store(x):
+    """What a q8 cache holds for the rows x: dequantize_q8(quantize_q8(x))."""
+    return dequantize_q8(*quantize_q8(x))
 
 
 # ---------------------------------------------------------------------------
@@ -269,7 +313,18 @@ class KV:
 # ---------------------------------------------------------------------------
 
 
-def decoder_layer(x, lw: Layer, shape: Shape, ctx_k, ctx_v, pos0, causal, rnd):
+def store_qkv(q, k, v, rnd, kv_format):
+    """The query, keys and values as attention consumes them: rounded at the
+    bf16 storage points, or (``kv_format`` "q8") keys and values through the
+    8-bit cache and the query in half precision."""
+    if kv_format == "q8":
+        if rnd.mode != "bf16":
+            raise ValueError("the 8-bit cache belongs to the bf16 configuration")
+        return round_f16(q), kv_q8_store(k), kv_q8_store(v)
+    return rnd(q), rnd(k), rnd(v)
+
+
+def decoder_layer(x, lw: Layer, shape: Shape, ctx_k, ctx_v, pos0, causal, rnd, kv_format="bf16"):
     """Pre-norm decoder layer on the rows x [n, H] at positions pos0..pos0+n-1.
 
     Keys/values attended: the context ctx_k/ctx_v [n_kv, P, d] (positions
@@ -277,6 +332,10 @@ def decoder_layer(x, lw: Layer, shape: Shape, ctx_k, ctx_v, pos0, causal, rnd):
     context and rows 0..j (target verification, [DD] §1.2).  Otherwise every
     row sees the context and every row (the drafter's in-block bidirectional
     attention, [DD] §2.2 "块内双向注意力").
+
+    ``kv_format`` "q8" (bf16 rounding only): the rows' keys and values are
+    stored in the 8-bit cache (``kv_q8_store``) and read back from it, and
+    the query enters attention in half precision.
 
     Returns the new residual rows and the rows' (rounded) keys/values
     [n, n_kv, d] that a cache would append."""
@@ -287,7 +346,7 @@ def decoder_layer(x, lw: Layer, shape: Shape, ctx_k, ctx_v, pos0, causal, rnd):
     q = rope(yq.reshape(n, nq, d), pos, shape.rope_theta)
     k = rope(yk.reshape(n, nkv, d), pos, shape.rope_theta)
     v = yv.reshape(n, nkv, d)
-    q, k, v = rnd(q), rnd(k), rnd(v)
+    q, k, v = store_qkv(q, k, v, rnd, kv_format)
     P = ctx_k.shape[1]
     allowed = np.ones((n, P + n), dtype=bool)
     if causal:
@@ -334,7 +393,7 @@ def target_forward(tg: Target, tokens, cache: KV, rnd, keep_logits=True):
     caps = {}
     new_k, new_v = [], []
     for li, lw in enumerate(tg.layers):
-        x, k, v = decoder_layer(x, lw, sh, cache.k[li], cache.v[li], P, True, rnd)
+        x, k, v = decoder_layer(x, lw, sh, cache.k[li], cache.v[li], P, True, rnd, tg.kv_format)
         new_k.append(k)
         new_v.append(v)
         if li in tg.capture:
@@ -649,9 +708,8 @@ def target_forward_tree(tg: Target, tree: Tree, cache: KV, rnd):
     caps, new_k, new_v = {}, [], []
     for li, lw in enumerate(tg.layers):
         yq, yk, yv = norm_linear(x, lw.attn_norm, sh.eps, (lw.wq, lw.wk, lw.wv), rnd)
-        q = rnd(rope(yq.reshape(n, nq, d), pos, sh.rope_theta))
-        k = rnd(rope(yk.reshape(n, nkv, d), pos, sh.rope_theta))
-        v = rnd(yv.reshape(n, nkv, d))
+        q, k, v = store_qkv(rope(yq.reshape(n, nq, d), pos, sh.rope_theta),
+                            rope(yk.reshape(n, nkv, d), pos, sh.rope_theta), yv.reshape(n, nkv, d), rnd, tg.kv_format)
         allowed = np.concatenate([np.ones((n, P), dtype=bool), allowed_block], axis=1)
         group = nq // nkv
         o = np.zeros((n, nq, d))

@@ -718,3 +718,92 @@ def test_planted_rope_sign_breaks_rotation():
 
     y = bad(q, [3], 1e6)
     assert not np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(q, axis=-1))
+
+
+# ---------------------------------------------------------------- 8-bit K/V cache
+
+
+def test_round_f16_hand_cases():
+    one = 1.0
+    assert O.round_f16(one + 2.0 ** -11) == one                      # tie -> even
+    assert O.round_f16(one + 3 * 2.0 ** -11) == one + 2.0 ** -9      # tie -> even (upwards)
+    assert O.round_f16(one + 2.0 ** -11 + 2.0 ** -20) == one + 2.0 ** -10
+    assert O.round_f16(65504.0) == 65504.0 and np.isinf(O.round_f16(65520.0))
+    assert O.round_f16(-0.1) == -O.round_f16(0.1)
+
+
+def test_q8_quantizer_pins():
+    d = 128
+    # a row whose largest entry is 127: s = 1 and the codes are the entries rounded half to even
+    x = np.zeros(d)
+    x[:7] = [127.0, 1.0, -0.5, 0.5, 1.5, -2.5, -126.6]
+    q, s = O.quantize_q8(x)
+    assert s == 1.0 and q[:7].tolist() == [127, 1, 0, 0, 2, -2, -127]
+    # a row of zeros keeps s = 0 and codes 0
+    q0, s0 = O.quantize_q8(np.zeros((2, d)))
+    assert np.all(q0 == 0) and np.all(s0 == 0)
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((50, d)) * rng.uniform(0.01, 100.0, (50, 1))
+    q, s = O.quantize_q8(x)
+    assert q.dtype == np.int8 and s.dtype == np.float32 and s.shape == (50,)
+    # the largest magnitude of a row maps to +-127; every entry within half a step of its float32 value
+    assert np.all(np.max(np.abs(q.astype(int)), axis=1) == 127)
+    x32 = x.astype(np.float32).astype(np.float64)
+    assert np.all(np.abs(O.dequantize_q8(q, s) - x32) <= s[:, None].astype(np.float64) * (0.5 + 1e-6))
+    # scaling a row by a power of two scales s and keeps the codes
+    q2, s2 = O.quantize_q8(x * 8.0)
+    assert np.array_equal(q2, q) and np.array_equal(s2, s * np.float32(8))
+    # rows that are already integers times a power of two round-trip exactly
+    qi = rng.integers(-127, 128, (5, d))
+    qi[:, 3] = -127
+    si = 2.0 ** -rng.integers(0, 10, 5).astype(float)
+    q3, s3 = O.quantize_q8(qi * si[:, None])
+    assert np.array_equal(q3, qi) and np.array_equal(s3, si)
+    assert np.array_equal(O.kv_q8_store(qi * si[:, None]), qi * si[:, None])
+
+
+def _q8_small():
+    wl = shrink(synth.WORKLOADS["small-bf16-gqa4"], n_layers=4, vocab=1024)
+    w = synth.host_weights(wl.target, wl.draft_layers, wl.dtype)
+    tg, dr = oracle_models(wl, w)
+    import dataclasses
+    return wl, dataclasses.replace(tg, kv_format="q8"), dr
+
+
+def test_q8_block_forward_equals_row_by_row():
+    """The block's own keys and values go through the 8-bit cache before
+    attention reads them: a causal forward of n rows equals n one-row
+    forwards that each read the earlier rows back from the cache."""
+    wl, tg, _ = _q8_small()
+    rnd = O.Rounder("bf16")
+    toks = synth.prompt_tokens(12, wl.target.vocab)
+    sh = tg.shape
+    c1 = O.KV.empty(sh.n_layers, sh.n_kv, sh.head_dim)
+    o1 = O.target_forward(tg, toks, c1, rnd)
+    c2 = O.KV.empty(sh.n_layers, sh.n_kv, sh.head_dim)
+    rows = []
+    for t in toks:
+        o = O.target_forward(tg, [t], c2, rnd)
+        O.commit(c2, o, 1)
+        rows.append(o.logits[0])
+    assert np.allclose(o1.logits, np.array(rows), rtol=0, atol=1e-9)
+    # the cached entries are 8-bit codes times one scale per row
+    k = c2.k[1][0]
+    q, s = O.quantize_q8(k)
+    assert np.array_equal(O.dequantize_q8(q, s), k)
+    # and differ from the bf16 configuration's keys (the quantisation is not a no-op)
+    import dataclasses
+    ob = O.target_forward(dataclasses.replace(tg, kv_format="bf16"), toks, O.KV.empty(sh.n_layers, sh.n_kv, sh.head_dim),
+                          rnd)
+    assert not np.allclose(ob.new_k[1], o1.new_k[1], atol=1e-6)
+
+
+def test_lossless_q8_cache():
+    wl, tg, dr = _q8_small()
+    rnd = O.Rounder("bf16")
+    prompt = synth.prompt_tokens(40, wl.target.vocab)
+    n = 20
+    ref, _ = O.greedy_ar(tg, prompt, n + wl.block, rnd)
+    k, r = synth.acceptance_draws(32, wl.target.vocab)
+    out, steps = O.spec_decode(tg, dr, prompt, n, wl.block, rnd, forcing=(k[:, 0], r[:, 0]), ref=ref)
+    assert np.array_equal(out, ref[:n])
