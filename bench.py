@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the CPU-baseline sample")
-    ap.add_argument("--also", nargs="*", default=["dense27b-36k"],
+    ap.add_argument("--also", nargs="*", default=["dense27b-36k", "dense27b-36k-q8"],
                     help="further workloads measured after the main one (one GPU only); empty to skip")
     return ap.parse_args()
 
@@ -91,10 +91,18 @@ def step_bytes(wl: synth.Workload, P_mean: float, batch=1):
     Wl = layer_weight_bytes(s)
     lm = 2 * s.vocab * s.hidden
     fc = 2 * s.hidden * 5 * s.hidden
-    kv_pos = 2 * 2 * s.n_kv * s.head_dim  # K and V, bf16, per layer per position
     weights = s.n_layers * Wl + lm + wl.draft_layers * Wl + lm + fc
-    kv = batch * (s.n_layers + wl.draft_layers) * P_mean * kv_pos
+    kv = batch * P_mean * (s.n_layers * kv_pos_bytes(wl, target=True) + wl.draft_layers * kv_pos_bytes(wl, False))
     return weights + kv, weights, kv
+
+
+def kv_pos_bytes(wl: synth.Workload, target: bool):
+    """Keys and values of one layer at one position: bf16, or (the target's
+    8-bit cache) one byte per entry plus a float32 scale per row."""
+    s = wl.target
+    if target and wl.kv == "q8":
+        return 2 * s.n_kv * (s.head_dim + 4)
+    return 2 * 2 * s.n_kv * s.head_dim
 
 
 def stage_bytes(wl: synth.Workload, P_mean: float, batch=1):
@@ -107,11 +115,11 @@ def stage_bytes(wl: synth.Workload, P_mean: float, batch=1):
     s = wl.target
     Wl = layer_weight_bytes(s)
     lm = 2 * s.vocab * s.hidden
-    kv_pos = 2 * 2 * s.n_kv * s.head_dim
     return {"fuse": 2 * s.hidden * 5 * s.hidden,
             "inject": 0,
-            "draft": wl.draft_layers * Wl + lm + batch * wl.draft_layers * P_mean * kv_pos,
-            "teacher": 0, "verify": s.n_layers * Wl + lm + batch * s.n_layers * P_mean * kv_pos, "accept": 0}
+            "draft": wl.draft_layers * Wl + lm + batch * wl.draft_layers * P_mean * kv_pos_bytes(wl, False),
+            "teacher": 0,
+            "verify": s.n_layers * Wl + lm + batch * s.n_layers * P_mean * kv_pos_bytes(wl, True), "accept": 0}
 
 
 # ---------------------------------------------------------------------------
@@ -410,14 +418,14 @@ def measure_ours(wl: synth.Workload, args, dist: Dist) -> dict:
     prompts = [synth.prompt_tokens(P, V, stream=1000 * dist.rank + b) for b, P in enumerate(lens0)]
 
     # the speculative session: prefill (target forward over the prompts, fusion and injection)
-    sess = Session(m, batch=nb, capacity=cap, block=B, stream_cap=n_ref + 8)
+    sess = Session(m, batch=nb, capacity=cap, block=B, stream_cap=n_ref + 8, kv_format=wl.kv)
     sess.prefill(prompts)
     torch.cuda.synchronize()
     t_prefill = time.perf_counter() - t_setup
 
     # greedy AR reference stream from the same committed state (and the plain
     # AR decode rate on this GPU)
-    ar = Session(m, batch=nb, capacity=cap, block=B, with_draft=False, stream_cap=n_ref + 8)
+    ar = Session(m, batch=nb, capacity=cap, block=B, with_draft=False, stream_cap=n_ref + 8, kv_format=wl.kv)
     ar.copy_target_from(sess)
     ar.ar_step()
     g_ar = ar.capture_graph(ar.ar_step)
@@ -570,7 +578,7 @@ def measure_ours(wl: synth.Workload, args, dist: Dist) -> dict:
         "config": {"workload": wl.name, "batch": nb, "block": B,
                    "context": lens0[0] if nb == 1 else lens0, "context_mean_timed": P_mean,
                    "target_layers": s.n_layers, "draft_layers": wl.draft_layers, "hidden": s.hidden,
-                   "vocab": V, "parallelism": f"replicas{dist.world}",
+                   "vocab": V, "target_kv": wl.kv, "parallelism": f"replicas{dist.world}",
                    "l2": "inputs larger than L2 (weights+KV read per step >> 129 MB)", "graph": "one CUDA graph per step"},
         "tau": tau,
         "bytes_per_step": bytes_step, "weight_bytes_per_step": w_bytes, "kv_bytes_per_step": kv_bytes,

@@ -18,6 +18,7 @@ F32 = 0
 BF16 = 1
 
 ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED_SHAPE = -2
 ERR_TOO_LARGE = -5
 ARGMAX_NOALLOC_MAX_ROWS = 128
 
@@ -59,6 +60,10 @@ _SIGS = {
     "dflash_strerror": (ctypes.c_char_p, [_I]),
     "dflash_capture_layers": (_I, [_I, POINTER(c_int32)]),
     "dflash_cache_alloc": (_I, [POINTER(ModelDesc), _I, _I, _I, POINTER(c_void_p)]),
+    "dflash_cache_alloc_ex": (_I, [POINTER(ModelDesc), _I, _I, _I, _I, POINTER(c_void_p)]),
+    "dflash_cache_kv_format": (_I, [_P]),
+    "dflash_cache_read_q8": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "dflash_cache_copy": (_I, [_P, _P, _P]),
     "dflash_cache_free": (_I, [_P]),
     "dflash_cache_view": (_I, [_P, _I, _I, POINTER(c_void_p)]),
     "dflash_cache_lengths": (c_void_p, [_P]),
@@ -158,6 +163,29 @@ def dflash_cache_alloc(desc: ModelDesc, n_layers, batch, capacity):
     _check(load().dflash_cache_alloc(ctypes.byref(desc), n_layers, batch, capacity, ctypes.byref(h)),
            "dflash_cache_alloc")
     return h.value
+
+
+KV_MODEL, KV_Q8 = 0, 1
+
+
+def dflash_cache_alloc_ex(desc: ModelDesc, n_layers, batch, capacity, kv_format):
+    h = c_void_p()
+    _check(load().dflash_cache_alloc_ex(ctypes.byref(desc), n_layers, batch, capacity, kv_format, ctypes.byref(h)),
+           "dflash_cache_alloc_ex")
+    return h.value
+
+
+def dflash_cache_kv_format(cache):
+    return load().dflash_cache_kv_format(cache)
+
+
+def dflash_cache_read_q8(cache, layer, seq, pos0, n, k_codes, v_codes, k_scales, v_scales, stream=None):
+    _check(load().dflash_cache_read_q8(cache, layer, seq, pos0, n, _ptr(k_codes), _ptr(v_codes), _ptr(k_scales),
+                                       _ptr(v_scales), _stream(stream)), "dflash_cache_read_q8")
+
+
+def dflash_cache_copy(dst, src, stream=None):
+    _check(load().dflash_cache_copy(dst, src, _stream(stream)), "dflash_cache_copy")
 
 
 def dflash_cache_free(cache):

@@ -28,6 +28,9 @@ struct dflash_cache {
   int32_t total_batch;    // sequences of the allocation (views share it)
   int32_t seq_base;       // first sequence of this view
   int32_t attn_gtiles;    // 128-key tiles per attention partial (fixed for the cache's life)
+  int32_t kv_format;      // DFLASH_KV_MODEL or DFLASH_KV_Q8
+  float* ks;              // q8: row scales [layer][seq][kv_head][capacity] (null otherwise)
+  float* vs;
 };
 
 static KvMaps kv_maps(const dflash_cache* c, int layer) {
@@ -35,6 +38,11 @@ static KvMaps kv_maps(const dflash_cache* c, int layer) {
   m.k = c->tk;
   m.v = c->tv;
   m.row0 = ((long long)layer * c->total_batch + c->seq_base) * c->n_kv * c->capacity;
+  m.q8 = c->kv_format == DFLASH_KV_Q8;
+  // the scales of the whole allocation (row0 indexes them like the maps' rows)
+  const size_t back = (size_t)c->seq_base * c->n_kv * c->capacity;
+  m.ks = c->ks ? c->ks - back : nullptr;
+  m.vs = c->vs ? c->vs - back : nullptr;
   return m;
 }
 
@@ -130,8 +138,20 @@ int dflash_capture_layers(int32_t n_layers, int32_t out[5]) {
 // ------------------------------------------------------------------ caches
 int dflash_cache_alloc(const dflash_model_desc* d, int32_t n_layers, int32_t batch, int32_t capacity,
                        dflash_cache** out) {
+  return dflash_cache_alloc_ex(d, n_layers, batch, capacity, DFLASH_KV_MODEL, out);
+}
+
+int32_t dflash_cache_kv_format(const dflash_cache* c) { return c ? c->kv_format : -1; }
+
+int dflash_cache_alloc_ex(const dflash_model_desc* d, int32_t n_layers, int32_t batch, int32_t capacity,
+                          int32_t kv_format, dflash_cache** out) {
   REQ(out && desc_ok(d) && n_layers > 0 && batch > 0 && capacity > 0);
+  REQ(kv_format == DFLASH_KV_MODEL || kv_format == DFLASH_KV_Q8);
   *out = nullptr;
+  const bool q8 = kv_format == DFLASH_KV_Q8;
+  if (q8 && (d->dtype != DFLASH_BF16 || d->head_dim != 128)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
+  // q8: rows of scales are fetched in 128-row copies that start 16-byte aligned
+  if (q8) capacity = (capacity + 7) & ~7;
   dflash_cache* c = new dflash_cache();
   c->n_layers = n_layers;
   c->batch = batch;
@@ -139,33 +159,44 @@ int dflash_cache_alloc(const dflash_model_desc* d, int32_t n_layers, int32_t bat
   c->n_kv = d->n_kv_heads;
   c->head_dim = d->head_dim;
   c->dtype = d->dtype;
-  c->elem = dtype_size(d->dtype);
+  c->kv_format = kv_format;
+  c->elem = q8 ? 1 : dtype_size(d->dtype);
   c->head_stride = (size_t)capacity * d->head_dim;
   c->seq_stride = c->head_stride * d->n_kv_heads;
   c->layer_stride = c->seq_stride * batch;
   c->owns = true;
   const size_t bytes = c->layer_stride * n_layers * c->elem;
+  const size_t sbytes = q8 ? c->layer_stride / d->head_dim * n_layers * sizeof(float) : 0;
   const int half = d->head_dim / 2;
   if (cudaMalloc(&c->k, bytes) != cudaSuccess || cudaMalloc(&c->v, bytes) != cudaSuccess ||
       cudaMalloc(&c->len, sizeof(int32_t) * batch) != cudaSuccess ||
-      cudaMalloc(&c->rope, sizeof(float2) * (size_t)capacity * half) != cudaSuccess) {
+      cudaMalloc(&c->rope, sizeof(float2) * (size_t)capacity * half) != cudaSuccess ||
+      (q8 && (cudaMalloc(&c->ks, sbytes) != cudaSuccess || cudaMalloc(&c->vs, sbytes) != cudaSuccess))) {
     cudaGetLastError();
     cudaFree(c->k);
     cudaFree(c->v);
     cudaFree(c->len);
     cudaFree(c->rope);
+    cudaFree(c->ks);
+    cudaFree(c->vs);
     delete c;
     return DFLASH_ERR_OOM;
   }
   cudaMemset(c->len, 0, sizeof(int32_t) * batch);
-  cudaMemset(c->k, 0, bytes);  // every position holds a finite value from the start
-  cudaMemset(c->v, 0, bytes);
+  // every position holds a finite value from the start (q8: codes 128 with scale 0, i.e. zeros)
+  cudaMemset(c->k, q8 ? 128 : 0, bytes);
+  cudaMemset(c->v, q8 ? 128 : 0, bytes);
+  if (q8) {
+    cudaMemset(c->ks, 0, sbytes);
+    cudaMemset(c->vs, 0, sbytes);
+  }
   c->total_batch = batch;
   c->seq_base = 0;
   c->has_maps = false;
   c->attn_gtiles = attn_group_tiles(capacity, d->n_kv_heads);
   if (d->dtype == DFLASH_BF16 && d->head_dim == 128) {
-    if (!make_kv_maps(c->k, c->v, (long long)n_layers * batch * d->n_kv_heads * capacity, &c->tk, &c->tv)) {
+    const long long rows = (long long)n_layers * batch * d->n_kv_heads * capacity;
+    if (!(q8 ? make_kv_maps_q8(c->k, c->v, rows, &c->tk, &c->tv) : make_kv_maps(c->k, c->v, rows, &c->tk, &c->tv))) {
       dflash_cache_free(c);
       return DFLASH_ERR_CUDA;
     }
@@ -194,6 +225,10 @@ int dflash_cache_view(dflash_cache* c, int32_t seq_begin, int32_t seq_count, dfl
   v->k = c->k + (size_t)seq_begin * c->seq_stride * c->elem;
   v->v = c->v + (size_t)seq_begin * c->seq_stride * c->elem;
   v->len = c->len + seq_begin;
+  if (c->ks) {
+    v->ks = c->ks + (size_t)seq_begin * c->seq_stride / c->head_dim;
+    v->vs = c->vs + (size_t)seq_begin * c->seq_stride / c->head_dim;
+  }
   v->batch = seq_count;
   v->seq_base = c->seq_base + seq_begin;
   v->owns = false;
@@ -208,6 +243,8 @@ int dflash_cache_free(dflash_cache* c) {
     cudaFree(c->v);
     cudaFree(c->len);
     cudaFree(c->rope);
+    cudaFree(c->ks);
+    cudaFree(c->vs);
   }
   delete c;
   return DFLASH_OK;
@@ -228,6 +265,12 @@ static int cache_copy(dflash_cache* c, int32_t layer, int32_t seq, int32_t pos0,
       pos0 + n <= c->capacity);
   const size_t es = c->elem;
   const size_t off = ((size_t)layer * c->layer_stride + (size_t)seq * c->seq_stride + (size_t)pos0 * c->head_dim) * es;
+  if (c->kv_format == DFLASH_KV_Q8) {
+    REQ(to_cache);  // the codes are read with dflash_cache_read_q8
+    const size_t soff = off / c->head_dim;
+    CK(kv_quant_write(k, v, c->n_kv, n, c->k + off, c->v + off, c->ks + soff, c->vs + soff, c->head_stride, s));
+    return DFLASH_OK;
+  }
   const size_t pitch_cache = c->head_stride * es, width = (size_t)n * c->head_dim * es;
   for (int t = 0; t < 2; ++t) {
     uint8_t* cbase = (t == 0 ? c->k : c->v) + off;
@@ -248,6 +291,46 @@ int dflash_cache_write(dflash_cache* c, int32_t layer, int32_t seq, int32_t pos0
 int dflash_cache_read(dflash_cache* c, int32_t layer, int32_t seq, int32_t pos0, int32_t n, void* k, void* v,
                       dflash_stream_t stream) {
   return cache_copy(c, layer, seq, pos0, n, k, v, false, (cudaStream_t)stream);
+}
+
+int dflash_cache_read_q8(dflash_cache* c, int32_t layer, int32_t seq, int32_t pos0, int32_t n, void* k_codes,
+                         void* v_codes, float* k_scales, float* v_scales, dflash_stream_t stream) {
+  REQ(c && c->kv_format == DFLASH_KV_Q8 && layer >= 0 && layer < c->n_layers && seq >= 0 && seq < c->batch &&
+      pos0 >= 0 && n > 0 && pos0 + n <= c->capacity);
+  REQ((k_codes != nullptr) == (v_codes != nullptr) && (k_scales != nullptr) == (v_scales != nullptr));
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t row = (size_t)layer * c->layer_stride / c->head_dim + (size_t)seq * c->seq_stride / c->head_dim + pos0;
+  const size_t rows_per_head = c->head_stride / c->head_dim;  // = capacity
+  if (k_codes) {
+    const size_t w = (size_t)n * c->head_dim;
+    CK(cudaMemcpy2DAsync(k_codes, w, c->k + row * c->head_dim, c->head_stride, w, c->n_kv, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpy2DAsync(v_codes, w, c->v + row * c->head_dim, c->head_stride, w, c->n_kv, cudaMemcpyDeviceToDevice, s));
+  }
+  if (k_scales) {
+    const size_t w = (size_t)n * sizeof(float);
+    CK(cudaMemcpy2DAsync(k_scales, w, c->ks + row, rows_per_head * sizeof(float), w, c->n_kv, cudaMemcpyDeviceToDevice,
+                         s));
+    CK(cudaMemcpy2DAsync(v_scales, w, c->vs + row, rows_per_head * sizeof(float), w, c->n_kv, cudaMemcpyDeviceToDevice,
+                         s));
+  }
+  return DFLASH_OK;
+}
+
+int dflash_cache_copy(dflash_cache* dst, const dflash_cache* src, dflash_stream_t stream) {
+  REQ(dst && src && dst != src && dst->owns && src->owns && dst->n_layers == src->n_layers &&
+      dst->batch == src->batch && dst->capacity == src->capacity && dst->n_kv == src->n_kv &&
+      dst->head_dim == src->head_dim && dst->dtype == src->dtype && dst->kv_format == src->kv_format);
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t bytes = dst->layer_stride * dst->n_layers * dst->elem;
+  CK(cudaMemcpyAsync(dst->k, src->k, bytes, cudaMemcpyDeviceToDevice, s));
+  CK(cudaMemcpyAsync(dst->v, src->v, bytes, cudaMemcpyDeviceToDevice, s));
+  if (dst->ks) {
+    const size_t sb = dst->layer_stride / dst->head_dim * dst->n_layers * sizeof(float);
+    CK(cudaMemcpyAsync(dst->ks, src->ks, sb, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(dst->vs, src->vs, sb, cudaMemcpyDeviceToDevice, s));
+  }
+  CK(cudaMemcpyAsync(dst->len, src->len, sizeof(int32_t) * dst->batch, cudaMemcpyDeviceToDevice, s));
+  return DFLASH_OK;
 }
 
 int dflash_cache_set_lengths(dflash_cache* c, const int32_t* host_len, int32_t n, dflash_stream_t stream) {
@@ -455,6 +538,11 @@ static GemmEpi epi_cache(int kind, void* out, int ldo, dflash_cache* c, int laye
   e.layer_stride = c->layer_stride;
   e.seq_stride = c->seq_stride;
   e.head_stride = c->head_stride;
+  if (c->kv_format == DFLASH_KV_Q8) {
+    e.kv_q8 = 1;
+    e.ks = c->ks + (size_t)layer * c->layer_stride / c->head_dim;
+    e.vs = c->vs + (size_t)layer * c->layer_stride / c->head_dim;
+  }
   return e;
 }
 
@@ -618,6 +706,7 @@ int dflash_fuse_features(const dflash_draft* dr, const void* hcap, int32_t rows,
 int dflash_inject_kv(const dflash_draft* dr, const void* fused, int32_t batch, int32_t rows_per_seq,
                      int32_t* n_pend, dflash_cache* dc, dflash_workspace* ws, dflash_stream_t stream) {
   REQ(dr && fused && n_pend && ws && desc_ok(&dr->d) && dr->w_kv_all);
+  if (dc && dc->kv_format != DFLASH_KV_MODEL) return DFLASH_ERR_UNSUPPORTED_SHAPE;  // the drafter's cache
   const dflash_model_desc& d = dr->d;
   REQ(cache_matches(dc, d, d.n_layers) && batch > 0 && batch <= dc->batch && rows_per_seq > 0 &&
       batch * rows_per_seq <= ws->max_rows);
@@ -649,6 +738,7 @@ int dflash_draft_block(const dflash_draft* dr, const dflash_target* tg, const in
   REQ(d.hidden == tg->d.hidden && d.vocab == tg->d.vocab && d.dtype == tg->d.dtype);
   REQ(block >= 2 && block <= 16 && batch > 0 && batch * block <= ws->max_rows);
   REQ(cache_matches(dc, d, d.n_layers) && batch <= dc->batch && dc->capacity <= ws->max_ctx);
+  if (dc->kv_format != DFLASH_KV_MODEL) return DFLASH_ERR_UNSUPPORTED_SHAPE;  // the drafter's cache
   REQ(dr->mask_id >= 0 && dr->mask_id < d.vocab && dr->cross_ctx >= 0);
   cudaStream_t s = (cudaStream_t)stream;
   const int rows = batch * block, H = d.hidden;
@@ -755,6 +845,7 @@ int target_verify_tree(const dflash_target* tg, const int32_t* tree_tokens, cons
   if (!desc_shapes_ok(&d)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
   REQ(batch > 0 && n >= 1 && n <= 64 && batch * n <= ws->max_rows);
   REQ(cache_matches(tc, d, d.n_layers) && batch <= tc->batch && tc->capacity <= ws->max_ctx);
+  if (tc->kv_format != DFLASH_KV_MODEL) return DFLASH_ERR_UNSUPPORTED_SHAPE;
   for (int i = 0; i < 5; ++i) REQ(tg->capture[i] >= 0 && tg->capture[i] < d.n_layers);
   cudaStream_t s = (cudaStream_t)cuda_stream;
   CK(embed(d.dtype, tg->embed, d.vocab, d.hidden, tree_tokens, nullptr, 0, batch, n, 0, nullptr, ws->x, ws->status, s));
@@ -772,6 +863,7 @@ int dflash_accept_tree(const dflash_target* tg, const int32_t* tree_tokens, cons
   REQ(tg && tree_tokens && tree_parent && argmax_in && tc && anchor && n_pend && ws && desc_ok(&tg->d));
   REQ(batch > 0 && batch <= tc->batch && n >= 1 && n <= 64 && batch * n <= ws->max_rows);
   REQ(cache_matches(tc, tg->d, tg->d.n_layers));
+  if (tc->kv_format != DFLASH_KV_MODEL) return DFLASH_ERR_UNSUPPORTED_SHAPE;
   REQ(!stream || (stream_len && stream_cap > 0));
   cudaStream_t s = (cudaStream_t)cuda_stream;
   CK(accept_tree(tree_tokens, tree_parent, argmax_in, batch, n, tc->len, anchor, n_pend, accept_len, stream,

@@ -205,6 +205,23 @@ bool make_kv_maps(const void* k, const void* v, long long rows_total, CUtensorMa
   return true;
 }
 
+// 8-bit caches: codes [rows][128] uint8 in unswizzled 128-key boxes (the
+// converter warps read them row by row).
+bool make_kv_maps_q8(const void* k, const void* v, long long rows_total, CUtensorMap* mk, CUtensorMap* mv) {
+  const PFN_encodeTiled_t fn = encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows_total};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t es[2] = {1, 1};
+  for (int i = 0; i < 2; ++i)
+    if (fn(i == 0 ? mk : mv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(i == 0 ? k : v), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  return true;
+}
+
 int attn_group_tiles(int capacity, int nkv) {
   // units of one sequence at full capacity ~ the SM count: tiles = cap/128 * nkv / SMs,
   // rounded to the nearest power of two

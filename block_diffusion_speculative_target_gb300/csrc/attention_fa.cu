@@ -59,6 +59,25 @@ struct FaLayout {
   static constexpr int kSmem = kBar + 256 + 1024;                           // + alignment slack
   static_assert(G > 5 || 16 * G * 128 + 2048 <= 16384, "exchange must fit in the query tile's padding rows");
 };
+
+// 8-bit caches (G <= 5): a 2-stage ring of byte tiles as the TMA lands them
+// (key codes, value codes, then their 128 key and 128 value scales), a
+// 2-stage ring of the fp16 operand tiles the converter warps build from them
+// (same layout as the bf16 ring's stages), the query tile, and in the query
+// tile's padding rows the maxima exchange and the barriers.  227 KB in all.
+template <int G>
+struct FaLayoutQ8 {
+  static constexpr uint32_t kU8Stage = 2 * 16384 + 2 * 512;
+  static constexpr uint32_t kF = 2 * kU8Stage;                  // fp16 ring, 2 x kStageBytes
+  static constexpr uint32_t kQ = kF + 2 * kStageBytes;
+  static constexpr uint32_t kXch = kQ + 16 * G * 128;           // half 0 padding: exchange, 2 KB
+  static constexpr uint32_t kBar = kQ + 16384 + 16 * G * 128;   // half 1 padding: barriers, TMEM slot, abort
+  static constexpr int kSmem = kQ + 32768 + 1024;
+  // (G > 5 leaves no padding rows: the launcher refuses 8-bit caches there)
+  static_assert(G > 5 || 16 * G * 128 + 2048 <= 16384, "the exchange must fit in the padding rows");
+  static_assert(kF % 1024 == 0 && kQ % 1024 == 0, "operand tiles are 1024-byte aligned");
+  static_assert(kSmem <= 232448, "shared memory per block");
+};
 constexpr uint64_t kFaWaitNs = 500000000ull;
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -120,29 +139,51 @@ __device__ __forceinline__ uint64_t smem_desc_mn(uint32_t addr, uint32_t block_s
 }
 }  // namespace
 
-template <int G>
+// Q8: the cache holds 8-bit codes u = q + 128 with a float32 scale per key or
+// value row, and the products run in IEEE half precision.  The converter
+// warps (those whose TMEM lane quarter holds only padding rows) turn each
+// byte tile into half operands: a byte permute places u under the exponent
+// of 1024 (the half 1024 + u, exact), a subtraction of 1152 leaves q, and a
+// multiplication by the row's scale rounded to half gives the entry
+// round(q * half(s)).  Keys are converted as soon as the products of two
+// tiles before are past them (their S exists), values once that tile's
+// P V is done, each released on its own barrier, so neither waits on the
+// other.  The query arrives in half precision, P is a half hi/lo pair, and
+// the softmax is the bf16 path's.
+template <int G, bool Q8>
 __global__ void __launch_bounds__(kFaThreads, 1)
     attn_fa_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, int batch, int n, int nq, int nkv, int causal, int window,
                    long long row0, int capacity, int gtiles, int ngroups, const int32_t* __restrict__ len,
-                   const uint64_t* __restrict__ tree_mask, float* __restrict__ part_o, float* __restrict__ part_ml,
+                   const uint64_t* __restrict__ tree_mask, const float* __restrict__ kscale,
+                   const float* __restrict__ vscale, float* __restrict__ part_o, float* __restrict__ part_ml,
                    float scale_log2, int* status) {
-  using Ly = FaLayout<G>;
-  constexpr int kStages = Ly::kStages;
-  constexpr uint32_t kQ = Ly::kQ;
+  constexpr int kStages = Q8 ? 2 : FaLayout<G>::kStages;
+  constexpr uint32_t kQ = Q8 ? FaLayoutQ8<G>::kQ : FaLayout<G>::kQ;
+  constexpr uint32_t kXchOff = Q8 ? FaLayoutQ8<G>::kXch : FaLayout<G>::kXch;
+  constexpr uint32_t kBarOff = Q8 ? FaLayoutQ8<G>::kBar : FaLayout<G>::kBar;
+  // TMEM lane quarters holding real rows; in Q8 the warps of the others convert
+  constexpr int kLiveQ = (16 * G + 31) / 32 < 4 ? (16 * G + 31) / 32 : 4;
+  constexpr int kSoftWarps = Q8 ? 2 * kLiveQ : 8;  // warps that arrive on p_full / xch_full
+  constexpr int kConvWarps = 8 - 2 * kLiveQ;
+  static_assert(!Q8 || kConvWarps >= 2, "the 8-bit path needs padding quarters for its converter warps");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Ly::kBar);
-  float* xch = reinterpret_cast<float*>(sm + Ly::kXch);  // [2][2][128] row maxima of each half
-  uint64_t* kv_full = bar;        // [3] a tile's keys and values landed
-  uint64_t* kv_empty = bar + 3;   // [3] its products completed
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kBarOff);
+  float* xch = reinterpret_cast<float*>(sm + kXchOff);  // [2][2][128] row maxima of each half
+  uint64_t* kv_full = bar;        // [kStages] a tile's operands ready (bf16: landed; Q8: converted)
+  uint64_t* kv_empty = bar + 3;   // [kStages] its products completed
   uint64_t* q_full = bar + 6;
   uint64_t* s_full = bar + 7;     // [2] S_t in TMEM
   uint64_t* p_full = bar + 9;     // [2] P_t in TMEM (one arrival per softmax warp)
   uint64_t* pv_done = bar + 11;   // [2] O += P_t V_t completed
   uint64_t* drain = bar + 13;     // every issued product completed
   uint64_t* xch_full = bar + 14;  // [2] both halves' maxima written (one arrival per softmax warp)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
+  // Q8: the byte ring's key half and value half land and are released separately
+  uint64_t* u8_full = bar + 16;   // Q8 [2] a tile's key codes and scales landed ([kv * 2 + s], kv = 0)
+  uint64_t* u8_empty = bar + 20;  // Q8 [2] converted (one arrival per converter warp; [kv * 2 + s])
+  uint64_t* vf_full = bar + 24;   // Q8 [2] a tile's values converted (kv_full: its keys)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 26);
   volatile int* abort_f = reinterpret_cast<volatile int*>(tslot + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Set-up that needs nothing from the previous kernel (barriers, TMEM, the
@@ -152,15 +193,22 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_full[i], Q8 ? kConvWarps : 1);
       mbar_init(&kv_empty[i], 1);
+      if (Q8) {
+        for (int kv = 0; kv < 2; ++kv) {
+          mbar_init(&u8_full[kv * 2 + i], 1);
+          mbar_init(&u8_empty[kv * 2 + i], kConvWarps);
+        }
+        mbar_init(&vf_full[i], kConvWarps);
+      }
     }
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 8);
+      mbar_init(&p_full[i], kSoftWarps);
       mbar_init(&pv_done[i], 1);
-      mbar_init(&xch_full[i], 8);
+      mbar_init(&xch_full[i], kSoftWarps);
     }
     mbar_init(drain, 1);
     *abort_f = 0;
@@ -197,8 +245,12 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
     return;
   }
+  const int q4w = warp & 3;
+  const bool live = q4w * 32 < 16 * G;  // softmax warps: the quarter holds real rows
+  const bool conv = Q8 && warp >= 2 && !live;
 
-  int issued = 0;  // producer: tiles whose copies were issued
+  int issued = 0;    // producer: tiles whose copies were issued (Q8: key halves)
+  int issued_v = 0;  // Q8: value halves
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -207,28 +259,53 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       for (int dh = 0; dh < 2; ++dh)
         tma_load_3d(sm + kQ + dh * 16384, &tmQ, q_full, dh * 64, hk * G, b * n + rb * 16);
       const int rowb = (int)(row0 + ((long long)b * nkv + hk) * capacity);
-      for (int t = 0; t < nt; ++t) {
-        const int s = t % kStages;
-        if (t >= kStages && !mbar_wait(&kv_empty[s], (uint32_t)((t / kStages) - 1) & 1u, kFaWaitNs)) {
-          *abort_f = 1;
-          set_status(status, DFLASH_STATUS_TIMEOUT);
-          break;
+      if constexpr (Q8) {
+        // key halves and value halves in the converters' order: keys of tile t, then values of t - 1
+        for (int t = 0; t <= nt && !*abort_f; ++t)
+          for (int kv = 0; kv < 2; ++kv) {
+            const int tt = t - kv;
+            if (tt < 0 || tt >= nt) continue;
+            const int s = tt & 1, bi = kv * 2 + s;
+            if (tt >= 2 && !mbar_wait(&u8_empty[bi], (uint32_t)((tt >> 1) - 1) & 1u, kFaWaitNs)) {
+              *abort_f = 1;
+              set_status(status, DFLASH_STATUS_TIMEOUT);
+              break;
+            }
+            const int key0 = rowb + (ta + tt) * 128;
+            uint8_t* st = sm + s * FaLayoutQ8<G>::kU8Stage;
+            mbar_arrive_expect_tx(&u8_full[bi], 16384 + 512);
+            tma_load_2d(st + kv * 16384, kv == 0 ? &tmK : &tmV, &u8_full[bi], 0, key0);
+            bulk_load(st + 32768 + kv * 512, (kv == 0 ? kscale : vscale) + key0, 512, &u8_full[bi]);
+            if (kv == 0)
+              issued = tt + 1;
+            else
+              issued_v = tt + 1;
+          }
+      } else {
+        for (int t = 0; t < nt; ++t) {
+          const int s = t % kStages;
+          if (t >= kStages && !mbar_wait(&kv_empty[s], (uint32_t)((t / kStages) - 1) & 1u, kFaWaitNs)) {
+            *abort_f = 1;
+            set_status(status, DFLASH_STATUS_TIMEOUT);
+            break;
+          }
+          if (*abort_f) break;
+          const int key0 = rowb + (ta + t) * 128;
+          uint8_t* st = sm + s * kStageBytes;
+          mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
+          for (int dh = 0; dh < 2; ++dh) tma_load_2d(st + dh * 16384, &tmK, &kv_full[s], dh * 64, key0);
+          for (int dh = 0; dh < 2; ++dh) tma_load_2d(st + kTileBytes + dh * 16384, &tmV, &kv_full[s], dh * 64, key0);
+          issued = t + 1;
         }
-        if (*abort_f) break;
-        uint8_t* st = sm + s * kStageBytes;
-        const int key0 = rowb + (ta + t) * 128;
-        mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
-        for (int dh = 0; dh < 2; ++dh) tma_load_2d(st + dh * 16384, &tmK, &kv_full[s], dh * 64, key0);
-        for (int dh = 0; dh < 2; ++dh) tma_load_2d(st + kTileBytes + dh * 16384, &tmV, &kv_full[s], dh * 64, key0);
-        issued = t + 1;
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ products
     if (lane == 0) {
-      const uint32_t idS = idesc_bf16_f32(128, 128);
-      const uint32_t idO = idesc_bf16_f32(128, 128) | (1u << 16);  // B (values) MN-major
+      const uint32_t idS = Q8 ? idesc_f16_f32(128, 128) : idesc_bf16_f32(128, 128);
+      const uint32_t idO = idS | (1u << 16);  // B (values) MN-major
+      const uint32_t kOps = Q8 ? FaLayoutQ8<G>::kF : 0u;  // the operand ring
       bool ok = mbar_wait(q_full, 0, kFaWaitNs);
       for (int t = 0; ok && t <= nt; ++t) {
         if (t < nt) {  // S_t = Q K_t^T into S[t & 1], once P_{t-2} (same buffer) has been consumed
@@ -237,7 +314,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           if (ok && t >= 2) ok = mbar_wait(&pv_done[sb], (uint32_t)((t - 2) >> 1) & 1u, kFaWaitNs);
           if (!ok || *abort_f) break;
           tc_fence_after();
-          const uint8_t* kt = sm + s * kStageBytes;
+          const uint8_t* kt = sm + kOps + s * kStageBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const int dh = kk >> 2;
@@ -250,9 +327,10 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         if (t >= 1) {  // O += P_hi V + P_lo V for tile t-1 (P of key half j at columns 64 j: hi, then lo)
           const int w = t - 1, wb = w & 1, s = w % kStages;
           ok = mbar_wait(&p_full[wb], (uint32_t)(w >> 1) & 1u, kFaWaitNs);
+          if (Q8 && ok) ok = mbar_wait(&vf_full[s], (uint32_t)(w / kStages) & 1u, kFaWaitNs);
           if (!ok || *abort_f) break;
           tc_fence_after();
-          const uint32_t vt = smem_u32(sm + s * kStageBytes + kTileBytes);
+          const uint32_t vt = smem_u32(sm + kOps + s * kStageBytes + kTileBytes);
 #pragma unroll
           for (int pass = 0; pass < 2; ++pass)
 #pragma unroll
@@ -270,13 +348,81 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       tc_commit(drain);  // arrives once every product issued above has completed
     }
     __syncwarp();
+  } else if (conv) {
+    // ------------------------------------------------------------ Q8: byte tiles -> fp16 operands
+    if constexpr (Q8) {
+      int cidx = 0;  // this warp's rank among the converter warps
+      for (int w = 2; w < warp; ++w) cidx += (w & 3) * 32 >= 16 * G;
+      const int ct = cidx * 32 + lane, nct = kConvWarps * 32;
+      const int ch = ct & 7, row0 = ct >> 3, rstep = nct >> 3;
+      const int sw = row0 & 7, d0 = (((ch & 3) * 2) ^ sw) << 4, d1 = (((ch & 3) * 2 + 1) ^ sw) << 4;
+      const __half2 off2 = __float2half2_rn(1152.f);
+      // jobs in deadline order: keys of tile t (needed by its Q K^T) before the values of tile t-1
+      // (needed only after tile t-1's softmax)
+      auto convert = [&](int kv, int t) -> bool {
+        const int s = t & 1;
+        const uint8_t* src = sm + s * FaLayoutQ8<G>::kU8Stage;
+        uint8_t* dst = sm + FaLayoutQ8<G>::kF + s * kStageBytes;
+        const float* scales = reinterpret_cast<const float*>(src + 32768);  // [128 keys | 128 values]
+        // keys: the stage's previous keys are free once that tile's S exists; values: once its P V is done
+        bool ok = mbar_wait(&u8_full[kv * 2 + s], (uint32_t)(t >> 1) & 1u, kFaWaitNs);
+        if (ok && t >= 2)
+          ok = kv == 0 ? mbar_wait(&s_full[s], (uint32_t)((t - 2) >> 1) & 1u, kFaWaitNs)
+                       : mbar_wait(&kv_empty[s], (uint32_t)((t - 2) >> 1) & 1u, kFaWaitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (__any_sync(0xffffffffu, !ok || *abort_f)) {
+          if (!ok) {
+            *abort_f = 1;
+            set_status(status, DFLASH_STATUS_TIMEOUT);
+          }
+          return false;
+        }
+        // this thread's 16-byte chunks: rows row0 + i * rstep, entries 16 ch .. + 15 (rstep is a multiple
+        // of 8, so every row keeps the same swizzle phase)
+        const uint8_t* sp = src + kv * 16384 + row0 * 128 + ch * 16;
+        uint8_t* dp = dst + kv * kTileBytes + (ch >> 2) * 16384 + row0 * 128;
+        const float* scp = scales + kv * 128 + row0;
+#pragma unroll 4
+        for (int row = row0; row < 128; row += rstep) {
+          const uint4 w = *reinterpret_cast<const uint4*>(sp);
+          const __half2 sc2 = __half2half2(__float2half_rn(*scp));
+          const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int j2 = 0; j2 < 4; ++j2) {
+            const uint32_t lo = __byte_perm(in[j2], 0x64646464u, 0x4140);  // halves 1024 + u of bytes 0, 1
+            const uint32_t hi = __byte_perm(in[j2], 0x64646464u, 0x4342);  // bytes 2, 3
+            const __half2 a = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&lo), off2), sc2);
+            const __half2 b = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&hi), off2), sc2);
+            o[2 * j2] = *reinterpret_cast<const uint32_t*>(&a);
+            o[2 * j2 + 1] = *reinterpret_cast<const uint32_t*>(&b);
+          }
+          // half tile: 64-entry half ch >> 2, 16-byte chunks 2 (ch & 3) and + 1, 128-byte swizzle
+          *reinterpret_cast<uint4*>(dp + d0) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(dp + d1) = make_uint4(o[4], o[5], o[6], o[7]);
+          sp += rstep * 128;
+          dp += rstep * 128;
+          scp += rstep;
+        }
+        fence_proxy_async_smem();  // the tensor cores read the tiles through the async proxy
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(kv == 0 ? &kv_full[s] : &vf_full[s]);
+          mbar_arrive(&u8_empty[kv * 2 + s]);
+        }
+        return true;
+      };
+      for (int t = 0; t <= nt; ++t) {
+        if (t < nt && !convert(0, t)) break;
+        if (t >= 1 && !convert(1, t - 1)) break;
+      }
+    }
   } else {
     // ------------------------------------------------------------ softmax
-    const int q4 = warp & 3, h = (warp - 2) >> 2;
+    const int q4 = q4w, h = (warp - 2) >> 2;
     const int r = q4 * 32 + lane;
     const int ri = r / G;
     const int qi = rb * 16 + ri;
-    const bool live = q4 * 32 < 16 * G;  // warp-uniform: the quarter holds real rows
     const bool row_ok = r < 16 * G && qi < n;
     const int lim = row_ok ? min(causal ? P + qi + 1 : P + n, capacity) : 0;  // visible keys [lo, lim)
     // tree verification: block key P + i is visible only when bit i is set (the node's ancestors)
@@ -287,7 +433,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     const uint32_t obase = tmem + lrow + 256 + h * 64;  // this half's 64 output columns
     float M = -INFINITY, Lh = 0.f;
     bool ok = true;
-    for (int t = 0; t < nt; ++t) {
+    for (int t = 0; ok && t < nt; ++t) {
       const int sb = t & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (uint32_t)(t >> 1) & 1u, kFaWaitNs));
       if (__any_sync(0xffffffffu, !ok || *abort_f)) break;  // warp-uniform
@@ -337,26 +483,34 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           }
         }
         const float negm = Mn == -INFINITY ? 0.f : -Mn;
+        const float sl = scale_log2;
         float lt = 0.f;
         uint32_t hi[32], lo_[32];
+        // p of entries 2e, 2e+1 into the row sum and the P hi/lo pair (bf16, or half for Q8)
+        auto emit = [&](int e, float p0, float p1) {
+          lt += p0;
+          lt += p1;
+          if constexpr (Q8) {
+            const __half2 hh = __floats2half2_rn(p0, p1);
+            const float2 hf = __half22float2(hh);
+            const __half2 ll = __floats2half2_rn(p0 - hf.x, p1 - hf.y);
+            hi[e] = *reinterpret_cast<const uint32_t*>(&hh);
+            lo_[e] = *reinterpret_cast<const uint32_t*>(&ll);
+          } else {
+            pack_bf16_hilo(p0, p1, hi[e], lo_[e]);
+          }
+        };
+        // two separately unrolled loops: the common one has no per-entry test, so the
+        // exponentials of different entries overlap freely
         if (wfull) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm));
-            const float p1 = ex2f(fmaf(__uint_as_float(v[2 * e + 1]), scale_log2, negm));
-            lt += p0;
-            lt += p1;
-            pack_bf16_hilo(p0, p1, hi[e], lo_[e]);
-          }
+          for (int e = 0; e < 32; ++e)
+            emit(e, ex2f(fmaf(__uint_as_float(v[2 * e]), sl, negm)), ex2f(fmaf(__uint_as_float(v[2 * e + 1]), sl, negm)));
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float p0 = vis(2 * e) ? ex2f(fmaf(__uint_as_float(v[2 * e]), scale_log2, negm)) : 0.f;
-            const float p1 = vis(2 * e + 1) ? ex2f(fmaf(__uint_as_float(v[2 * e + 1]), scale_log2, negm)) : 0.f;
-            lt += p0;
-            lt += p1;
-            pack_bf16_hilo(p0, p1, hi[e], lo_[e]);
-          }
+          for (int e = 0; e < 32; ++e)
+            emit(e, vis(2 * e) ? ex2f(fmaf(__uint_as_float(v[2 * e]), sl, negm)) : 0.f,
+                 vis(2 * e + 1) ? ex2f(fmaf(__uint_as_float(v[2 * e + 1]), sl, negm)) : 0.f);
         }
         // every score of this half is in registers: P overwrites them (hi at +0..31, lo at +32..63)
         tmem_st16(sbase, *reinterpret_cast<const uint32_t(*)[16]>(&hi[0]));
@@ -395,14 +549,15 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       *abort_f = 1;
       set_status(status, DFLASH_STATUS_TIMEOUT);
     }
-    __syncthreads();
     // ---- the unit's partial, staged through the (dead) ring so that each
     // row leaves as one contiguous 512-byte store: row r at r * 512, its
     // 16-byte chunks XOR-swizzled by (r & 7).  Row sums of the two halves at
-    // 64 KB, row maxima after them.
+    // 64 KB, row maxima after them.  (Q8: every byte tile has been converted
+    // once the last scores exist, so the 8-bit ring is dead here too.)
     float* stg = reinterpret_cast<float*>(sm);
     float* stg_l = stg + 128 * 128;
     float* stg_m = stg_l + 256;
+    __syncthreads();
     const bool good = !*abort_f;
     if (good && live) {
       tc_fence_after();
@@ -422,7 +577,10 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     __syncthreads();
     if (good) {
       const int rows_live = min(16 * G, 128);
-      for (int rr = warp - 2; rr < rows_live; rr += 8) {
+      int srank = warp - 2;  // this warp's rank among the warps of this branch
+      if (Q8)
+        for (int w = 2; w < warp; ++w) srank -= (w & 3) * 32 >= 16 * G;
+      for (int rr = srank; rr < rows_live; rr += kSoftWarps) {
         const int ir = rr / G, hr = rr - ir * G, qr = rb * 16 + ir;
         if (qr >= n) continue;  // warp-uniform
         const size_t prow = ((size_t)(b * n + qr) * nq + hk * G + hr) * ngroups + gi;
@@ -433,16 +591,24 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       }
     }
   }
-  if (warp < 2) {  // match the softmax warps' two block-wide barriers
+  if (warp < 2 || conv) {  // match the softmax warps' two block-wide barriers
     __syncthreads();
     __syncthreads();
   }
   // ---- teardown: copies and products still in flight complete before the
   // ring and TMEM are released
   if (warp == 0 && lane == 0 && *abort_f) {
-    const int first = issued > kStages ? issued - kStages : 0;
-    for (int t = first; t < issued; ++t)
-      mbar_wait(&kv_full[t % kStages], (uint32_t)(t / kStages) & 1u, kFaWaitNs / 4);
+    if (Q8) {  // the last two halves of each kind that were issued
+      for (int kv = 0; kv < 2; ++kv) {
+        const int last = kv == 0 ? issued : issued_v;
+        for (int tt = last > 2 ? last - 2 : 0; tt < last; ++tt)
+          mbar_wait(&u8_full[kv * 2 + (tt & 1)], (uint32_t)(tt >> 1) & 1u, kFaWaitNs / 4);
+      }
+    } else {
+      const int first = issued > kStages ? issued - kStages : 0;
+      for (int t = first; t < issued; ++t)
+        mbar_wait(&kv_full[t % kStages], (uint32_t)(t / kStages) & 1u, kFaWaitNs / 4);
+    }
   }
   if (warp == 1 && lane == 0) mbar_wait(drain, 0, kFaWaitNs / 4);
   __syncwarp();
@@ -463,29 +629,36 @@ cudaError_t attention_fa(int G, const KvMaps& maps, const CUtensorMap& qmap, int
   const long long units = (long long)ngroups * nkv * batch * ((n + 15) / 16);
   if (units <= 0) return cudaSuccess;
   if (units > INT32_MAX) return cudaErrorInvalidValue;
-#define DFL_FA_CASE(GG)                                                                                         \
-  case GG: {                                                                                                     \
+  if (maps.q8 && (G > 5 || !maps.ks || !maps.vs)) return cudaErrorInvalidValue;
+#define DFL_FA_CASE(GG, QQ, LY)                                                                                  \
+  {                                                                                                              \
     static bool set = false;                                                                                     \
     if (!set) {                                                                                                  \
-      DFL_RET(cudaFuncSetAttribute(attn_fa_kernel<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize,              \
-                                   FaLayout<GG>::kSmem));                                                        \
+      DFL_RET(cudaFuncSetAttribute(attn_fa_kernel<GG, QQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,          \
+                                   LY<GG>::kSmem));                                                              \
       set = true;                                                                                                \
     }                                                                                                            \
-    DFL_RET(launch_pdl(attn_fa_kernel<GG>, dim3((unsigned)units), dim3(kFaThreads), FaLayout<GG>::kSmem, s,       \
-                       maps.k, maps.v,                                                                             \
-                       qmap, batch, n, nq, nkv, causal, window, maps.row0, capacity, gtiles, sc.nchunk, len,       \
-                       tree_mask, sc.o,                                                                            \
-                       sc.ml, scale_log2, status));                                                              \
+    DFL_RET(launch_pdl(attn_fa_kernel<GG, QQ>, dim3((unsigned)units), dim3(kFaThreads), LY<GG>::kSmem, s, maps.k, \
+                       maps.v, qmap, batch, n, nq, nkv, causal, window, maps.row0, capacity, gtiles, sc.nchunk,   \
+                       len, tree_mask, maps.ks, maps.vs, sc.o, sc.ml, scale_log2, status));                       \
     return cudaSuccess;                                                                                          \
   }
+  if (maps.q8) {
+    switch (G) {
+      case 1: DFL_FA_CASE(1, true, FaLayoutQ8)
+      case 2: DFL_FA_CASE(2, true, FaLayoutQ8)
+      case 4: DFL_FA_CASE(4, true, FaLayoutQ8)
+      case 5: DFL_FA_CASE(5, true, FaLayoutQ8)
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (G) {
-    DFL_FA_CASE(1)
-    DFL_FA_CASE(2)
-    DFL_FA_CASE(4)
-    DFL_FA_CASE(5)
-    DFL_FA_CASE(8)
-    default:
-      return cudaErrorInvalidValue;
+    case 1: DFL_FA_CASE(1, false, FaLayout)
+    case 2: DFL_FA_CASE(2, false, FaLayout)
+    case 4: DFL_FA_CASE(4, false, FaLayout)
+    case 5: DFL_FA_CASE(5, false, FaLayout)
+    case 8: DFL_FA_CASE(8, false, FaLayout)
+    default: return cudaErrorInvalidValue;
   }
 #undef DFL_FA_CASE
 }

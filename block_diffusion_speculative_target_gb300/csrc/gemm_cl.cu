@@ -157,6 +157,43 @@ __device__ __forceinline__ void gemm_epi_rope(const GemmEpi& e, int n, int m, fl
       __float2bfloat16_rn(r);
 }
 
+// GE_QKV into an 8-bit cache, output (n, m) with its RoPE partner and the
+// row's position and cos/sin at hand: the query leaves as fp16; a key or
+// value row -- the CTA's 128 columns are one head -- is quantised with
+// s = max|x| / 127 over the CTA's 128 threads (two rounds of named barrier 1
+// through `red`) and q = round-half-even(x / s), stored as q + 128 with s.
+// Every thread of the CTA calls it for the same row (the kind is uniform over
+// the CTA); `ok` is false after a time-out.
+__device__ __forceinline__ void qkv_q8_out(const GemmEpi& e, int n, int m, float v, float partner, int pos,
+                                           float2 cs, bool ok, float* red, int* status) {
+  const int t = m >> 7, ml = m & 127;
+  const int kind = t < e.nq ? 0 : (t < e.nq + e.nkv ? 1 : 2);  // 0 q, 1 k, 2 v
+  const int h = kind == 0 ? t : (kind == 1 ? t - e.nq : t - e.nq - e.nkv);
+  const float r = kind == 2 ? v : (ml < 64 ? v * cs.x - partner * cs.y : v * cs.x + partner * cs.y);
+  if (kind == 0) {
+    if (ok) reinterpret_cast<__half*>(e.out)[((size_t)n * e.nq + h) * 128 + ml] = __float2half_rn(r);
+    return;
+  }
+  float a = fabsf(r);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  const float amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  asm volatile("bar.sync 1, 128;" ::: "memory");  // `red` is rewritten for the next row
+  const float sc = __fdiv_rn(amax, 127.0f);
+  const float q = sc > 0.f ? fminf(fmaxf(rintf(__fdiv_rn(r, sc)), -127.f), 127.f) : 0.f;
+  if (!ok || pos < 0) return;
+  if (pos >= e.capacity) {
+    set_status(status, DFLASH_STATUS_CAPACITY);
+    return;
+  }
+  const int b = n / e.rows_per_seq;
+  const size_t row = (size_t)b * (e.seq_stride >> 7) + (size_t)h * (e.head_stride >> 7) + (size_t)pos;
+  reinterpret_cast<uint8_t*>(kind == 1 ? e.kc : e.vc)[row * 128 + ml] = (uint8_t)((int)q + 128);
+  if (ml == 0) (kind == 1 ? e.ks : e.vs)[row] = sc;
+}
+
 // Final value y of output (n, m): apply the epilogue.  `partner` is y[n][m^1]
 // (SwiGLU) or y[n][m^64] within the head (RoPE).
 __device__ __forceinline__ void gemm_epi(const GemmEpi& e, int n, int m, float v, float partner, int* status) {
@@ -236,6 +273,7 @@ __global__ void __launch_bounds__(128)
   float2* pre_cs = reinterpret_cast<float2*>(pre);
   int* pre_pos = reinterpret_cast<int*>(tail + 192);  // [4], after the barriers and flags
   float* rsc = reinterpret_cast<float*>(tail + C::TAIL + C::PRE);  // [rows] 1 / rms of a fused RMSNorm
+  float* red_q8 = reinterpret_cast<float*>(tail + 128);              // [4] row maxima of an 8-bit cache write
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = (int)cluster_rank();  // split index
@@ -451,6 +489,22 @@ __global__ void __launch_bounds__(128)
       pacc *= rsc[n];
     }
     const bool ok = !flags[0];
+    if (epi.kv_q8) {  // GE_QKV into an 8-bit cache
+      int pos;
+      float2 cs;
+      if (pf) {
+        const int j = (n - r) / S;
+        pos = pre_pos[j];
+        cs = pre_cs[j * 64 + (ml & 63)];
+      } else {
+        const int b = n / epi.rows_per_seq, jj = n % epi.rows_per_seq;
+        pos = epi.len[b] + jj;
+        const int rpos = epi.rope_off ? epi.len[b] + epi.rope_off[n] : pos;
+        cs = (rpos >= 0 && rpos < epi.capacity) ? epi.rope[(size_t)rpos * 64 + (ml & 63)] : make_float2(1.f, 0.f);
+      }
+      qkv_q8_out(epi, n, m0 + ml, acc, pacc, pos, cs, ok, red_q8, status);
+      continue;
+    }
     if (pf) {  // operands already in shared memory
       const int j = (n - r) / S;
       if (epi.kind == GE_RESID) {

@@ -67,6 +67,11 @@ struct GemmEpi {
   const float* in_ssq;
   int in_cols;
   float in_eps;
+  // GE_QKV with an 8-bit cache: keys/values leave as codes (kc/vc uint8) with
+  // one scale per row in ks/vs (indexed like kc / 128), the query as fp16
+  int kv_q8;
+  float* ks;
+  float* vs;
 };
 
 // bf16 weight product on tcgen05 with cluster split-K (M % 128 == 0, K % 64 == 0, rows <= 128).
@@ -153,8 +158,20 @@ struct AttnScratch {
 struct KvMaps {
   CUtensorMap k, v;
   long long row0;
+  // 8-bit caches: the maps cover uint8 codes, and ks/vs are the float32 row
+  // scales of the whole allocation, indexed by the same flattened row
+  bool q8;
+  const float* ks;
+  const float* vs;
 };
 bool make_kv_maps(const void* k, const void* v, long long rows_total, CUtensorMap* mk, CUtensorMap* mv);
+bool make_kv_maps_q8(const void* k, const void* v, long long rows_total, CUtensorMap* mk, CUtensorMap* mv);
+// Quantise rows of bf16 keys/values [n_kv][n][128] into an 8-bit cache's codes
+// (u = q + 128) and scales: k_dst/v_dst point at position pos0 of head 0
+// (head stride `head_stride` codes), ks/vs at the matching scale (stride
+// head_stride / 128).
+cudaError_t kv_quant_write(const void* k, const void* v, int n_kv, int n, uint8_t* k_dst, uint8_t* v_dst, float* ks,
+                           float* vs, size_t head_stride, cudaStream_t s);
 // window > 0: keys below len[b] - window (a cross-context window) are not attended.
 // gtiles: 128-key tiles per partial of the bf16 path (a property of the cache).
 // tree_mask (nullable, non-causal calls with n <= 64): row b*n+j sees the

@@ -75,6 +75,54 @@ cudaError_t norm_prep(const float* x, const void* g, void* xg, float* ssq, int r
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ 8-bit cache rows
+// One warp per 128-entry row (lane l: entries 4 l .. 4 l + 3): s = max|x| /
+// 127 and q = round-half-even(x / s) in float32 (IEEE division), stored as
+// u = q + 128 with the scale.  Rows 0 .. n_kv * n - 1 are keys, the next as
+// many values.
+__global__ void __launch_bounds__(256) kv_quant_write_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
+                                                             int n_kv, int n, uint8_t* __restrict__ k_dst,
+                                                             uint8_t* __restrict__ v_dst, float* __restrict__ ks,
+                                                             float* __restrict__ vs, size_t head_stride) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  pdl_launch();
+  pdl_wait();
+  if (row >= 2 * n_kv * n) return;  // warp-uniform
+  const int isv = row >= n_kv * n, r = isv ? row - n_kv * n : row;
+  const int h = r / n, j = r - h * n;
+  const bf16* src = (isv ? v : k) + (size_t)r * 128 + 4 * lane;
+  float x[4], a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[i] = __bfloat162float(src[i]);
+    a = fmaxf(a, fabsf(x[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const float sc = __fdiv_rn(a, 127.0f);
+  uchar4 u;
+  uint8_t* ub = reinterpret_cast<uint8_t*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float q = sc > 0.f ? fminf(fmaxf(rintf(__fdiv_rn(x[i], sc)), -127.f), 127.f) : 0.f;
+    ub[i] = (uint8_t)((int)q + 128);
+  }
+  const size_t crow = (size_t)h * head_stride + (size_t)j * 128;
+  *reinterpret_cast<uchar4*>((isv ? v_dst : k_dst) + crow + 4 * lane) = u;
+  if (lane == 0) (isv ? vs : ks)[crow / 128] = sc;
+}
+
+cudaError_t kv_quant_write(const void* k, const void* v, int n_kv, int n, uint8_t* k_dst, uint8_t* v_dst, float* ks,
+                           float* vs, size_t head_stride, cudaStream_t s) {
+  const int rows = 2 * n_kv * n;
+  if (rows <= 0) return cudaSuccess;
+  DFL_RET(launch_pdl(kv_quant_write_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, (const bf16*)k, (const bf16*)v, n_kv,
+                     n, k_dst, v_dst, ks, vs, head_stride));
+  count_launch();
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ capture
 template <typename T>
 __global__ void capture_kernel(const float* __restrict__ x, T* __restrict__ hcap, int H, int slot) {

@@ -135,10 +135,15 @@ class Session:
     """Caches, workspace and device state for ``batch`` sequences."""
 
     def __init__(self, model: Model, batch=1, capacity=1024, block=16, prefill_chunk=128, stream_cap=None,
-                 with_draft=True, tree_budget=0):
+                 with_draft=True, tree_budget=0, kv_format="bf16"):
         tree_n = tree_budget + 1 if tree_budget else 0
         if batch * max(block, tree_n) > 128 or prefill_chunk > 128 or tree_n > 64:
             raise ValueError("at most 128 rows per call and 64 tree nodes")
+        if kv_format not in ("bf16", "q8"):
+            raise ValueError(kv_format)
+        self.kv_format = kv_format
+        if kv_format == "q8":
+            capacity = (capacity + 7) // 8 * 8  # the 8-bit cache's capacity granularity
         self.m, self.batch, self.block, self.capacity = model, batch, block, capacity
         self.chunk = prefill_chunk
         self.stream_cap = stream_cap or capacity
@@ -147,7 +152,8 @@ class Session:
         self.ddesc = desc_of(s, model.dtype, model.draft_layers)
         dev = model.device
         tdt = _DT[model.dtype][1]
-        self.tcache = capi.dflash_cache_alloc(self.tdesc, s.n_layers, batch, capacity)
+        self.tcache = capi.dflash_cache_alloc_ex(self.tdesc, s.n_layers, batch, capacity,
+                                                 capi.KV_Q8 if kv_format == "q8" else capi.KV_MODEL)
         self.dcache = capi.dflash_cache_alloc(self.ddesc, model.draft_layers, batch, capacity) if with_draft else None
         self.max_rows = max(batch * block, batch * tree_n, prefill_chunk)
         self.ws = capi.dflash_workspace_alloc(self.tdesc, self.ddesc if with_draft else None, self.max_rows, capacity)
@@ -234,18 +240,23 @@ class Session:
         """Take over another session's committed target state (keys/values of
         positions 0..len-1 of every layer, lengths, anchors and emitted
         streams) instead of prefilling the same prompts again."""
-        s = self.m.shape
-        lens = other.target_len()
-        tdt = _DT[self.m.dtype][1]
-        for b, n in enumerate(lens):
-            if n == 0:
-                continue
-            k = torch.empty(s.n_kv, n, s.head_dim, dtype=tdt, device=self.m.device)
-            v = torch.empty_like(k)
-            for li in range(s.n_layers):
-                capi.dflash_cache_read(other.tcache, li, b, 0, n, k, v)
-                capi.dflash_cache_write(self.tcache, li, b, 0, n, k, v)
-        capi.dflash_cache_set_lengths(self.tcache, lens)
+        if (other.capacity, other.batch, other.kv_format) == (self.capacity, self.batch, self.kv_format):
+            capi.dflash_cache_copy(self.tcache, other.tcache)  # the whole cache in a few copies
+        else:
+            if self.kv_format != "bf16" or other.kv_format != "bf16":
+                raise ValueError("8-bit caches are copied whole, between sessions of the same geometry")
+            s = self.m.shape
+            lens = other.target_len()
+            tdt = _DT[self.m.dtype][1]
+            for b, n in enumerate(lens):
+                if n == 0:
+                    continue
+                k = torch.empty(s.n_kv, n, s.head_dim, dtype=tdt, device=self.m.device)
+                v = torch.empty_like(k)
+                for li in range(s.n_layers):
+                    capi.dflash_cache_read(other.tcache, li, b, 0, n, k, v)
+                    capi.dflash_cache_write(self.tcache, li, b, 0, n, k, v)
+            capi.dflash_cache_set_lengths(self.tcache, lens)
         self.anchor.copy_(other.anchor)
         w = min(self.stream_cap, other.stream_cap)
         self.stream[:, :w].copy_(other.stream[:, :w])

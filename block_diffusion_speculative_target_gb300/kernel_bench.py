@@ -68,20 +68,23 @@ def bench_gemm(M, K, rows, iters, warmup, copies=None):
             "GBps": byt / (avg / 1e3) / 1e9, "splits_copies": copies}
 
 
-def bench_attention(P, nq, nkv, n, iters, warmup, causal=1):
+def bench_attention(P, nq, nkv, n, iters, warmup, causal=1, kv="bf16"):
     dev = torch.device("cuda")
     hd = 128
     d = capi.ModelDesc(1, nq * hd, nq, nkv, hd, 256, 256, 1e6, 1e-6, capi.BF16)
-    cap = P + n + 64
-    copies = max(2, -(-3 * L2_BYTES // (2 * 2 * nkv * cap * hd)))
-    caches = [capi.dflash_cache_alloc(d, 1, 1, cap) for _ in range(copies)]
+    cap = (P + n + 64 + 7) // 8 * 8
+    ebytes = 1 if kv == "q8" else 2          # bytes per cached entry (q8: plus 4 per row of 128)
+    copies = max(2, -(-3 * L2_BYTES // (2 * ebytes * nkv * cap * hd)))
+    fmt = capi.KV_Q8 if kv == "q8" else capi.KV_MODEL
+    caches = [capi.dflash_cache_alloc_ex(d, 1, 1, cap, fmt) for _ in range(copies)]
     ws = capi.dflash_workspace_alloc(d, None, max(16, n), cap)
     g = torch.Generator(device=dev).manual_seed(1)
-    kv = torch.empty(nkv, P + n, hd, dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+    kvt = torch.empty(nkv, P + n, hd, dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
     for c in caches:
-        capi.dflash_cache_write(c, 0, 0, 0, P + n, kv, kv)
+        capi.dflash_cache_write(c, 0, 0, 0, P + n, kvt, kvt)
         capi.dflash_cache_set_lengths(c, [P])
-    q = torch.empty(n, nq, hd, dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+    q = torch.empty(n, nq, hd, dtype=torch.float16 if kv == "q8" else torch.bfloat16, device=dev).normal_(
+        0, 1, generator=g)
     out = torch.empty(n, nq * hd, dtype=torch.bfloat16, device=dev)
     for i in range(warmup):
         capi.dflash_attention(d, q, 1, n, causal, caches[i % copies], 0, out, ws)
@@ -91,9 +94,9 @@ def bench_attention(P, nq, nkv, n, iters, warmup, causal=1):
     for c in caches:
         capi.dflash_cache_free(c)
     capi.dflash_workspace_free(ws)
-    byt = 2 * 2 * nkv * (P + n) * hd
-    return {"kernel": "attn_fa_kernel+attn_combine_kernel", "P": P, "nq": nq, "nkv": nkv, "n": n, "ms": avg,
-            "bytes": byt, "GBps": byt / (avg / 1e3) / 1e9}
+    byt = 2 * nkv * (P + n) * (ebytes * hd + (4 if kv == "q8" else 0))
+    return {"kernel": "attn_fa_kernel+attn_combine_kernel", "kv": kv, "P": P, "nq": nq, "nkv": nkv, "n": n,
+            "ms": avg, "bytes": byt, "GBps": byt / (avg / 1e3) / 1e9}
 
 
 def bench_rmsnorm(rows, H, iters, warmup):
@@ -147,12 +150,13 @@ def main():
     ap.add_argument("--n", type=int, default=16)
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--kv", choices=["bf16", "q8"], default="bf16", help="attention: the cache's storage")
     a = ap.parse_args()
     capi.load()
     if a.kernel == "gemm":
         print(json.dumps(bench_gemm(a.M, a.K, a.rows, a.iters, a.warmup)))
     elif a.kernel == "attention":
-        print(json.dumps(bench_attention(a.P, a.nq, a.nkv, a.n, a.iters, a.warmup)))
+        print(json.dumps(bench_attention(a.P, a.nq, a.nkv, a.n, a.iters, a.warmup, kv=a.kv)))
     elif a.kernel == "rmsnorm":
         print(json.dumps(bench_rmsnorm(a.rows, a.H, a.iters, a.warmup)))
     elif a.kernel == "argmax":

@@ -127,6 +127,28 @@ typedef struct dflash_cache dflash_cache;
 
 int dflash_cache_alloc(const dflash_model_desc *d, int32_t n_layers, int32_t batch,
                        int32_t capacity, dflash_cache **out);
+
+/* Storage of a cache's keys and values. */
+enum { DFLASH_KV_MODEL = 0, DFLASH_KV_Q8 = 1 };
+/* dflash_cache_alloc with a storage format.  DFLASH_KV_MODEL: the model dtype
+ * (as dflash_cache_alloc).  DFLASH_KV_Q8 (bf16 models with head_dim 128; the
+ * 8-bit K/V cache of DFlash 深度解析 §8.3 "显存优化" 方案3 and the
+ * quantised cache types the datacamp tutorial runs, §5/§7, read as stated in
+ * the oracle): each key or value row of 128 entries is kept as 8-bit codes
+ * u = q + 128 (q in [-127, 127]) [layer][seq][kv_head][capacity][128] uint8
+ * and one float32 scale s per row [layer][seq][kv_head][capacity]; the entry
+ * is q * s, quantised from the float32 row x as s = max|x| / 127,
+ * q = round-half-even(x / s) (a zero row keeps s = 0).  target_verify writes
+ * its rows this way before attention reads them.  Attention computes in IEEE
+ * half precision: the query is half, and each entry is read as the half
+ * product of q and s rounded to half, half(q * half(s)).  Target caches only: the drafter's cache,
+ * tree verification (target_verify_tree, dflash_accept_tree) and the fp32
+ * configuration return DFLASH_ERR_UNSUPPORTED_SHAPE with a q8 cache.  A q8
+ * cache's capacity is rounded up to a multiple of 8 positions. */
+int dflash_cache_alloc_ex(const dflash_model_desc *d, int32_t n_layers, int32_t batch,
+                          int32_t capacity, int32_t kv_format, dflash_cache **out);
+/* The cache's storage format (DFLASH_KV_MODEL or DFLASH_KV_Q8), or -1. */
+int32_t dflash_cache_kv_format(const dflash_cache *c);
 int dflash_cache_free(dflash_cache *c);
 /* A view of sequences [seq_begin, seq_begin + seq_count) sharing memory with
  * `c` (used to prefill a ragged batch one sequence at a time).  Free views
@@ -144,6 +166,18 @@ int dflash_cache_write(dflash_cache *c, int32_t layer, int32_t seq, int32_t pos0
                        const void *k, const void *v, dflash_stream_t stream);
 int dflash_cache_read(dflash_cache *c, int32_t layer, int32_t seq, int32_t pos0, int32_t n, void *k,
                       void *v, dflash_stream_t stream);
+/* q8 caches: dflash_cache_write takes bf16 rows and quantises them on the
+ * device (same rule as target_verify's writes); dflash_cache_read returns
+ * DFLASH_ERR_INVALID_ARG, and dflash_cache_read_q8 copies the stored codes
+ * u (uint8 [n_kv][n][128]) and scales (float32 [n_kv][n]) instead.  Either
+ * output pair may be NULL. */
+int dflash_cache_read_q8(dflash_cache *c, int32_t layer, int32_t seq, int32_t pos0, int32_t n,
+                         void *k_codes, void *v_codes, float *k_scales, float *v_scales,
+                         dflash_stream_t stream);
+/* Copy every key, value (codes and scales for q8) and length of `src` into
+ * `dst`, two caches (not views) of identical geometry and storage format
+ * (asynchronous device-to-device copies). */
+int dflash_cache_copy(dflash_cache *dst, const dflash_cache *src, dflash_stream_t stream);
 /* Set the first n lengths from host memory (asynchronous). */
 int dflash_cache_set_lengths(dflash_cache *c, const int32_t *host_len, int32_t n,
                              dflash_stream_t stream);
@@ -404,10 +438,15 @@ int dflash_argmax_noalloc(const float *logits, int32_t rows, int32_t V, int32_t 
  * drafter's cross-context window, see dflash_draft.cross_ctx); 0 keeps all.
  * out [batch][n][nq * hd] dtype.  q, out: device
  * pointers owned by the caller; q must be 16-byte aligned (the bf16 path
- * loads it by TMA), else DFLASH_ERR_INVALID_ARG before any CUDA call.
- * Every score and softmax sum is exact per fixed 256-position chunk and the
- * chunks merge in order (the scaled dot-product attention of "DFlash 深度解析",
- * §2.2 draft_inference, evaluated chunkwise). */
+ * loads it by TMA), else DFLASH_ERR_INVALID_ARG before any CUDA call.  With
+ * a DFLASH_KV_Q8 cache q is IEEE half precision (out stays bf16) and the
+ * keys/values are the cache's codes times their row scales.
+ * The scaled dot-product attention of "DFlash 深度解析" §2.2
+ * draft_inference, evaluated per key group: the bf16 path splits the keys
+ * into groups of a fixed number of 128-key tiles (a property of the cache),
+ * keeps one running (max, sum, output) per row and group, and merges the
+ * groups in order; the fp32 path does the same with 256-position chunks.
+ * A row's result depends only on its own query and keys. */
 int dflash_attention(const dflash_model_desc *d, const void *q, int32_t batch, int32_t n,
                      int32_t causal, int32_t window, dflash_cache *cache, int32_t layer, void *out,
                      dflash_workspace *ws, dflash_stream_t stream);

@@ -157,7 +157,9 @@ def round_f16(x):
 # RoPE): s = max|x| / 127 and q = round-half-even(x / s), both in float32
 # arithmetic; a row of zeros keeps s = 0.  Every row the target writes --
 # the block's own rows included -- is stored this way before attention reads
-# it, and the query enters attention in IEEE half precision.
+# it.  Attention computes in IEEE half precision: the query enters rounded to
+# half, and each cached entry is read as the half-precision product of its
+# code and its scale rounded to half, round_f16(q * round_f16(s)).
 
 
 def quantize_q8(x):
@@ -176,9 +178,15 @@ def dequantize_q8(q, s):
     return np.asarray(q, dtype=np.float64) * np.asarray(s, dtype=np.float64)[..., None]
 
 
+def kv_q8_read(q, s):
+    """The entries as attention reads them: round_f16(q * round_f16(s)) (the
+    product of an 8-bit code and an 11-bit scale is exact in float64)."""
+    return round_f16(np.asarray(q, dtype=np.float64) * round_f16(np.asarray(s, dtype=np.float64))[..., None])
+
+
 def kv_q8_store(x):
-    """What a q8 cache holds for the rows x: dequantize_q8(quantize_q8(x))."""
-    return dequantize_q8(*quantize_q8(x))
+    """What attention reads from a q8 cache that was given the rows x."""
+    return kv_q8_read(*quantize_q8(x))
 
 
 # ---------------------------------------------------------------------------

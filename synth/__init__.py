@@ -54,6 +54,7 @@ class Workload:
     teacher_forced: bool
     batch: int = 1
     final_gain: float = 1.0   # initial value of the final RMSNorm gains (test workloads widen logit gaps)
+    kv: str = "bf16"          # the target's K/V cache: "bf16" or "q8" (8-bit codes, a scale per row)
 
     @property
     def draft(self) -> ModelShape:
@@ -83,6 +84,8 @@ WORKLOADS = {
     "qwen3-8b-4k": Workload("qwen3-8b-4k", _qwen3_8b_shape(), 5, "bf16", 16, 4096, 2048, True),
     # 27B-class dense target, block 15, 36K prompt, 1500 tokens, teacher forced
     "dense27b-36k": Workload("dense27b-36k", _dense27b_shape(), 5, "bf16", 15, 36864, 1500, True),
+    # the same with the target's cache in 8 bits
+    "dense27b-36k-q8": Workload("dense27b-36k-q8", _dense27b_shape(), 5, "bf16", 15, 36864, 1500, True, kv="q8"),
     # Qwen3-8B shapes, 8 sequences with prompt lengths uniform on 2048..6144
     # (batch_prompt_lengths; prompt_len is the upper end), block 16
     "qwen3-8b-batch8": Workload("qwen3-8b-batch8", _qwen3_8b_shape(), 5, "bf16", 16, 6144, 512, True, batch=8),

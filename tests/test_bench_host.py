@@ -39,6 +39,19 @@ def test_step_bytes_qwen3_8b_by_hand(bench):
     assert total == weights + kv_per_pos * 4096
 
 
+def test_step_bytes_q8_cache_by_hand(bench):
+    """The 27B-class shapes with the target's cache in 8 bits: per target
+    layer and position, K and V are 8 heads x (128 one-byte codes + a 4-byte
+    scale); the drafter's 5 layers stay bf16 (8 heads x 128 x 2 B each)."""
+    q8, bf = synth.WORKLOADS["dense27b-36k-q8"], synth.WORKLOADS["dense27b-36k"]
+    P = 36864.0
+    t8, w8, kv8 = bench.step_bytes(q8, P)
+    tb, wb, kvb = bench.step_bytes(bf, P)
+    assert w8 == wb
+    assert kv8 == P * (64 * 2 * 8 * (128 + 4) + 5 * 2 * 2 * 8 * 128)
+    assert kvb == P * 69 * 2 * 2 * 8 * 128
+
+
 @pytest.mark.parametrize("name", sorted(synth.WORKLOADS))
 @pytest.mark.parametrize("P", [0.0, 512.0, 4120.5, 36871.0])
 def test_stage_bytes_partition_the_step(bench, name, P):
