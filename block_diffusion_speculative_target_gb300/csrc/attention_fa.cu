@@ -355,7 +355,12 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       for (int w = 2; w < warp; ++w) cidx += (w & 3) * 32 >= 16 * G;
       const int ct = cidx * 32 + lane, nct = kConvWarps * 32;
       const int ch = ct & 7, row0 = ct >> 3, rstep = nct >> 3;
+      // The 8 lanes of a quarter warp convert one row: lanes ch and ch + 4 fill the same swizzled chunk
+      // positions of the two 64-entry halves, so the upper four store their second chunk first; each
+      // store instruction then writes 8 distinct bank groups per quarter warp.
+      const bool swap = ch >= 4;
       const int sw = row0 & 7, d0 = (((ch & 3) * 2) ^ sw) << 4, d1 = (((ch & 3) * 2 + 1) ^ sw) << 4;
+      const int da = swap ? d1 : d0, db = swap ? d0 : d1;
       const __half2 off2 = __float2half2_rn(1152.f);
       // jobs in deadline order: keys of tile t (needed by its Q K^T) before the values of tile t-1
       // (needed only after tile t-1's softmax)
@@ -386,7 +391,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         for (int row = row0; row < 128; row += rstep) {
           const uint4 w = *reinterpret_cast<const uint4*>(sp);
           const __half2 sc2 = __half2half2(__float2half_rn(*scp));
-          const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+          // entries 0..7 of the chunk go to d0, 8..15 to d1; the first store takes the da half
+          const uint32_t in[4] = {swap ? w.z : w.x, swap ? w.w : w.y, swap ? w.x : w.z, swap ? w.y : w.w};
           uint32_t o[8];
 #pragma unroll
           for (int j2 = 0; j2 < 4; ++j2) {
@@ -398,8 +404,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             o[2 * j2 + 1] = *reinterpret_cast<const uint32_t*>(&b);
           }
           // half tile: 64-entry half ch >> 2, 16-byte chunks 2 (ch & 3) and + 1, 128-byte swizzle
-          *reinterpret_cast<uint4*>(dp + d0) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(dp + d1) = make_uint4(o[4], o[5], o[6], o[7]);
+          *reinterpret_cast<uint4*>(dp + da) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(dp + db) = make_uint4(o[4], o[5], o[6], o[7]);
           sp += rstep * 128;
           dp += rstep * 128;
           scp += rstep;
