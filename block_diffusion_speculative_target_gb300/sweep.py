@@ -58,21 +58,24 @@ def fill_cache(cache, n_layers, P, shape, seed):
     capi.dflash_cache_set_lengths(cache, [P])
 
 
-def step_bytes(shape, draft_layers, P, window=0):
+def step_bytes(shape, draft_layers, P, window=0, kv="bf16"):
     """Weights once (the injection's W_k/W_v are the drafter layers' own) plus
-    the keys/values read: the target's over P positions, the drafter's over
-    min(P, window) positions when a cross-context window is set."""
+    the keys/values read: the target's over P positions (bf16, or with the
+    8-bit cache one byte per entry plus a 4-byte scale per row), the
+    drafter's over min(P, window) positions when a cross-context window is
+    set."""
     d = shape.head_dim
     layer = 2 * (shape.hidden * (shape.n_q + 2 * shape.n_kv) * d + shape.n_q * d * shape.hidden
                  + 3 * shape.hidden * shape.ffn)
     lm = 2 * shape.vocab * shape.hidden
     fc = 2 * shape.hidden * 5 * shape.hidden
     Pd = min(P, window) if window > 0 else P
-    kv = (shape.n_layers * P + draft_layers * Pd) * 2 * 2 * shape.n_kv * d
-    return shape.n_layers * layer + lm + draft_layers * layer + lm + fc + kv
+    tpos = 2 * shape.n_kv * (d + 4) if kv == "q8" else 2 * 2 * shape.n_kv * d
+    kvb = shape.n_layers * P * tpos + draft_layers * Pd * 2 * 2 * shape.n_kv * d
+    return shape.n_layers * layer + lm + draft_layers * layer + lm + fc + kvb
 
 
-def run(contexts, blocks, steps, warmup, stage_passes, peak, window=0):
+def run(contexts, blocks, steps, warmup, stage_passes, peak, window=0, kv="bf16"):
     wl = synth.WORKLOADS["qwen3-8b-4k"]
     s = wl.target
     dev = torch.device("cuda", 0)
@@ -85,7 +88,7 @@ def run(contexts, blocks, steps, warmup, stage_passes, peak, window=0):
     out = []
     for P0 in contexts:
         cap = P0 + n_ref + 64
-        sess = Session(m, batch=1, capacity=cap, block=Bmax, stream_cap=n_ref + 8)
+        sess = Session(m, batch=1, capacity=cap, block=Bmax, stream_cap=n_ref + 8, kv_format=kv)
         fill_cache(sess.tcache, s.n_layers, P0, s, seed=100 + P0)
         fill_cache(sess.dcache, wl.draft_layers, P0, s, seed=200 + P0)
         anchor = int(synth.prompt_tokens(1, s.vocab, stream=P0)[0])
@@ -93,7 +96,7 @@ def run(contexts, blocks, steps, warmup, stage_passes, peak, window=0):
         sess.stream[0, 0] = anchor
         sess.stream_len.fill_(1)
         sess.n_pend.zero_()
-        ar = Session(m, batch=1, capacity=cap, block=Bmax, with_draft=False, stream_cap=n_ref + 8)
+        ar = Session(m, batch=1, capacity=cap, block=Bmax, with_draft=False, stream_cap=n_ref + 8, kv_format=kv)
         ar.copy_target_from(sess)
         for _ in range(n_ref - 1):
             ar.ar_step()
@@ -152,8 +155,8 @@ def run(contexts, blocks, steps, warmup, stage_passes, peak, window=0):
             E = sess.emitted()[0]
             assert np.array_equal(E, G[:len(E)]), "speculative stream left the greedy stream"
             P_mid = P0 + 0.5 * (len0 + int(sess.stream_len.item())) - 1
-            by = step_bytes(s, wl.draft_layers, P_mid, window)
-            rec = {"P0": P0, "block": B, "cross_ctx": window, "ms_per_step": ms, "tokens_per_s": tokens / total, "tau": tokens / steps,
+            by = step_bytes(s, wl.draft_layers, P_mid, window, kv)
+            rec = {"P0": P0, "block": B, "cross_ctx": window, "target_kv": kv, "ms_per_step": ms, "tokens_per_s": tokens / total, "tau": tokens / steps,
                    "bytes_per_step": by, "roofline_frac": by / (ms / 1e3) / (peak * 1e9),
                    "stage_ms": {k: statistics.median(v) for k, v in stage.items()}}
             print(json.dumps(rec), flush=True)
@@ -182,11 +185,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--stage-passes", type=int, default=2)
     ap.add_argument("--cross-ctx", type=int, default=0, help="the drafter's cross-context window (0: whole context)")
+    ap.add_argument("--kv", choices=["bf16", "q8"], default="bf16", help="the target's K/V cache storage")
     args = ap.parse_args()
     capi.load()
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     peak = json.load(open(p)).get("hbm_gbs", 6800.0) if os.path.exists(p) else 6800.0
-    recs = run(args.contexts, args.blocks, args.steps, args.warmup, args.stage_passes, peak, args.cross_ctx)
+    recs = run(args.contexts, args.blocks, args.steps, args.warmup, args.stage_passes, peak, args.cross_ctx, args.kv)
     print(table(recs, peak), flush=True)
 
 
