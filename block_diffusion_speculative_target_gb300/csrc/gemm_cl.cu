@@ -356,15 +356,17 @@ __global__ void __launch_bounds__(128)
       }
     }
     if (epi.in_ssq) {
-      // a fused RMSNorm: each of this CTA's rows' 1 / rms from its 32-column sums of squares, one thread
-      // per row adding them in column order (the same order for every row, CTA and batch size)
+      // a fused RMSNorm: each of this CTA's rows' 1 / rms from its 32-column sums of squares, added in
+      // column order per lane and then over a fixed butterfly (the same value in every CTA)
       const int nw = epi.in_cols >> 5;
-      for (int n = r + gt * S; n < rows; n += 64 * S) {
+      for (int n = r + (warp - 2) * S; n < rows; n += 2 * S) {
         const float* sp = epi.in_ssq + (size_t)n * nw;
         float t = 0.f;
-#pragma unroll 8
-        for (int c = 0; c < nw; ++c) t += sp[c];
-        rsc[n] = 1.0f / sqrtf(t / (float)epi.in_cols + epi.in_eps);
+#pragma unroll 4
+        for (int c = lane; c < nw; c += 32) t += sp[c];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0) rsc[n] = 1.0f / sqrtf(t / (float)epi.in_cols + epi.in_eps);
       }
     }
   } else if (warp == 1) {
