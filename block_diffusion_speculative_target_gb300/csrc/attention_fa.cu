@@ -453,10 +453,25 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       // warp-uniform fast path when every real row of the warp sees the whole half (padding rows -- past
       // 16 G or past the block -- are never read, so their values may be anything)
       const bool wfull = __all_sync(0xffffffffu, !row_ok || (!tree && va == 0 && vb == 64));
-      auto vis = [&](int e) {
-        const int k = k0 + e;
-        return e >= va && e < vb && (!tree || k < P || ((tm >> (k - P)) & 1ull));
-      };
+      // the visible entries as a bit mask (entry e: bit e & 31 of word e >> 5), so the masked loops
+      // select instead of branching: keys [va, vb), and in tree mode the context or an ancestor
+      uint32_t vw[2];
+      if (!wfull) {
+        auto range32 = [](int a, int b) -> uint32_t {  // bits [a, b) of a word, 0 <= a, b <= 32
+          const uint32_t below_b = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+          const uint32_t below_a = a >= 32 ? 0xffffffffu : ((1u << a) - 1u);
+          return a < b ? (below_b & ~below_a) : 0u;
+        };
+        vw[0] = range32(min(va, 32), min(vb, 32));
+        vw[1] = range32(max(va - 32, 0), max(vb - 32, 0));
+        if (tree) {  // entry e is key P + (d + e): context below d + e = 0, else bit d + e of the node's mask
+          const int d = k0 - P;
+          const uint64_t tv = d >= 64 ? 0ull : d >= 0 ? tm >> d : d > -64 ? (tm << -d) | ((1ull << -d) - 1ull) : ~0ull;
+          vw[0] &= (uint32_t)tv;
+          vw[1] &= (uint32_t)(tv >> 32);
+        }
+      }
+      auto vis = [&](int e) { return ((vw[e >> 5] >> (e & 31)) & 1u) != 0u; };
       if (live) {  // this half's scores and their maximum over the visible keys
         tmem_ld32(sbase, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         tmem_ld32(sbase + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
@@ -466,8 +481,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           for (int e = 0; e < 64; ++e) lm = fmaxf(lm, __uint_as_float(v[e]));
         } else {
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (vis(e)) lm = fmaxf(lm, __uint_as_float(v[e]));
+          for (int e = 0; e < 64; ++e) lm = fmaxf(lm, vis(e) ? __uint_as_float(v[e]) : -INFINITY);
         }
         xch[(sb * 2 + h) * 128 + r] = lm;
       }
@@ -514,9 +528,9 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             emit(e, ex2f(fmaf(__uint_as_float(v[2 * e]), sl, negm)), ex2f(fmaf(__uint_as_float(v[2 * e + 1]), sl, negm)));
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            emit(e, vis(2 * e) ? ex2f(fmaf(__uint_as_float(v[2 * e]), sl, negm)) : 0.f,
-                 vis(2 * e + 1) ? ex2f(fmaf(__uint_as_float(v[2 * e + 1]), sl, negm)) : 0.f);
+          for (int e = 0; e < 32; ++e)  // a hidden entry: 2^-inf = +0
+            emit(e, ex2f(vis(2 * e) ? fmaf(__uint_as_float(v[2 * e]), sl, negm) : -INFINITY),
+                 ex2f(vis(2 * e + 1) ? fmaf(__uint_as_float(v[2 * e + 1]), sl, negm) : -INFINITY));
         }
         // every score of this half is in registers: P overwrites them (hi at +0..31, lo at +32..63)
         tmem_st16(sbase, *reinterpret_cast<const uint32_t(*)[16]>(&hi[0]));

@@ -19,7 +19,7 @@ def _desc(H=256, nq=4, nkv=4, hd=64, F=768, V=2048, dt=capi.F32, L=1):
 @pytest.fixture(scope="module")
 def ws():
     d = _desc(H=5120, nq=40, nkv=8, hd=128, F=25600, V=151936, dt=capi.BF16)
-    h = capi.dflash_workspace_alloc(d, None, 128, 8192)
+    h = capi.dflash_workspace_alloc(d, None, 128, 20480)
     yield h
     capi.dflash_workspace_free(h)
 
@@ -134,8 +134,11 @@ ATT_CASES = [
     ("bf16", 8, 4, 128, [1024], 128),
     # G = 8: no padding rows, the copy/PV issuing lane sits in a live warp
     ("bf16", 64, 8, 128, [700], 16),
-    # G = 1 with several work items per persistent CTA (512 items)
+    # G = 1, 16 key groups of 4 tiles per sequence
     ("bf16", 8, 8, 128, [8000, 3000], 16),
+    # many key groups (36 and 79): the combine merges more than 32 partials per row
+    ("bf16", 4, 1, 128, [9000], 16),
+    ("bf16", 8, 2, 128, [20000, 611], 16),
 ]
 
 
@@ -189,3 +192,55 @@ def test_attention_rejects_misaligned_query(ws):
         assert capi.dflash_status(ws) == 0
     finally:
         capi.dflash_cache_free(cache)
+
+
+def _window_case(ws, nq, nkv, lens, n, causal, window):
+    """dflash_attention over a 1-layer cache; returns (output, oracle outputs,
+    launches enqueued by the call)."""
+    batch = len(lens)
+    cap = max(lens) + n + 64
+    d = _desc(H=nq * 128, nq=nq, nkv=nkv, hd=128, F=256, V=256, dt=capi.BF16)
+    cache = capi.dflash_cache_alloc(d, 1, batch, cap)
+    try:
+        ks, vs = [], []
+        for b, P in enumerate(lens):
+            k = synth.to_bf16_f32(synth.gaussian((nkv, P + n, 128), seed=30, stream=b))
+            v = synth.to_bf16_f32(synth.gaussian((nkv, P + n, 128), seed=31, stream=b))
+            capi.dflash_cache_write(cache, 0, b, 0, P + n, to_dev(k, "bf16"), to_dev(v, "bf16"))
+            ks.append(k)
+            vs.append(v)
+        capi.dflash_cache_set_lengths(cache, lens)
+        q = synth.to_bf16_f32(synth.gaussian((batch, n, nq, 128), seed=32, scale=1.5))
+        out = torch.empty(batch, n, nq * 128, dtype=torch.bfloat16, device=dev())
+        torch.cuda.synchronize()
+        l0 = capi.dflash_launch_count()
+        capi.dflash_attention(d, to_dev(q, "bf16"), batch, n, causal, cache, 0, out, ws, window=window)
+        launches = capi.dflash_launch_count() - l0
+        got = to_np(out).reshape(batch, n, nq, 128)
+        G = nq // nkv
+        refs = []
+        for b, P in enumerate(lens):
+            allowed = np.ones((n, P + n), bool)
+            if causal:
+                allowed[:, P:] = np.tril(np.ones((n, n), bool))
+            if window > 0:
+                allowed[:, :max(0, P - window)] = False
+            refs.append([O.attention(q[b, :, h], ks[b][h // G], vs[b][h // G], allowed) for h in range(nq)])
+        assert capi.dflash_status(ws) == 0
+        return got, refs, launches
+    finally:
+        capi.dflash_cache_free(cache)
+
+
+@pytest.mark.parametrize("lens,nkv", [([700, 64], 8), ([9000, 2500], 1)])
+@pytest.mark.parametrize("causal,window", [(0, 0), (0, 512), (1, 1000)])
+def test_attention_window_groups(ws, lens, nkv, causal, window):
+    """A few key groups (700 positions, 8 KV heads) and many (9000, one KV
+    head: 36 groups of two tiles), with and without a cross-context window
+    (keys below P - window not visible): every row against the oracle."""
+    nq = 4 * nkv
+    got, refs, launches = _window_case(ws, nq, nkv, lens, 16, causal, window)
+    assert launches == 2  # the group kernel and the combine
+    for b, P in enumerate(lens):
+        for h in range(nq):
+            assert_close(got[b, :, h], refs[b][h], "bf16", f"b={b} h={h} P={P} window={window}")
