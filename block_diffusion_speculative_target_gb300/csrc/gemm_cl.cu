@@ -60,6 +60,8 @@ struct ClCfg {
   static constexpr int PRE = 2048;   // epilogue operands prefetched during the main loop
   static constexpr int RS = kMaxRows * 4;  // rows' 1 / rms of a fused RMSNorm
   static constexpr int SMEM = (RING > RED_BYTES ? RING : RED_BYTES) + 1024 + TAIL + PRE + RS;
+  // a split CTA's summed rows (at most BN / 2 of them) in the dead ring past the partial tile
+  static_assert(RED_BYTES + BN / 2 * BM * 4 <= RING, "the summed rows fit in the dead ring");
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -84,23 +86,32 @@ __device__ __forceinline__ float ld_dsmem(uint32_t addr) {
 
 // Sum of the SS split partials of one element (and of its RoPE partner) in
 // split order, every load issued before the first add.
+__device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Four consecutive columns of one row summed over the SS split partials in
+// split order, every load issued before the first add (16-byte DSMEM loads:
+// a remote request costs about the same whatever its width).
 template <int SS>
-__device__ __forceinline__ void sum_partials(uint32_t red_local, uint32_t off, uint32_t poff, bool rope, float& acc,
-                                             float& pacc) {
-  float p[SS], q[SS];
+__device__ __forceinline__ float4 sum_splits4(uint32_t red_local, uint32_t off) {
+  float4 p[SS];
+#pragma unroll
+  for (int cc = 0; cc < SS; ++cc) p[cc] = ld_dsmem4(dsmem_addr(red_local, (uint32_t)cc) + off);
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int cc = 0; cc < SS; ++cc) {
-    const uint32_t base = dsmem_addr(red_local, (uint32_t)cc);
-    p[cc] = ld_dsmem(base + off);
-    q[cc] = rope ? ld_dsmem(base + poff) : 0.f;
+    a.x += p[cc].x;
+    a.y += p[cc].y;
+    a.z += p[cc].z;
+    a.w += p[cc].w;
   }
-  acc = 0.f;
-  pacc = 0.f;
-#pragma unroll
-  for (int cc = 0; cc < SS; ++cc) {
-    acc += p[cc];
-    pacc += q[cc];
-  }
+  return a;
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
@@ -467,23 +478,38 @@ __global__ void __launch_bounds__(128)
   }
   tc_fence_before();
   cluster_sync();  // every partial of the tile is in shared memory
-  const uint32_t red_local = smem_u32(red);
-  for (int n = r; n < rows; n += S) {
-    const uint32_t off = (uint32_t)((n * C::BM + ml) * 4);
-    const uint32_t poff = (uint32_t)((n * C::BM + (ml ^ 64)) * 4);
-    float acc, pacc;
-    switch (S) {  // the split counts the policy produces: all loads of a row in flight together
-      case 2: sum_partials<2>(red_local, off, poff, rope, acc, pacc); break;
-      case 4: sum_partials<4>(red_local, off, poff, rope, acc, pacc); break;
-      case 8: sum_partials<8>(red_local, off, poff, rope, acc, pacc); break;
-      default:
-        acc = pacc = 0.f;
-        for (int cc = 0; cc < S; ++cc) {
-          const uint32_t base = dsmem_addr(red_local, (uint32_t)cc);
-          acc += ld_dsmem(base + off);
-          if (rope) pacc += ld_dsmem(base + poff);
-        }
+  // This CTA's rows n = r + j S summed over the splits: warp w takes rows j = w, w + 4, ..., each lane
+  // four columns; the sums go to the dead ring past the partial tile.  (S = 1: the tile is the sum.)
+  const float* sums = red;
+  if (S > 1) {
+    const uint32_t red_local = smem_u32(red);
+    float* sbuf = reinterpret_cast<float*>(smem + C::RED_BYTES);  // [row j][128]
+    const int J = rows > r ? (rows - r + S - 1) / S : 0;
+    for (int j = warp; j < J; j += 4) {
+      const uint32_t off = (uint32_t)(((r + j * S) * C::BM + lane * 4) * 4);
+      float4 a;
+      switch (S) {  // the split counts the policy produces
+        case 2: a = sum_splits4<2>(red_local, off); break;
+        case 4: a = sum_splits4<4>(red_local, off); break;
+        case 8: a = sum_splits4<8>(red_local, off); break;
+        default:
+          a = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int cc = 0; cc < S; ++cc) {
+            const float4 p = ld_dsmem4(dsmem_addr(red_local, (uint32_t)cc) + off);
+            a.x += p.x;
+            a.y += p.y;
+            a.z += p.z;
+            a.w += p.w;
+          }
+      }
+      reinterpret_cast<float4*>(sbuf)[j * 32 + lane] = a;
     }
+    __syncthreads();
+    sums = sbuf;
+  }
+  for (int n = r; n < rows; n += S) {
+    const int j = (n - r) / S;
+    float acc = sums[j * C::BM + ml], pacc = rope ? sums[j * C::BM + (ml ^ 64)] : 0.f;
     if (epi.in_ssq) {
       acc *= rsc[n];
       pacc *= rsc[n];
