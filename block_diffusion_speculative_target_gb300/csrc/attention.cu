@@ -224,10 +224,13 @@ bool make_kv_maps_q8(const void* k, const void* v, long long rows_total, CUtenso
 
 int attn_group_tiles(int capacity, int nkv) {
   // units of one sequence at full capacity ~ the SM count: tiles = cap/128 * nkv / SMs,
-  // rounded to the nearest power of two
-  const double x = (double)((capacity + 127) / 128) * nkv / (double)num_sms();
+  // rounded to the nearest power of two, then raised until those units fit in one wave (one
+  // CTA per SM): a second wave of a few units costs a whole unit's latency
+  const int tiles = (capacity + 127) / 128, sms = num_sms();
+  const double x = (double)tiles * nkv / (double)sms;
   int g = 2;
   while (g < 64 && (double)g * 1.41421356 < x) g *= 2;
+  while (g < 64 && (long long)((tiles + g - 1) / g) * nkv > sms) ++g;
   return g;
 }
 

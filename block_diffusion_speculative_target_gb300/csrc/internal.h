@@ -181,8 +181,9 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
                       const int32_t* len, const uint64_t* tree_mask, const KvMaps* maps, const AttnScratch& sc,
                       void* out, int* status, cudaStream_t s);
 // The tiles per partial for a cache of `capacity` positions and nkv heads:
-// about one unit per SM for one sequence at full capacity, a power of two in
-// [2, 64]; depends on nothing else, so results do not depend on the batch.
+// about one unit per SM for one sequence at full capacity (a power of two in
+// [2, 64], raised until those units fit in one wave); depends on nothing
+// else, so results do not depend on the batch.
 int attn_group_tiles(int capacity, int nkv);
 
 // 3-D map over a bf16 query buffer [rows][nq][128]: boxes of 64 head-dim
