@@ -423,7 +423,10 @@ __global__ void __launch_bounds__(128)
   if (S == 1 && !rope) {
     // Unsplit tile: the accumulator is the result.  Read it straight from
     // TMEM, 16 rows at a time, and run the epilogue with the rows unrolled
-    // (a residual's old values all in flight before the first add).
+    // (a residual's old values all in flight before the first add).  SwiGLU
+    // and float outputs with 16-byte aligned rows leave through a staged slab.
+    const bool slab = (epi.kind == GE_SWIGLU || epi.kind == GE_F32) &&
+                      (reinterpret_cast<uintptr_t>(epi.out) & 15) == 0 && (epi.ldo & (epi.kind == GE_F32 ? 3 : 7)) == 0;
 #pragma unroll 1
     for (int c = 0; c < BN / 16; ++c) {
       if (c * 16 >= rows) break;  // uniform
@@ -448,6 +451,35 @@ __global__ void __launch_bounds__(128)
           if (ok) resid_store(epi, n, m0 + ml, x);
           if (epi.norm_out) norm_handover(epi, n, m0 + ml, x, ok, lane);
         }
+      } else if (slab) {
+        // the 16-row slab staged in the dead ring, then stored in 16-byte row pieces (one store per
+        // thread for SwiGLU's 16 x 64 bf16, four for 16 x 128 float)
+        if (epi.kind == GE_SWIGLU) {
+          bf16* st = reinterpret_cast<bf16*>(smem);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float partner = __shfl_xor_sync(0xffffffffu, v[i], 1);  // the up row of gate row ml
+            if ((ml & 1) == 0) st[i * 64 + (ml >> 1)] = __float2bfloat16_rn(silu_f(v[i]) * partner);
+          }
+          __syncthreads();
+          const int n = c * 16 + (ml >> 3);
+          if (n < rows && !flags[0])
+            *reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(epi.out) + (size_t)n * epi.ldo + (m0 >> 1) + (ml & 7) * 8) =
+                reinterpret_cast<const uint4*>(smem)[ml];
+        } else {  // GE_F32
+          float* st = reinterpret_cast<float*>(smem);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) st[i * 128 + ml] = v[i];
+          __syncthreads();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int idx = k * 128 + ml, n = c * 16 + (idx >> 5);
+            if (n < rows && !flags[0])
+              *reinterpret_cast<float4*>(reinterpret_cast<float*>(epi.out) + (size_t)n * epi.ldo + m0 + (idx & 31) * 4) =
+                  reinterpret_cast<const float4*>(smem)[idx];
+          }
+        }
+        __syncthreads();  // the slab is rewritten for the next 16 rows
       } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
