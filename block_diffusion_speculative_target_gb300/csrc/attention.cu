@@ -87,10 +87,11 @@ __global__ void __launch_bounds__(NT)
   }
 }
 
-// Merge of the key-group partials of one (row, head), one warp per pair:
-// with w_c = 2^(m_c - max m), out[d] = sum_c w_c o_c[d] / sum_c w_c l_c, the
-// numerator summed over c in increasing order.  Lane l owns columns 4 l ..
-// 4 l + 3.  The row's length, the first 32 groups' maxima and sums and the
+// Merge of the key-group partials of one (row, head), two warps per pair
+// (64 of the 128 columns each): with w_c = 2^(m_c - max m), out[d] =
+// sum_c w_c o_c[d] / sum_c w_c l_c, the numerator summed over c in
+// increasing order.  Lane l of half h owns columns 64 h + 2 l and + 1.  The
+// row's length, the first 32 groups' maxima and sums and the
 // first kCombineBatch groups' partial rows are all requested at once, before
 // the row's group range is known (slots past it are read but never used), so
 // a row with few groups needs one trip to memory.  The denominator's per-lane
@@ -100,7 +101,7 @@ __global__ void __launch_bounds__(NT)
 // waits there for it to finish.
 constexpr int kCombineMaxChunks = 1024;
 constexpr int kCombineWarps = 4;
-constexpr int kCombineBatch = 12;  // partial rows in flight per lane
+constexpr int kCombineBatch = 16;  // partial rows in flight per lane
 
 template <typename T>
 __global__ void __launch_bounds__(kCombineWarps * 32, 6)
@@ -108,7 +109,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 6)
                         int hd, int causal, int capacity, int window, int gk, const int32_t* __restrict__ len,
                         int nchunk, T* __restrict__ out) {
   const int lane = threadIdx.x & 31;
-  const int item = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  const int wi = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  const int item = wi >> 1, half = wi & 1;  // two warps per (row, head): 64 of the 128 dimensions each
   pdl_launch();
   pdl_wait();
   if (item >= rows * nq) return;  // warp-uniform
@@ -116,13 +118,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 6)
   const int b = r / n, j = r - b * n;
   const size_t row0 = ((size_t)r * nq + hq) * nchunk;
   const float2* ml = reinterpret_cast<const float2*>(part_ml) + row0;
-  const float4* po = reinterpret_cast<const float4*>(part_o + row0 * kHD) + lane;  // group c at po[c * kHD / 4]
+  const float2* po = reinterpret_cast<const float2*>(part_o + row0 * kHD) + half * 32 + lane;  // group c: po[c * kHD / 2]
   const int P = len[b];
   const float2 ml0 = lane < nchunk ? ml[lane] : make_float2(-INFINITY, 0.f);  // group `lane`
-  float4 v[kCombineBatch];
+  float2 v[kCombineBatch];
 #pragma unroll
   for (int u = 0; u < kCombineBatch; ++u)
-    if (u < nchunk) v[u] = po[(size_t)u * (kHD / 4)];
+    if (u < nchunk) v[u] = po[(size_t)u * (kHD / 2)];
   const int lim = min(causal ? P + j + 1 : P + n, capacity);
   const int nch = min((lim + gk - 1) / gk, min(nchunk, kCombineMaxChunks));
   // groups below a cross-context window hold no partial
@@ -133,13 +135,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 6)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   const float M = m;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float2 acc = make_float2(0.f, 0.f);
   float lsum = 0.f;
   for (int c0 = 0; c0 < nch; c0 += kCombineBatch) {
     if (c0 > 0) {
 #pragma unroll
       for (int u = 0; u < kCombineBatch; ++u)
-        if (c0 + u < nch) v[u] = po[(size_t)(c0 + u) * (kHD / 4)];
+        if (c0 + u < nch) v[u] = po[(size_t)(c0 + u) * (kHD / 2)];
     }
     // lane u < kCombineBatch: group c0 + u's weight and its term of the denominator (groups below 32
     // come from the lane that loaded them)
@@ -155,19 +157,16 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 6)
       if (c0 + u >= clo && c0 + u < nch) {
         acc.x += w * v[u].x;
         acc.y += w * v[u].y;
-        acc.z += w * v[u].z;
-        acc.w += w * v[u].w;
       }
     }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-  if (4 * lane < hd) {
-    T* dst = out + ((size_t)r * nq + hq) * hd + 4 * lane;
+  const int d = half * 64 + 2 * lane;
+  if (d < hd) {
+    T* dst = out + ((size_t)r * nq + hq) * hd + d;
     dst[0] = from_f<T>(acc.x / lsum);
     dst[1] = from_f<T>(acc.y / lsum);
-    dst[2] = from_f<T>(acc.z / lsum);
-    dst[3] = from_f<T>(acc.w / lsum);
   }
 }
 
@@ -277,7 +276,7 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
   const int nchunk_launch = (capacity + kAttnChunk - 1) / kAttnChunk;
   if (nchunk_launch > sc.nchunk || nchunk_launch > kCombineMaxChunks || hd > kHD) return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
-  const unsigned combine_blocks = (unsigned)((batch * n * nq + kCombineWarps - 1) / kCombineWarps);
+  const unsigned combine_blocks = (unsigned)((2 * batch * n * nq + kCombineWarps - 1) / kCombineWarps);
   if (dtype == DFLASH_BF16) {
     if (hd != kHD || !maps) return cudaErrorInvalidValue;
     const int G = nq / nkv;
