@@ -339,12 +339,14 @@ __global__ void __launch_bounds__(NT) argmax_kernel(const float* __restrict__ lo
   const float* row = logits + (size_t)row_i * V;
   pdl_launch();
   pdl_wait();
-  const int per = (V + ns - 1) / ns;
-  const int v0 = sl * per, v1 = min(V, v0 + per);
+  // 16-byte loads when the rows allow them (slices then start on multiples of 4 entries); each thread
+  // takes its entries in increasing index order, so ties keep the lowest index
+  const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+  const int per = vec ? (((V + ns - 1) / ns + 3) & ~3) : (V + ns - 1) / ns;
+  const int v0 = min(V, sl * per), v1 = min(V, v0 + per);
   Top2 t{-INFINITY, -INFINITY, 0x7fffffff};
   bool bad = false;
-  for (int i = v0 + threadIdx.x; i < v1; i += NT) {
-    const float v = row[i];
+  auto take = [&](float v, int i) {
     bad |= !(fabsf(v) <= 3.0e38f);
     if (v > t.v1) {
       t.v2 = t.v1;
@@ -353,6 +355,33 @@ __global__ void __launch_bounds__(NT) argmax_kernel(const float* __restrict__ lo
     } else if (v > t.v2) {
       t.v2 = v;
     }
+  };
+  if (vec) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const int q1 = v1 >> 2;
+    int q = (v0 >> 2) + threadIdx.x;
+    for (; q + 3 * NT < q1; q += 4 * NT) {  // four 16-byte loads in flight per thread
+      float4 a[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) a[k] = r4[q + k * NT];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = 4 * (q + k * NT);
+        take(a[k].x, i);
+        take(a[k].y, i + 1);
+        take(a[k].z, i + 2);
+        take(a[k].w, i + 3);
+      }
+    }
+    for (; q < q1; q += NT) {
+      const float4 a = r4[q];
+      take(a.x, 4 * q);
+      take(a.y, 4 * q + 1);
+      take(a.z, 4 * q + 2);
+      take(a.w, 4 * q + 3);
+    }
+  } else {
+    for (int i = v0 + threadIdx.x; i < v1; i += NT) take(row[i], i);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {

@@ -91,7 +91,7 @@ def test_rmsnorm(dt, rows, H):
 
 # ---------------------------------------------------------------- argmax
 
-@pytest.mark.parametrize("V", [2048, 1000, 151936])
+@pytest.mark.parametrize("V", [2048, 1000, 1001, 20001, 151936])
 def test_argmax_ties_gap(ws, V):
     rows = 20
     lg = synth.gaussian((rows, V), seed=18, stream=V, scale=2.0)
