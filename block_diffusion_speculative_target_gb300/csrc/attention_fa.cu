@@ -60,16 +60,19 @@ struct FaLayout {
   static_assert(G > 5 || 16 * G * 128 + 2048 <= 16384, "exchange must fit in the query tile's padding rows");
 };
 
-// 8-bit caches (G <= 5): a 2-stage ring of byte tiles as the TMA lands them
-// (key codes, value codes, then their 128 key and 128 value scales), a
-// 2-stage ring of the fp16 operand tiles the converter warps build from them
-// (same layout as the bf16 ring's stages), the query tile, and in the query
-// tile's padding rows the maxima exchange and the barriers.  227 KB in all.
+// 8-bit caches (G <= 5): a 3-stage ring of byte tiles as the TMA lands them
+// (key codes, value codes, then their 128 key and 128 value scales), one
+// half-precision key tile and one value tile that the converter warps build
+// from them (the bf16 ring's stage layout), the query tile, and in the query
+// tile's padding rows the maxima exchange and the barriers.  Three byte
+// stages keep more codes in flight against the DRAM latency than two byte
+// and two half stages did.
 template <int G>
 struct FaLayoutQ8 {
+  static constexpr int kU8Stages = 3;
   static constexpr uint32_t kU8Stage = 2 * 16384 + 2 * 512;
-  static constexpr uint32_t kF = 2 * kU8Stage;                  // fp16 ring, 2 x kStageBytes
-  static constexpr uint32_t kQ = kF + 2 * kStageBytes;
+  static constexpr uint32_t kF = kU8Stages * kU8Stage;          // half keys, then half values
+  static constexpr uint32_t kQ = kF + kStageBytes;
   static constexpr uint32_t kXch = kQ + 16 * G * 128;           // half 0 padding: exchange, 2 KB
   static constexpr uint32_t kBar = kQ + 16384 + 16 * G * 128;   // half 1 padding: barriers, TMEM slot, abort
   static constexpr int kSmem = kQ + 32768 + 1024;
@@ -145,11 +148,12 @@ __device__ __forceinline__ uint64_t smem_desc_mn(uint32_t addr, uint32_t block_s
 // byte tile into half operands: a byte permute places u under the exponent
 // of 1024 (the half 1024 + u, exact), a subtraction of 1152 leaves q, and a
 // multiplication by the row's scale rounded to half gives the entry
-// round(q * half(s)).  Keys are converted as soon as the products of two
-// tiles before are past them (their S exists), values once that tile's
-// P V is done, each released on its own barrier, so neither waits on the
-// other.  The query arrives in half precision, P is a half hi/lo pair, and
-// the softmax is the bf16 path's.
+// round(q * half(s)).  The keys of a tile are converted into the one half
+// key tile as soon as the previous tile's Q K^T has read it (its S exists),
+// its values into the one half value tile once the previous P V is done;
+// each is released on its own barrier, so neither waits on the other, and
+// the byte ring runs three tiles ahead.  The query arrives in half
+// precision, P is a half hi/lo pair, and the softmax is the bf16 path's.
 template <int G, bool Q8>
 __global__ void __launch_bounds__(kFaThreads, 1)
     attn_fa_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -180,10 +184,11 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   uint64_t* drain = bar + 13;     // every issued product completed
   uint64_t* xch_full = bar + 14;  // [2] both halves' maxima written (one arrival per softmax warp)
   // Q8: the byte ring's key half and value half land and are released separately
-  uint64_t* u8_full = bar + 16;   // Q8 [2] a tile's key codes and scales landed ([kv * 2 + s], kv = 0)
-  uint64_t* u8_empty = bar + 20;  // Q8 [2] converted (one arrival per converter warp; [kv * 2 + s])
-  uint64_t* vf_full = bar + 24;   // Q8 [2] a tile's values converted (kv_full: its keys)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 26);
+  constexpr int kU8S = 3;         // byte stages
+  uint64_t* u8_full = bar + 16;   // Q8 [2][3] a tile's codes and scales landed ([kv * 3 + stage], kv 0: keys)
+  uint64_t* u8_empty = bar + 22;  // Q8 [2][3] converted (one arrival per converter warp)
+  uint64_t* vf_full = bar + 28;   // Q8 the half value tile holds the next tile (kv_full[0]: the key tile)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + (Q8 ? 30 : 26));
   volatile int* abort_f = reinterpret_cast<volatile int*>(tslot + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Set-up that needs nothing from the previous kernel (barriers, TMEM, the
@@ -195,13 +200,13 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&kv_full[i], Q8 ? kConvWarps : 1);
       mbar_init(&kv_empty[i], 1);
-      if (Q8) {
-        for (int kv = 0; kv < 2; ++kv) {
-          mbar_init(&u8_full[kv * 2 + i], 1);
-          mbar_init(&u8_empty[kv * 2 + i], kConvWarps);
-        }
-        mbar_init(&vf_full[i], kConvWarps);
+    }
+    if (Q8) {
+      for (int i = 0; i < 2 * kU8S; ++i) {
+        mbar_init(&u8_full[i], 1);
+        mbar_init(&u8_empty[i], kConvWarps);
       }
+      mbar_init(vf_full, kConvWarps);
     }
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
@@ -265,8 +270,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           for (int kv = 0; kv < 2; ++kv) {
             const int tt = t - kv;
             if (tt < 0 || tt >= nt) continue;
-            const int s = tt & 1, bi = kv * 2 + s;
-            if (tt >= 2 && !mbar_wait(&u8_empty[bi], (uint32_t)((tt >> 1) - 1) & 1u, kFaWaitNs)) {
+            const int s = tt % kU8S, bi = kv * kU8S + s;
+            if (tt >= kU8S && !mbar_wait(&u8_empty[bi], (uint32_t)((tt / kU8S) - 1) & 1u, kFaWaitNs)) {
               *abort_f = 1;
               set_status(status, DFLASH_STATUS_TIMEOUT);
               break;
@@ -305,12 +310,13 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     if (lane == 0) {
       const uint32_t idS = Q8 ? idesc_f16_f32(128, 128) : idesc_bf16_f32(128, 128);
       const uint32_t idO = idS | (1u << 16);  // B (values) MN-major
-      const uint32_t kOps = Q8 ? FaLayoutQ8<G>::kF : 0u;  // the operand ring
+      const uint32_t kOps = Q8 ? FaLayoutQ8<G>::kF : 0u;  // the operand ring (Q8: one key and one value tile)
+      constexpr int kOpS = Q8 ? 1 : kStages;
       bool ok = mbar_wait(q_full, 0, kFaWaitNs);
       for (int t = 0; ok && t <= nt; ++t) {
         if (t < nt) {  // S_t = Q K_t^T into S[t & 1], once P_{t-2} (same buffer) has been consumed
-          const int s = t % kStages, sb = t & 1;
-          ok = mbar_wait(&kv_full[s], (uint32_t)(t / kStages) & 1u, kFaWaitNs);
+          const int s = t % kOpS, sb = t & 1;
+          ok = mbar_wait(&kv_full[s], (uint32_t)(t / kOpS) & 1u, kFaWaitNs);
           if (ok && t >= 2) ok = mbar_wait(&pv_done[sb], (uint32_t)((t - 2) >> 1) & 1u, kFaWaitNs);
           if (!ok || *abort_f) break;
           tc_fence_after();
@@ -325,9 +331,9 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           tc_commit(&s_full[sb]);
         }
         if (t >= 1) {  // O += P_hi V + P_lo V for tile t-1 (P of key half j at columns 64 j: hi, then lo)
-          const int w = t - 1, wb = w & 1, s = w % kStages;
+          const int w = t - 1, wb = w & 1, s = w % kOpS;
           ok = mbar_wait(&p_full[wb], (uint32_t)(w >> 1) & 1u, kFaWaitNs);
-          if (Q8 && ok) ok = mbar_wait(&vf_full[s], (uint32_t)(w / kStages) & 1u, kFaWaitNs);
+          if (Q8 && ok) ok = mbar_wait(vf_full, (uint32_t)w & 1u, kFaWaitNs);
           if (!ok || *abort_f) break;
           tc_fence_after();
           const uint32_t vt = smem_u32(sm + kOps + s * kStageBytes + kTileBytes);
@@ -365,15 +371,16 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       // jobs in deadline order: keys of tile t (needed by its Q K^T) before the values of tile t-1
       // (needed only after tile t-1's softmax)
       auto convert = [&](int kv, int t) -> bool {
-        const int s = t & 1;
+        const int s = t % kU8S;
         const uint8_t* src = sm + s * FaLayoutQ8<G>::kU8Stage;
-        uint8_t* dst = sm + FaLayoutQ8<G>::kF + s * kStageBytes;
+        uint8_t* dst = sm + FaLayoutQ8<G>::kF;
         const float* scales = reinterpret_cast<const float*>(src + 32768);  // [128 keys | 128 values]
-        // keys: the stage's previous keys are free once that tile's S exists; values: once its P V is done
-        bool ok = mbar_wait(&u8_full[kv * 2 + s], (uint32_t)(t >> 1) & 1u, kFaWaitNs);
-        if (ok && t >= 2)
-          ok = kv == 0 ? mbar_wait(&s_full[s], (uint32_t)((t - 2) >> 1) & 1u, kFaWaitNs)
-                       : mbar_wait(&kv_empty[s], (uint32_t)((t - 2) >> 1) & 1u, kFaWaitNs);
+        // the half tile is free once the previous tile's product has read it: the keys once its S
+        // exists, the values once its P V is done
+        bool ok = mbar_wait(&u8_full[kv * kU8S + s], (uint32_t)(t / kU8S) & 1u, kFaWaitNs);
+        if (ok && t >= 1)
+          ok = kv == 0 ? mbar_wait(&s_full[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, kFaWaitNs)
+                       : mbar_wait(&pv_done[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, kFaWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (__any_sync(0xffffffffu, !ok || *abort_f)) {
           if (!ok) {
@@ -413,8 +420,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         fence_proxy_async_smem();  // the tensor cores read the tiles through the async proxy
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(kv == 0 ? &kv_full[s] : &vf_full[s]);
-          mbar_arrive(&u8_empty[kv * 2 + s]);
+          mbar_arrive(kv == 0 ? &kv_full[0] : vf_full);
+          mbar_arrive(&u8_empty[kv * kU8S + s]);
         }
         return true;
       };
@@ -618,11 +625,11 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   // ---- teardown: copies and products still in flight complete before the
   // ring and TMEM are released
   if (warp == 0 && lane == 0 && *abort_f) {
-    if (Q8) {  // the last two halves of each kind that were issued
+    if (Q8) {  // the last byte tiles of each kind that were issued
       for (int kv = 0; kv < 2; ++kv) {
         const int last = kv == 0 ? issued : issued_v;
-        for (int tt = last > 2 ? last - 2 : 0; tt < last; ++tt)
-          mbar_wait(&u8_full[kv * 2 + (tt & 1)], (uint32_t)(tt >> 1) & 1u, kFaWaitNs / 4);
+        for (int tt = last > kU8S ? last - kU8S : 0; tt < last; ++tt)
+          mbar_wait(&u8_full[kv * kU8S + tt % kU8S], (uint32_t)(tt / kU8S) & 1u, kFaWaitNs / 4);
       }
     } else {
       const int first = issued > kStages ? issued - kStages : 0;
