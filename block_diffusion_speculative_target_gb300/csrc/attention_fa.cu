@@ -171,6 +171,10 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   constexpr int kSoftWarps = Q8 ? 2 * kLiveQ : 8;  // warps that arrive on p_full / xch_full
   constexpr int kConvWarps = 8 - 2 * kLiveQ;
   static_assert(!Q8 || kConvWarps >= 2, "the 8-bit path needs padding quarters for its converter warps");
+  // Q8: with only two converter warps (GQA 5) the softmax warps convert each tile's values, else the
+  // converter warps convert keys and values
+  constexpr bool kSoftV = Q8 && kConvWarps < 4;
+  constexpr int kVConv = kSoftV ? kSoftWarps : kConvWarps;  // warps converting the values
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kBarOff);
@@ -204,9 +208,9 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     if (Q8) {
       for (int i = 0; i < 2 * kU8S; ++i) {
         mbar_init(&u8_full[i], 1);
-        mbar_init(&u8_empty[i], kConvWarps);
+        mbar_init(&u8_empty[i], i < kU8S ? kConvWarps : kVConv);
       }
-      mbar_init(vf_full, kConvWarps);
+      mbar_init(vf_full, kVConv);
     }
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
@@ -253,6 +257,75 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   const int q4w = warp & 3;
   const bool live = q4w * 32 < 16 * G;  // softmax warps: the quarter holds real rows
   const bool conv = Q8 && warp >= 2 && !live;
+
+  // Q8: one byte-to-half conversion job -- kind kv (0 keys, 1 values) of tile t -- shared by `nparts`
+  // warps, this one of rank `part`.  The converter warps convert the keys, and the values too unless
+  // there are only two of them: then the softmax warps convert a tile's values right after writing
+  // its P, while the next scores are computed.
+  auto convert = [&](int kv, int t, int part, int nparts) -> bool {
+    const int ct = part * 32 + lane, nct = nparts * 32;
+    const int ch = ct & 7, row0 = ct >> 3, rstep = nct >> 3;
+    // The 8 lanes of a quarter warp convert one row: lanes ch and ch + 4 fill the same swizzled chunk
+    // positions of the two 64-entry halves, so the upper four store their second chunk first; each
+    // store instruction then writes 8 distinct bank groups per quarter warp.
+    const bool swap = ch >= 4;
+    const int sw = row0 & 7, d0 = (((ch & 3) * 2) ^ sw) << 4, d1 = (((ch & 3) * 2 + 1) ^ sw) << 4;
+    const int da = swap ? d1 : d0, db = swap ? d0 : d1;
+    const __half2 off2 = __float2half2_rn(1152.f);
+    const int s = t % kU8S;
+    const uint8_t* src = sm + s * FaLayoutQ8<G>::kU8Stage;
+    uint8_t* dst = sm + FaLayoutQ8<G>::kF;
+    const float* scales = reinterpret_cast<const float*>(src + 32768);  // [128 keys | 128 values]
+    // the half tile is free once the previous tile's product has read it: the keys once its S
+    // exists, the values once its P V is done
+    bool ok = mbar_wait(&u8_full[kv * kU8S + s], (uint32_t)(t / kU8S) & 1u, kFaWaitNs);
+    if (ok && t >= 1)
+      ok = kv == 0 ? mbar_wait(&s_full[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, kFaWaitNs)
+                   : mbar_wait(&pv_done[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, kFaWaitNs);
+    ok = __all_sync(0xffffffffu, ok);
+    if (__any_sync(0xffffffffu, !ok || *abort_f)) {
+      if (!ok) {
+        *abort_f = 1;
+        set_status(status, DFLASH_STATUS_TIMEOUT);
+      }
+      return false;
+    }
+    // this thread's 16-byte chunks: rows row0 + i * rstep, entries 16 ch .. + 15 (rstep is a multiple
+    // of 8, so every row keeps the same swizzle phase)
+    const uint8_t* sp = src + kv * 16384 + row0 * 128 + ch * 16;
+    uint8_t* dp = dst + kv * kTileBytes + (ch >> 2) * 16384 + row0 * 128;
+    const float* scp = scales + kv * 128 + row0;
+#pragma unroll 4
+    for (int row = row0; row < 128; row += rstep) {
+      const uint4 w = *reinterpret_cast<const uint4*>(sp);
+      const __half2 sc2 = __half2half2(__float2half_rn(*scp));
+      // entries 0..7 of the chunk go to d0, 8..15 to d1; the first store takes the da half
+      const uint32_t in[4] = {swap ? w.z : w.x, swap ? w.w : w.y, swap ? w.x : w.z, swap ? w.y : w.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int j2 = 0; j2 < 4; ++j2) {
+        const uint32_t lo = __byte_perm(in[j2], 0x64646464u, 0x4140);  // halves 1024 + u of bytes 0, 1
+        const uint32_t hi = __byte_perm(in[j2], 0x64646464u, 0x4342);  // bytes 2, 3
+        const __half2 a = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&lo), off2), sc2);
+        const __half2 b = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&hi), off2), sc2);
+        o[2 * j2] = *reinterpret_cast<const uint32_t*>(&a);
+        o[2 * j2 + 1] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      // half tile: 64-entry half ch >> 2, 16-byte chunks 2 (ch & 3) and + 1, 128-byte swizzle
+      *reinterpret_cast<uint4*>(dp + da) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(dp + db) = make_uint4(o[4], o[5], o[6], o[7]);
+      sp += rstep * 128;
+      dp += rstep * 128;
+      scp += rstep;
+    }
+    fence_proxy_async_smem();  // the tensor cores read the tiles through the async proxy
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(kv == 0 ? &kv_full[0] : vf_full);
+      mbar_arrive(&u8_empty[kv * kU8S + s]);
+    }
+    return true;
+  };
 
   int issued = 0;    // producer: tiles whose copies were issued (Q8: key halves)
   int issued_v = 0;  // Q8: value halves
@@ -359,80 +432,20 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     if constexpr (Q8) {
       int cidx = 0;  // this warp's rank among the converter warps
       for (int w = 2; w < warp; ++w) cidx += (w & 3) * 32 >= 16 * G;
-      const int ct = cidx * 32 + lane, nct = kConvWarps * 32;
-      const int ch = ct & 7, row0 = ct >> 3, rstep = nct >> 3;
-      // The 8 lanes of a quarter warp convert one row: lanes ch and ch + 4 fill the same swizzled chunk
-      // positions of the two 64-entry halves, so the upper four store their second chunk first; each
-      // store instruction then writes 8 distinct bank groups per quarter warp.
-      const bool swap = ch >= 4;
-      const int sw = row0 & 7, d0 = (((ch & 3) * 2) ^ sw) << 4, d1 = (((ch & 3) * 2 + 1) ^ sw) << 4;
-      const int da = swap ? d1 : d0, db = swap ? d0 : d1;
-      const __half2 off2 = __float2half2_rn(1152.f);
       // jobs in deadline order: keys of tile t (needed by its Q K^T) before the values of tile t-1
       // (needed only after tile t-1's softmax)
-      auto convert = [&](int kv, int t) -> bool {
-        const int s = t % kU8S;
-        const uint8_t* src = sm + s * FaLayoutQ8<G>::kU8Stage;
-        uint8_t* dst = sm + FaLayoutQ8<G>::kF;
-        const float* scales = reinterpret_cast<const float*>(src + 32768);  // [128 keys | 128 values]
-        // the half tile is free once the previous tile's product has read it: the keys once its S
-        // exists, the values once its P V is done
-        bool ok = mbar_wait(&u8_full[kv * kU8S + s], (uint32_t)(t / kU8S) & 1u, kFaWaitNs);
-        if (ok && t >= 1)
-          ok = kv == 0 ? mbar_wait(&s_full[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, kFaWaitNs)
-                       : mbar_wait(&pv_done[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, kFaWaitNs);
-        ok = __all_sync(0xffffffffu, ok);
-        if (__any_sync(0xffffffffu, !ok || *abort_f)) {
-          if (!ok) {
-            *abort_f = 1;
-            set_status(status, DFLASH_STATUS_TIMEOUT);
-          }
-          return false;
-        }
-        // this thread's 16-byte chunks: rows row0 + i * rstep, entries 16 ch .. + 15 (rstep is a multiple
-        // of 8, so every row keeps the same swizzle phase)
-        const uint8_t* sp = src + kv * 16384 + row0 * 128 + ch * 16;
-        uint8_t* dp = dst + kv * kTileBytes + (ch >> 2) * 16384 + row0 * 128;
-        const float* scp = scales + kv * 128 + row0;
-#pragma unroll 4
-        for (int row = row0; row < 128; row += rstep) {
-          const uint4 w = *reinterpret_cast<const uint4*>(sp);
-          const __half2 sc2 = __half2half2(__float2half_rn(*scp));
-          // entries 0..7 of the chunk go to d0, 8..15 to d1; the first store takes the da half
-          const uint32_t in[4] = {swap ? w.z : w.x, swap ? w.w : w.y, swap ? w.x : w.z, swap ? w.y : w.w};
-          uint32_t o[8];
-#pragma unroll
-          for (int j2 = 0; j2 < 4; ++j2) {
-            const uint32_t lo = __byte_perm(in[j2], 0x64646464u, 0x4140);  // halves 1024 + u of bytes 0, 1
-            const uint32_t hi = __byte_perm(in[j2], 0x64646464u, 0x4342);  // bytes 2, 3
-            const __half2 a = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&lo), off2), sc2);
-            const __half2 b = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&hi), off2), sc2);
-            o[2 * j2] = *reinterpret_cast<const uint32_t*>(&a);
-            o[2 * j2 + 1] = *reinterpret_cast<const uint32_t*>(&b);
-          }
-          // half tile: 64-entry half ch >> 2, 16-byte chunks 2 (ch & 3) and + 1, 128-byte swizzle
-          *reinterpret_cast<uint4*>(dp + da) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(dp + db) = make_uint4(o[4], o[5], o[6], o[7]);
-          sp += rstep * 128;
-          dp += rstep * 128;
-          scp += rstep;
-        }
-        fence_proxy_async_smem();  // the tensor cores read the tiles through the async proxy
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(kv == 0 ? &kv_full[0] : vf_full);
-          mbar_arrive(&u8_empty[kv * kU8S + s]);
-        }
-        return true;
-      };
       for (int t = 0; t <= nt; ++t) {
-        if (t < nt && !convert(0, t)) break;
-        if (t >= 1 && !convert(1, t - 1)) break;
+        if (t < nt && !convert(0, t, cidx, kConvWarps)) break;
+        if (!kSoftV && t >= 1 && !convert(1, t - 1, cidx, kConvWarps)) break;
       }
+
     }
   } else {
     // ------------------------------------------------------------ softmax
     const int q4 = q4w, h = (warp - 2) >> 2;
+    int srank = warp - 2;  // this warp's rank among the softmax warps
+    if (Q8)
+      for (int w = 2; w < warp; ++w) srank -= (w & 3) * 32 >= 16 * G;
     const int r = q4 * 32 + lane;
     const int ri = r / G;
     const int qi = rb * 16 + ri;
@@ -568,6 +581,12 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
+      if constexpr (kSoftV) {  // this tile's values, while the next tile's scores are computed
+        if (!convert(1, t, srank, kSoftWarps)) {
+          ok = false;
+          break;
+        }
+      }
     }
     // the last product of the unit completes before O is read
     if (ok && !*abort_f)
@@ -604,9 +623,6 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     __syncthreads();
     if (good) {
       const int rows_live = min(16 * G, 128);
-      int srank = warp - 2;  // this warp's rank among the warps of this branch
-      if (Q8)
-        for (int w = 2; w < warp; ++w) srank -= (w & 3) * 32 >= 16 * G;
       for (int rr = srank; rr < rows_live; rr += kSoftWarps) {
         const int ir = rr / G, hr = rr - ir * G, qr = rb * 16 + ir;
         if (qr >= n) continue;  // warp-uniform

@@ -88,6 +88,10 @@ Q8_CASES = [
     (8, 4, [300, 17], 1, 0),          # GQA 2, one row
     (8, 8, [3000], 16, 0),            # GQA 1
     (32, 8, [700], 16, 256),          # cross-context window
+    # four tiles per unit: the 3-stage byte ring wraps (GQA 4: converter warps convert the values;
+    # GQA 5: the softmax warps do)
+    (32, 8, [8000], 16, 0),
+    (40, 8, [8000], 15, 0),
 ]
 
 
