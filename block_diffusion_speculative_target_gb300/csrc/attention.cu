@@ -107,7 +107,7 @@ template <typename T>
 __global__ void __launch_bounds__(kCombineWarps * 32, 6)
     attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int rows, int n, int nq,
                         int hd, int causal, int capacity, int window, int gk, const int32_t* __restrict__ len,
-                        int nchunk, T* __restrict__ out) {
+                        int nchunk, int swz_g, T* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int wi = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   const int item = wi >> 1, half = wi & 1;  // two warps per (row, head): 64 of the 128 dimensions each
@@ -118,7 +118,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 6)
   const int b = r / n, j = r - b * n;
   const size_t row0 = ((size_t)r * nq + hq) * nchunk;
   const float2* ml = reinterpret_cast<const float2*>(part_ml) + row0;
-  const float2* po = reinterpret_cast<const float2*>(part_o + row0 * kHD) + half * 32 + lane;  // group c: po[c * kHD / 2]
+  // this lane's two columns 64 half + 2 lane: 16-byte chunk 16 half + lane / 2 of the row, which the
+  // tcgen05 kernel leaves XOR-swizzled by (the row's index within its attention unit) & 7
+  const int sw = swz_g > 0 ? (((j & 15) * swz_g + hq % swz_g) & 7) : 0;
+  const float2* po = reinterpret_cast<const float2*>(part_o + row0 * kHD) +
+                     ((((half * 16 + (lane >> 1)) ^ sw) << 1) | (lane & 1));  // group c: po[c * kHD / 2]
   const int P = len[b];
   const float2 ml0 = lane < nchunk ? ml[lane] : make_float2(-INFINITY, 0.f);  // group `lane`
   float2 v[kCombineBatch];
@@ -285,14 +289,14 @@ cudaError_t attention(int dtype, const void* q, int batch, int n, int nq, int nk
     DFL_RET(attention_fa(G, *maps, qmap, batch, n, nq, nkv, causal, window, capacity, gtiles, len, tree_mask, sc,
                          scale_log2, status, s));
     DFL_RET(launch_pdl(attn_combine_kernel<bf16>, dim3(combine_blocks), dim3(kCombineWarps * 32), 0, s, sc.o, sc.ml,
-                       batch * n, n, nq, hd, causal, capacity, window, gtiles * 128, len, sc.nchunk, (bf16*)out));
+                       batch * n, n, nq, hd, causal, capacity, window, gtiles * 128, len, sc.nchunk, G, (bf16*)out));
   } else {
     const dim3 grid(nchunk_launch, nq, batch * n);
     DFL_RET(launch_pdl(attn_f32_kernel<128>, grid, dim3(128), 0, s, (const float*)q, n, nq, nkv, hd, causal,
                        (const float*)kc, (const float*)vc, seq_stride, head_stride, capacity, window, len, tree_mask,
                        sc.o, sc.ml, sc.nchunk, scale_log2));
     DFL_RET(launch_pdl(attn_combine_kernel<float>, dim3(combine_blocks), dim3(kCombineWarps * 32), 0, s, sc.o, sc.ml,
-                       batch * n, n, nq, hd, causal, capacity, window, kAttnChunk, len, sc.nchunk, (float*)out));
+                       batch * n, n, nq, hd, causal, capacity, window, kAttnChunk, len, sc.nchunk, 0, (float*)out));
   }
   count_launch(2);
   return cudaSuccess;

@@ -620,17 +620,22 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       stg_l[2 * r + h] = Lh;
       if (h == 0) stg_m[r] = M;
     }
+    fence_proxy_async_smem();  // the staged rows leave through the bulk-copy engine
     __syncthreads();
     if (good) {
       const int rows_live = min(16 * G, 128);
-      for (int rr = srank; rr < rows_live; rr += kSoftWarps) {
-        const int ir = rr / G, hr = rr - ir * G, qr = rb * 16 + ir;
-        if (qr >= n) continue;  // warp-uniform
+      // lane l of this warp sends row srank + l kSoftWarps: its 512 bytes as they are staged (16-byte
+      // chunks XOR-swizzled by the row's index in the unit, which the combine undoes) by one bulk copy,
+      // its maximum and sum by a plain store
+      const int rr = srank + lane * kSoftWarps;
+      const int ir = rr / G, hr = rr - ir * G, qr = rb * 16 + ir;
+      const bool mine = rr < rows_live && qr < n;
+      if (mine) {
         const size_t prow = ((size_t)(b * n + qr) * nq + hk * G + hr) * ngroups + gi;
-        *reinterpret_cast<float4*>(part_o + prow * 128 + lane * 4) =
-            *reinterpret_cast<const float4*>(stg + rr * 128 + ((lane ^ (rr & 7)) << 2));
-        if (lane == 0)
-          *reinterpret_cast<float2*>(part_ml + prow * 2) = make_float2(stg_m[rr], stg_l[2 * rr] + stg_l[2 * rr + 1]);
+        bulk_store(part_o + prow * 128, stg + rr * 128, 512);
+        bulk_store_commit();
+        *reinterpret_cast<float2*>(part_ml + prow * 2) = make_float2(stg_m[rr], stg_l[2 * rr] + stg_l[2 * rr + 1]);
+        bulk_store_wait();  // the copy has read the staged row and written it before the ring is released
       }
     }
   }

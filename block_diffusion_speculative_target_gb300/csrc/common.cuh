@@ -127,6 +127,17 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// Shared memory to global memory, `bytes` (a multiple of 16, both addresses
+// 16-byte aligned) by the bulk-copy engine; completion tracked per thread
+// with bulk_store_commit / bulk_store_wait.
+__device__ __forceinline__ void bulk_store(void* dst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Every bulk store this thread committed has completed (its writes performed).
+__device__ __forceinline__ void bulk_store_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Shared-memory writes made by ordinary stores become visible to the tensor
 // cores' (async-proxy) operand reads.
 __device__ __forceinline__ void fence_proxy_async_smem() {
