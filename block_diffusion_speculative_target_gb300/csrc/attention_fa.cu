@@ -62,8 +62,8 @@ struct FaLayout {
 
 // 8-bit caches (G <= 5): a 3-stage ring of byte tiles as the TMA lands them
 // (key codes, value codes, then their 128 key and 128 value scales), one
-// half-precision key tile and one value tile that the converter warps build
-// from them (the bf16 ring's stage layout), the query tile, and in the query
+// half-precision key tile and one value tile built from them (the bf16
+// ring's stage layout), the query tile, and in the query
 // tile's padding rows the maxima exchange and the barriers.  Three byte
 // stages keep more codes in flight against the DRAM latency than two byte
 // and two half stages did.
@@ -188,9 +188,9 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   uint64_t* drain = bar + 13;     // every issued product completed
   uint64_t* xch_full = bar + 14;  // [2] both halves' maxima written (one arrival per softmax warp)
   // Q8: the byte ring's key half and value half land and are released separately
-  constexpr int kU8S = 3;         // byte stages
+  constexpr int kU8S = FaLayoutQ8<G>::kU8Stages;  // byte stages (3)
   uint64_t* u8_full = bar + 16;   // Q8 [2][3] a tile's codes and scales landed ([kv * 3 + stage], kv 0: keys)
-  uint64_t* u8_empty = bar + 22;  // Q8 [2][3] converted (one arrival per converter warp)
+  uint64_t* u8_empty = bar + 22;  // Q8 [2][3] converted (one arrival per warp converting that kind)
   uint64_t* vf_full = bar + 28;   // Q8 the half value tile holds the next tile (kv_full[0]: the key tile)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + (Q8 ? 30 : 26));
   volatile int* abort_f = reinterpret_cast<volatile int*>(tslot + 1);
