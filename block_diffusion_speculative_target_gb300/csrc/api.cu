@@ -594,6 +594,12 @@ static int layer_forward_f32(const dflash_model_desc& d, const dflash_layer_w& w
 // positions (the drafter's cross-context window).  rope_off/tree_mask
 // (nullable, tree verification): row n's RoPE position is len + rope_off[n]
 // and it attends to the context and the block keys its mask selects.
+// The gain of a stack's first RMSNorm: its first layer's attention norm (the final norm of an empty stack).
+static const void* first_norm(const dflash_model_desc& d, const dflash_layer_w* layers, const void* final_norm) {
+  return d.n_layers > 0 ? layers[0].attn_norm : final_norm;
+}
+
+// bf16: expects x and the first norm's hand-over (xn, ssq) already written, by the embedding.
 static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layers, dflash_cache* c, int batch, int n,
                          int causal, int window, const int32_t* rope_off, const uint64_t* tree_mask,
                          const int32_t* capture, void* hcap, const void* final_norm, const void* lm_head,
@@ -632,7 +638,7 @@ static int decoder_stack(const dflash_model_desc& d, const dflash_layer_w* layer
     e.norm_ssq = ws->ssq;
     return e;
   };
-  CK(norm_prep(ws->x, L > 0 ? layers[0].attn_norm : final_norm, ws->xn, ws->ssq, rows, H, s));
+  // (the first norm's hand-over comes with the embedding rows)
   for (int l = 0; l < L; ++l) {
     const dflash_layer_w& w = layers[l];
     uint8_t* kc = c->k + (size_t)l * c->layer_stride * c->elem;
@@ -674,7 +680,10 @@ int target_verify(const dflash_target* tg, const int32_t* tokens, int32_t batch,
   for (int i = 0; i < 5; ++i) REQ(tg->capture[i] >= 0 && tg->capture[i] < d.n_layers);
   cudaStream_t s = (cudaStream_t)cuda_stream;
   const int rows = batch * n, H = d.hidden;
-  CK(embed(d.dtype, tg->embed, d.vocab, H, tokens, nullptr, 0, batch, n, 0, nullptr, ws->x, ws->status, s));
+  const bool b16 = d.dtype == DFLASH_BF16;
+  CK(embed(d.dtype, tg->embed, d.vocab, H, tokens, nullptr, 0, batch, n, 0, nullptr, ws->x,
+           b16 ? first_norm(d, tg->layers, tg->final_norm) : nullptr, b16 ? ws->xn : nullptr, b16 ? ws->ssq : nullptr,
+           ws->status, s));
   int rc = decoder_stack(d, tg->layers, tc, batch, n, 1, 0, nullptr, nullptr, tg->capture, hcap, tg->final_norm,
                          tg->lm_head, ws->logits, ws, s);
   if (rc != DFLASH_OK) return rc;
@@ -742,7 +751,9 @@ int dflash_draft_block(const dflash_draft* dr, const dflash_target* tg, const in
   REQ(dr->mask_id >= 0 && dr->mask_id < d.vocab && dr->cross_ctx >= 0);
   cudaStream_t s = (cudaStream_t)stream;
   const int rows = batch * block, H = d.hidden;
+  const bool b16 = d.dtype == DFLASH_BF16;
   CK(embed(d.dtype, tg->embed, d.vocab, H, nullptr, anchor, dr->mask_id, batch, block, 1, draft_tokens, ws->x,
+           b16 ? first_norm(d, dr->layers, dr->final_norm) : nullptr, b16 ? ws->xn : nullptr, b16 ? ws->ssq : nullptr,
            ws->status, s));
   int rc = decoder_stack(d, dr->layers, dc, batch, block, 0, dr->cross_ctx, nullptr, nullptr, nullptr, nullptr,
                          dr->final_norm, tg->lm_head, ws->dlogits, ws, s);
@@ -848,7 +859,10 @@ int target_verify_tree(const dflash_target* tg, const int32_t* tree_tokens, cons
   if (tc->kv_format != DFLASH_KV_MODEL) return DFLASH_ERR_UNSUPPORTED_SHAPE;
   for (int i = 0; i < 5; ++i) REQ(tg->capture[i] >= 0 && tg->capture[i] < d.n_layers);
   cudaStream_t s = (cudaStream_t)cuda_stream;
-  CK(embed(d.dtype, tg->embed, d.vocab, d.hidden, tree_tokens, nullptr, 0, batch, n, 0, nullptr, ws->x, ws->status, s));
+  const bool b16 = d.dtype == DFLASH_BF16;
+  CK(embed(d.dtype, tg->embed, d.vocab, d.hidden, tree_tokens, nullptr, 0, batch, n, 0, nullptr, ws->x,
+           b16 ? first_norm(d, tg->layers, tg->final_norm) : nullptr, b16 ? ws->xn : nullptr, b16 ? ws->ssq : nullptr,
+           ws->status, s));
   int rc = decoder_stack(d, tg->layers, tc, batch, n, 0, 0, tree_depth, tree_mask, tg->capture, hcap, tg->final_norm,
                          tg->lm_head, ws->logits, ws, s);
   if (rc != DFLASH_OK) return rc;

@@ -123,18 +123,17 @@ cudaError_t gemm_simt(const float* X, int ldx, int rows, const float* W, int M, 
 bool gemm_shape_ok(int dtype, int M, int K);
 
 // Row-wise RMSNorm: y = T(x * 1/sqrt(mean(x^2)+eps) * g).
-// The first normed product's operand bf16(x * g) [rows][H] and the sums of x^2
-// over each 32 consecutive columns [rows][H / 32] (bf16; H % 32 == 0).
-cudaError_t norm_prep(const float* x, const void* g, void* xg, float* ssq, int rows, int H, cudaStream_t s);
 cudaError_t rmsnorm(int dtype, const float* x, const void* g, void* y, int rows, int H, float eps,
                     cudaStream_t s);
 // Copy T(x) into column block `slot` of hcap [rows][5H].
 cudaError_t capture(int dtype, const float* x, void* hcap, int rows, int H, int slot, cudaStream_t s);
 // x[r] = float(E[token(r)]).  mode 0: token = tokens[r]; mode 1 (draft block):
 // token = anchor[b] for slot 0 else mask_id, and draft_out[b][0] = anchor[b].
+// With xg (bf16), also the first norm's hand-over: xg = bf16(x * norm_gain)
+// and ssq [rows][H/32] (the sums of x^2 over each 32 consecutive columns).
 cudaError_t embed(int dtype, const void* E, int V, int H, const int32_t* tokens, const int32_t* anchor,
-                  int mask_id, int batch, int n, int mode, int32_t* draft_out, float* x, int* status,
-                  cudaStream_t s);
+                  int mask_id, int batch, int n, int mode, int32_t* draft_out, float* x, const void* norm_gain,
+                  void* xg, float* ssq, int* status, cudaStream_t s);
 // RoPE on the q and k parts of qkv (f32 [rows][(nq+2nkv)hd]); q -> qout (T), k/v -> cache at len[b]+j.
 // rope_off (nullable): row r's RoPE position is len[b] + rope_off[r] instead of len[b] + j (tree nodes).
 cudaError_t rope_qkv(int dtype, const float* qkv, int batch, int n, int nq, int nkv, int hd, void* qout,

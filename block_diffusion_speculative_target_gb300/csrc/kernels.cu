@@ -50,31 +50,6 @@ cudaError_t rmsnorm(int dtype, const float* x, const void* g, void* y, int rows,
   return cudaGetLastError();
 }
 
-// One CTA per row; warp w of pass k covers columns 256 k + 32 w .. + 31, so each
-// warp sum is one 32-column slice.
-__global__ void __launch_bounds__(256) norm_prep_kernel(const float* __restrict__ x, const bf16* __restrict__ g,
-                                                        bf16* __restrict__ xg, float* __restrict__ ssq, int H) {
-  const float* xr = x + (size_t)blockIdx.x * H;
-  pdl_launch();
-  pdl_wait();
-  for (int i = threadIdx.x; i < H; i += 256) {
-    const float v = xr[i];
-    xg[(size_t)blockIdx.x * H + i] = __float2bfloat16_rn(v * __bfloat162float(g[i]));
-    float t = v * v;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    if ((threadIdx.x & 31) == 0) ssq[(size_t)blockIdx.x * (H >> 5) + (i >> 5)] = t;
-  }
-}
-
-cudaError_t norm_prep(const float* x, const void* g, void* xg, float* ssq, int rows, int H, cudaStream_t s) {
-  if (rows <= 0) return cudaSuccess;
-  if (H % 32) return cudaErrorInvalidValue;
-  DFL_RET(launch_pdl(norm_prep_kernel, dim3(rows), dim3(256), 0, s, x, (const bf16*)g, (bf16*)xg, ssq, H));
-  count_launch();
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------------ 8-bit cache rows
 // One warp per 128-entry row (lane l: entries 4 l .. 4 l + 3): s = max|x| /
 // 127 and q = round-half-even(x / s) in float32 (IEEE division), stored as
@@ -144,10 +119,17 @@ cudaError_t capture(int dtype, const float* x, void* hcap, int rows, int H, int 
 }
 
 // ------------------------------------------------------------------ embedding
+// With `xg` given (bf16 only), the row also leaves as the first layer's
+// norm operand, as a residual-add epilogue hands it over to the next
+// product: bf16(x * g) and the sums of x^2 over each warp's 32-column slices
+// (pass k, warp w: columns 256 k + 32 w .. + 31).
 template <typename T>
-__global__ void embed_kernel(const T* __restrict__ E, int V, int H, const int32_t* __restrict__ tokens,
-                             const int32_t* __restrict__ anchor, int mask_id, int n, int mode,
-                             int32_t* __restrict__ draft_out, float* __restrict__ x, int* status) {
+__global__ void __launch_bounds__(256) embed_kernel(const T* __restrict__ E, int V, int H,
+                                                    const int32_t* __restrict__ tokens,
+                                                    const int32_t* __restrict__ anchor, int mask_id, int n, int mode,
+                                                    int32_t* __restrict__ draft_out, float* __restrict__ x,
+                                                    const bf16* __restrict__ g, bf16* __restrict__ xg,
+                                                    float* __restrict__ ssq, int* status) {
   const int r = blockIdx.x, b = r / n, j = r % n;
   pdl_launch();
   pdl_wait();
@@ -164,19 +146,32 @@ __global__ void embed_kernel(const T* __restrict__ E, int V, int H, const int32_
   }
   const T* er = E + (size_t)tok * H;
   float* xr = x + (size_t)r * H;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) xr[i] = to_f<T>(er[i]);
+  for (int i = threadIdx.x; i < H; i += blockDim.x) {
+    const float v = to_f<T>(er[i]);
+    xr[i] = v;
+    if (xg) {  // uniform
+      xg[(size_t)r * H + i] = __float2bfloat16_rn(v * __bfloat162float(g[i]));
+      float t = v * v;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      if ((threadIdx.x & 31) == 0) ssq[(size_t)r * (H >> 5) + (i >> 5)] = t;
+    }
+  }
 }
 
 cudaError_t embed(int dtype, const void* E, int V, int H, const int32_t* tokens, const int32_t* anchor, int mask_id,
-                  int batch, int n, int mode, int32_t* draft_out, float* x, int* status, cudaStream_t s) {
+                  int batch, int n, int mode, int32_t* draft_out, float* x, const void* norm_gain, void* xg, float* ssq,
+                  int* status, cudaStream_t s) {
   const int rows = batch * n;
   if (rows <= 0) return cudaSuccess;
+  if (xg && (dtype != DFLASH_BF16 || H % 32 || !norm_gain || !ssq)) return cudaErrorInvalidValue;
   if (dtype == DFLASH_BF16)
-    DFL_RET(launch_pdl(embed_kernel<bf16>, dim3(rows), dim3(256), 0, s, (const bf16*)E, V, H, tokens, anchor, mask_id, n, mode, draft_out, x,
-                                            status));
+    DFL_RET(launch_pdl(embed_kernel<bf16>, dim3(rows), dim3(256), 0, s, (const bf16*)E, V, H, tokens, anchor, mask_id,
+                       n, mode, draft_out, x, (const bf16*)norm_gain, (bf16*)xg, ssq, status));
   else
-    DFL_RET(launch_pdl(embed_kernel<float>, dim3(rows), dim3(256), 0, s, (const float*)E, V, H, tokens, anchor, mask_id, n, mode, draft_out, x,
-                                             status));
+    DFL_RET(launch_pdl(embed_kernel<float>, dim3(rows), dim3(256), 0, s, (const float*)E, V, H, tokens, anchor,
+                       mask_id, n, mode, draft_out, x, (const bf16*)nullptr, (bf16*)nullptr, (float*)nullptr,
+                       status));
   count_launch();
   return cudaGetLastError();
 }
