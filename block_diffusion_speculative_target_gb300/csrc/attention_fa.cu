@@ -232,7 +232,6 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   pdl_launch();
-  pdl_wait();
 
   // ---- the unit
   const int nrb = (n + 15) >> 4;
@@ -243,13 +242,43 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   u /= nrb;
   const int b = u % batch;
   const int gi = u / batch;
-  const int P = len[b];
   const int r_last = min(rb * 16 + 15, n - 1);
-  const int kmax = min(causal ? P + r_last + 1 : P + n, capacity);
+  // the unit's key tiles [ta, ta + nt) when the sequence holds P positions before the block
+  auto tile_range = [&](int P, int& ta_, int& nt_) {
+    const int kmax = min(causal ? P + r_last + 1 : P + n, capacity);
+    const int lo_ = window > 0 ? max(0, P - window) : 0;
+    ta_ = max(gi * gtiles, lo_ >> 7);
+    nt_ = min((gi + 1) * gtiles, (kmax + 127) >> 7) - ta_;
+  };
+  // Before the wait on the previous kernel (which may still be writing the block's rows of this cache),
+  // the producer asks L2 for the unit's first ring stages of keys and values, so that their DRAM
+  // latency overlaps the previous kernel's tail.  Every write lands in L2, so no copy requested here
+  // is ever read stale; the length read here may be stale, which only misplaces the requests.
+  if (warp == 0 && lane == 0) {
+    int pta, pnt;
+    tile_range(*reinterpret_cast<const volatile int32_t*>(len + b), pta, pnt);
+    const long long rowp = row0 + ((long long)b * nkv + hk) * capacity;
+    constexpr int kEarly = Q8 ? FaLayoutQ8<G>::kU8Stages : FaLayout<G>::kStages;
+    for (int t = 0; t < min(pnt, kEarly); ++t) {
+      const int key0 = (int)(rowp + (long long)(pta + t) * 128);
+      if constexpr (Q8) {
+        tma_prefetch_l2_2d(&tmK, 0, key0);
+        tma_prefetch_l2_2d(&tmV, 0, key0);
+        bulk_prefetch_l2(kscale + key0, 512);
+        bulk_prefetch_l2(vscale + key0, 512);
+      } else {
+        for (int dh = 0; dh < 2; ++dh) {
+          tma_prefetch_l2_2d(&tmK, dh * 64, key0);
+          tma_prefetch_l2_2d(&tmV, dh * 64, key0);
+        }
+      }
+    }
+  }
+  pdl_wait();
+  const int P = len[b];
   const int lo = window > 0 ? max(0, P - window) : 0;
-  const int ta = max(gi * gtiles, lo >> 7);
-  const int tb = min((gi + 1) * gtiles, (kmax + 127) >> 7);
-  const int nt = tb - ta;
+  int ta, nt;
+  tile_range(P, ta, nt);
   if (nt <= 0) {  // uniform over the CTA: no key of this group is visible
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
     return;

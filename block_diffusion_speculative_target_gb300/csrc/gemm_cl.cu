@@ -72,6 +72,9 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The two halves of cluster_sync, for work that may run between them.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // Address of the same shared-memory offset in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
   uint32_t r;
@@ -539,6 +542,9 @@ __global__ void __launch_bounds__(128)
     __syncthreads();
     sums = sbuf;
   }
+  // this CTA has read the other partials: its own may be released once every CTA has said so, which
+  // the epilogue's stores overlap
+  cluster_arrive();
   for (int n = r; n < rows; n += S) {
     const int j = (n - r) / S;
     float acc = sums[j * C::BM + ml], pacc = rope ? sums[j * C::BM + (ml ^ 64)] : 0.f;
@@ -583,7 +589,7 @@ __global__ void __launch_bounds__(128)
     const float partner = rope ? pacc : __shfl_xor_sync(0xffffffffu, acc, 1);
     if (ok) gemm_epi(epi, n, m0 + ml, acc, partner, status);
   }
-  cluster_sync();  // no CTA leaves while its partial may still be read
+  cluster_wait();  // no CTA leaves while its partial may still be read
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
