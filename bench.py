@@ -36,12 +36,14 @@ import synth  # noqa: E402
 METRIC = "emitted tokens/s per step (draft block+verify) at 4K/36K ctx; % of HBM roofline"
 UNIT = "tokens/s"
 
-# DRAM bytes (read + write) per gemm_cl_kernel launch, averaged over the
-# weight-product launches of one step of the 4K workload, from an ncu launch
-# list of this command (gpu__time_duration.sum, dram__bytes_read.sum,
-# dram__bytes_write.sum over the timed graph replays).  None whenever the
-# kernel has changed since the counters were taken.
-GEMM_TRAFFIC = {"workload": "qwen3-8b-4k", "bytes_per_launch": None}
+# DRAM bytes (read + write) per gemm_cl_kernel launch, averaged over the 168
+# weight-product launches of one step of the 4K workload: ncu
+# (dram__bytes_read.sum + dram__bytes_write.sum, two launches per shape) on
+# `kernel_bench gemm` for each of the step's seven product shapes, weighted by
+# how often the step launches each (1 fusion, 1 injection, 41 each of QKV, O,
+# gate/up and down, 2 LM heads).  None whenever the kernel has changed since
+# the counters were taken.
+GEMM_TRAFFIC = {"workload": "qwen3-8b-4k", "bytes_per_launch": 111487280}
 
 
 def parse():
