@@ -208,6 +208,170 @@ __device__ __forceinline__ void qkv_q8_out(const GemmEpi& e, int n, int m, float
   if (ml == 0) (kind == 1 ? e.ks : e.vs)[row] = sc;
 }
 
+// ---- the split path's epilogue, four columns per lane
+// A warp applies the epilogue to one row of the tile: lane l holds columns
+// m = m0 + 4l .. + 3 (the four sums it reduced), its RoPE partners (column
+// ^ 64 within the head) sit in lane l ^ 16, and every store moves 4, 8 or 16
+// bytes.  The arithmetic per element is the per-column epilogue's.
+
+// Every pointer the epilogue touches is 16-byte aligned and every row stride a
+// multiple of 4 elements: then the four-column stores stay aligned.
+__device__ __forceinline__ bool epi_vec4_ok(const GemmEpi& e) {
+  auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  bool ok = al(e.out) && (e.ldo & 3) == 0 && al(e.hcap) && (e.cap_H & 3) == 0 && al(e.norm_gain) && al(e.norm_out) &&
+            al(e.rope) && al(e.kc) && al(e.vc);
+  if (e.kind == GE_QKV || e.kind == GE_INJECT)
+    ok = ok && (e.layer_stride & 3) == 0 && (e.seq_stride & 3) == 0 && (e.head_stride & 3) == 0;
+  return ok;
+}
+__device__ __forceinline__ void st_bf16x4(void* p, float a, float b, float c, float d) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  *reinterpret_cast<uint2*>(p) = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+__device__ __forceinline__ void st_halfx4(void* p, float a, float b, float c, float d) {
+  const __half2 lo = __floats2half2_rn(a, b), hi = __floats2half2_rn(c, d);
+  *reinterpret_cast<uint2*>(p) = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+
+// Row n, columns m .. m + 3 with their values v (row scale applied).  j: the
+// row's index among this CTA's rows; with `pf`, the residual's old values and
+// the row's position and cos/sin were fetched during the main loop.  Every
+// lane of the warp calls it for the same row; `ok` is false after a time-out.
+__device__ __forceinline__ void gemm_epi4(const GemmEpi& e, int n, int m, float4 v, bool ok, int lane, bool pf, int j,
+                                          const float* pre_x, const float2* pre_cs, const int* pre_pos, int* status) {
+  const float vv[4] = {v.x, v.y, v.z, v.w};
+  switch (e.kind) {
+    case GE_F32:
+      if (ok) *reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out) + (size_t)n * e.ldo + m) = v;
+      return;
+    case GE_STORE:
+      if (ok) st_bf16x4(reinterpret_cast<bf16*>(e.out) + (size_t)n * e.ldo + m, v.x, v.y, v.z, v.w);
+      return;
+    case GE_SWIGLU:
+      if (ok) {
+        const __nv_bfloat162 o = __floats2bfloat162_rn(silu_f(v.x) * v.y, silu_f(v.z) * v.w);
+        *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<bf16*>(e.out) + (size_t)n * e.ldo + (m >> 1)) = o;
+      }
+      return;
+    case GE_RESID: {
+      float* xo = reinterpret_cast<float*>(e.out) + (size_t)n * e.ldo + m;
+      float4 x;
+      if (pf) {
+        const float* px = pre_x + j * 128 + (m & 127);
+        x = make_float4(px[0] + v.x, px[1] + v.y, px[2] + v.z, px[3] + v.w);
+      } else {
+        const float4 o = *reinterpret_cast<const float4*>(xo);
+        x = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+      }
+      if (ok) {
+        *reinterpret_cast<float4*>(xo) = x;
+        if (e.cap_mask)
+          for (int s = 0; s < 5; ++s)
+            if (e.cap_mask & (1 << s))
+              st_bf16x4(reinterpret_cast<bf16*>(e.hcap) + (size_t)n * 5 * e.cap_H + (size_t)s * e.cap_H + m, x.x, x.y,
+                        x.z, x.w);
+      }
+      if (e.norm_out) {  // the next product's operand bf16(x * g) and the sums of x^2 over 32 columns (8 lanes)
+        const uint2 gw = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(e.norm_gain) + m);
+        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw.x));
+        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw.y));
+        if (ok)
+          st_bf16x4(reinterpret_cast<bf16*>(e.norm_out) + (size_t)n * e.ldo + m, x.x * g01.x, x.y * g01.y,
+                    x.z * g23.x, x.w * g23.y);
+        float t = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (ok && (lane & 7) == 0) e.norm_ssq[(size_t)n * (e.ldo >> 5) + (m >> 5)] = t;
+      }
+      return;
+    }
+    default:
+      break;
+  }
+  // GE_QKV / GE_INJECT: the head's 128 columns are this row's 32 lanes
+  float pp[4];
+  pp[0] = __shfl_xor_sync(0xffffffffu, v.x, 16);
+  pp[1] = __shfl_xor_sync(0xffffffffu, v.y, 16);
+  pp[2] = __shfl_xor_sync(0xffffffffu, v.z, 16);
+  pp[3] = __shfl_xor_sync(0xffffffffu, v.w, 16);
+  const int t = m >> 7, ml = m & 127;
+  int kind, h, layer = 0;  // kind: 0 q, 1 k, 2 v
+  if (e.kind == GE_QKV) {
+    kind = t < e.nq ? 0 : (t < e.nq + e.nkv ? 1 : 2);
+    h = kind == 0 ? t : (kind == 1 ? t - e.nq : t - e.nq - e.nkv);
+  } else {
+    layer = t / (2 * e.nkv);
+    const int rem = t % (2 * e.nkv);
+    kind = rem < e.nkv ? 1 : 2;
+    h = rem % e.nkv;
+  }
+  const int b = n / e.rows_per_seq, jj = n % e.rows_per_seq;
+  int pos;
+  float2 cs[4];
+  if (pf) {
+    pos = pre_pos[j];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cs[i] = pre_cs[j * 64 + ((ml + i) & 63)];
+  } else {
+    const bool skip = e.kind == GE_INJECT && jj >= e.n_pend[b];
+    pos = skip ? -1 : e.len[b] + jj;
+    const int rpos = e.rope_off ? e.len[b] + e.rope_off[n] : e.len[b] + jj;  // RoPE position (a tree node's depth)
+    if (rpos >= 0 && rpos < e.capacity) {
+      const float4* c = reinterpret_cast<const float4*>(e.rope + (size_t)rpos * 64 + (ml & 63));
+      const float4 c0 = c[0], c1 = c[1];
+      cs[0] = make_float2(c0.x, c0.y);
+      cs[1] = make_float2(c0.z, c0.w);
+      cs[2] = make_float2(c1.x, c1.y);
+      cs[3] = make_float2(c1.z, c1.w);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cs[i] = make_float2(1.f, 0.f);
+    }
+  }
+  float rr[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    rr[i] = kind == 2 ? vv[i] : (ml < 64 ? vv[i] * cs[i].x - pp[i] * cs[i].y : vv[i] * cs[i].x + pp[i] * cs[i].y);
+  if (e.kv_q8) {  // GE_QKV into an 8-bit cache: s = max|x| / 127 over the row's 128 columns (this warp)
+    if (kind == 0) {
+      if (ok) st_halfx4(reinterpret_cast<__half*>(e.out) + ((size_t)n * e.nq + h) * 128 + ml, rr[0], rr[1], rr[2], rr[3]);
+      return;
+    }
+    float a = fmaxf(fmaxf(fabsf(rr[0]), fabsf(rr[1])), fmaxf(fabsf(rr[2]), fabsf(rr[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const float sc = __fdiv_rn(a, 127.0f);
+    uint32_t word = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float q = sc > 0.f ? fminf(fmaxf(rintf(__fdiv_rn(rr[i], sc)), -127.f), 127.f) : 0.f;
+      word |= (uint32_t)((int)q + 128) << (8 * i);
+    }
+    if (!ok || pos < 0) return;
+    if (pos >= e.capacity) {
+      set_status(status, DFLASH_STATUS_CAPACITY);
+      return;
+    }
+    const size_t row = (size_t)b * (e.seq_stride >> 7) + (size_t)h * (e.head_stride >> 7) + (size_t)pos;
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(kind == 1 ? e.kc : e.vc) + row * 128 + ml) = word;
+    if (ml == 0) (kind == 1 ? e.ks : e.vs)[row] = sc;
+    return;
+  }
+  if (!ok || pos < 0) return;
+  if (kind == 0) {
+    st_bf16x4(reinterpret_cast<bf16*>(e.out) + ((size_t)n * e.nq + h) * 128 + ml, rr[0], rr[1], rr[2], rr[3]);
+    return;
+  }
+  if (pos >= e.capacity) {
+    set_status(status, DFLASH_STATUS_CAPACITY);
+    return;
+  }
+  bf16* dst = reinterpret_cast<bf16*>(kind == 1 ? e.kc : e.vc);
+  st_bf16x4(dst + (size_t)layer * e.layer_stride + (size_t)b * e.seq_stride + (size_t)h * e.head_stride + (size_t)pos * 128 +
+                ml,
+            rr[0], rr[1], rr[2], rr[3]);
+}
+
 // Final value y of output (n, m): apply the epilogue.  `partner` is y[n][m^1]
 // (SwiGLU) or y[n][m^64] within the head (RoPE).
 __device__ __forceinline__ void gemm_epi(const GemmEpi& e, int n, int m, float v, float partner, int* status) {
@@ -513,17 +677,18 @@ __global__ void __launch_bounds__(128)
   }
   tc_fence_before();
   cluster_sync();  // every partial of the tile is in shared memory
-  // This CTA's rows n = r + j S summed over the splits: warp w takes rows j = w, w + 4, ..., each lane
-  // four columns; the sums go to the dead ring past the partial tile.  (S = 1: the tile is the sum.)
-  const float* sums = red;
-  if (S > 1) {
+  if (epi_vec4_ok(epi)) {
+    // This CTA's rows n = r + j S, warp w taking rows j = w, w + 4, ...: each lane sums four columns
+    // over the splits (split order) and applies the epilogue to them straight away.
     const uint32_t red_local = smem_u32(red);
-    float* sbuf = reinterpret_cast<float*>(smem + C::RED_BYTES);  // [row j][128]
     const int J = rows > r ? (rows - r + S - 1) / S : 0;
+    const bool ok = !flags[0];
     for (int j = warp; j < J; j += 4) {
-      const uint32_t off = (uint32_t)(((r + j * S) * C::BM + lane * 4) * 4);
+      const int n = r + j * S;
+      const uint32_t off = (uint32_t)((n * C::BM + lane * 4) * 4);
       float4 a;
       switch (S) {  // the split counts the policy produces
+        case 1: a = *reinterpret_cast<const float4*>(red + n * C::BM + lane * 4); break;
         case 2: a = sum_splits4<2>(red_local, off); break;
         case 4: a = sum_splits4<4>(red_local, off); break;
         case 8: a = sum_splits4<8>(red_local, off); break;
@@ -537,57 +702,90 @@ __global__ void __launch_bounds__(128)
             a.w += p.w;
           }
       }
-      reinterpret_cast<float4*>(sbuf)[j * 32 + lane] = a;
-    }
-    __syncthreads();
-    sums = sbuf;
-  }
-  // this CTA has read the other partials: its own may be released once every CTA has said so, which
-  // the epilogue's stores overlap
-  cluster_arrive();
-  for (int n = r; n < rows; n += S) {
-    const int j = (n - r) / S;
-    float acc = sums[j * C::BM + ml], pacc = rope ? sums[j * C::BM + (ml ^ 64)] : 0.f;
-    if (epi.in_ssq) {
-      acc *= rsc[n];
-      pacc *= rsc[n];
-    }
-    const bool ok = !flags[0];
-    if (epi.kv_q8) {  // GE_QKV into an 8-bit cache
-      int pos;
-      float2 cs;
-      if (pf) {
-        const int j = (n - r) / S;
-        pos = pre_pos[j];
-        cs = pre_cs[j * 64 + (ml & 63)];
-      } else {
-        const int b = n / epi.rows_per_seq, jj = n % epi.rows_per_seq;
-        pos = epi.len[b] + jj;
-        const int rpos = epi.rope_off ? epi.len[b] + epi.rope_off[n] : pos;
-        cs = (rpos >= 0 && rpos < epi.capacity) ? epi.rope[(size_t)rpos * 64 + (ml & 63)] : make_float2(1.f, 0.f);
+      if (epi.in_ssq) {
+        const float sc = rsc[n];
+        a = make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
       }
-      qkv_q8_out(epi, n, m0 + ml, acc, pacc, pos, cs, ok, red_q8, status);
-      continue;
+      gemm_epi4(epi, n, m0 + lane * 4, a, ok, lane, pf, j, pre_x, pre_cs, pre_pos, status);
     }
-    if (pf) {  // operands already in shared memory
+    cluster_arrive();  // this CTA has read the other partials
+  } else {
+    // This CTA's rows n = r + j S summed over the splits: warp w takes rows j = w, w + 4, ..., each lane
+    // four columns; the sums go to the dead ring past the partial tile.  (S = 1: the tile is the sum.)
+    const float* sums = red;
+    if (S > 1) {
+      const uint32_t red_local = smem_u32(red);
+      float* sbuf = reinterpret_cast<float*>(smem + C::RED_BYTES);  // [row j][128]
+      const int J = rows > r ? (rows - r + S - 1) / S : 0;
+      for (int j = warp; j < J; j += 4) {
+        const uint32_t off = (uint32_t)(((r + j * S) * C::BM + lane * 4) * 4);
+        float4 a;
+        switch (S) {  // the split counts the policy produces
+          case 2: a = sum_splits4<2>(red_local, off); break;
+          case 4: a = sum_splits4<4>(red_local, off); break;
+          case 8: a = sum_splits4<8>(red_local, off); break;
+          default:
+            a = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int cc = 0; cc < S; ++cc) {
+              const float4 p = ld_dsmem4(dsmem_addr(red_local, (uint32_t)cc) + off);
+              a.x += p.x;
+              a.y += p.y;
+              a.z += p.z;
+              a.w += p.w;
+            }
+        }
+        reinterpret_cast<float4*>(sbuf)[j * 32 + lane] = a;
+      }
+      __syncthreads();
+      sums = sbuf;
+    }
+    // this CTA has read the other partials: its own may be released once every CTA has said so, which
+    // the epilogue's stores overlap
+    cluster_arrive();
+    for (int n = r; n < rows; n += S) {
       const int j = (n - r) / S;
-      if (epi.kind == GE_RESID) {
-        const float x = pre_x[j * 128 + ml] + acc;
-        if (ok) resid_store(epi, n, m0 + ml, x);
-        if (epi.norm_out) norm_handover(epi, n, m0 + ml, x, ok, lane);
-      } else if (ok && pre_pos[j] >= 0) {
-        gemm_epi_rope(epi, n, m0 + ml, acc, pacc, pre_pos[j], pre_cs[j * 64 + (ml & 63)], status);
+      float acc = sums[j * C::BM + ml], pacc = rope ? sums[j * C::BM + (ml ^ 64)] : 0.f;
+      if (epi.in_ssq) {
+        acc *= rsc[n];
+        pacc *= rsc[n];
       }
-      continue;
+      const bool ok = !flags[0];
+      if (epi.kv_q8) {  // GE_QKV into an 8-bit cache
+        int pos;
+        float2 cs;
+        if (pf) {
+          const int j = (n - r) / S;
+          pos = pre_pos[j];
+          cs = pre_cs[j * 64 + (ml & 63)];
+        } else {
+          const int b = n / epi.rows_per_seq, jj = n % epi.rows_per_seq;
+          pos = epi.len[b] + jj;
+          const int rpos = epi.rope_off ? epi.len[b] + epi.rope_off[n] : pos;
+          cs = (rpos >= 0 && rpos < epi.capacity) ? epi.rope[(size_t)rpos * 64 + (ml & 63)] : make_float2(1.f, 0.f);
+        }
+        qkv_q8_out(epi, n, m0 + ml, acc, pacc, pos, cs, ok, red_q8, status);
+        continue;
+      }
+      if (pf) {  // operands already in shared memory
+        const int j = (n - r) / S;
+        if (epi.kind == GE_RESID) {
+          const float x = pre_x[j * 128 + ml] + acc;
+          if (ok) resid_store(epi, n, m0 + ml, x);
+          if (epi.norm_out) norm_handover(epi, n, m0 + ml, x, ok, lane);
+        } else if (ok && pre_pos[j] >= 0) {
+          gemm_epi_rope(epi, n, m0 + ml, acc, pacc, pre_pos[j], pre_cs[j * 64 + (ml & 63)], status);
+        }
+        continue;
+      }
+      if (epi.kind == GE_RESID && epi.norm_out) {
+        const float x = reinterpret_cast<const float*>(epi.out)[(size_t)n * epi.ldo + m0 + ml] + acc;
+        if (ok) resid_store(epi, n, m0 + ml, x);
+        norm_handover(epi, n, m0 + ml, x, ok, lane);
+        continue;
+      }
+      const float partner = rope ? pacc : __shfl_xor_sync(0xffffffffu, acc, 1);
+      if (ok) gemm_epi(epi, n, m0 + ml, acc, partner, status);
     }
-    if (epi.kind == GE_RESID && epi.norm_out) {
-      const float x = reinterpret_cast<const float*>(epi.out)[(size_t)n * epi.ldo + m0 + ml] + acc;
-      if (ok) resid_store(epi, n, m0 + ml, x);
-      norm_handover(epi, n, m0 + ml, x, ok, lane);
-      continue;
-    }
-    const float partner = rope ? pacc : __shfl_xor_sync(0xffffffffu, acc, 1);
-    if (ok) gemm_epi(epi, n, m0 + ml, acc, partner, status);
   }
   cluster_wait();  // no CTA leaves while its partial may still be read
   if (warp == 2) {
