@@ -117,6 +117,34 @@ __device__ __forceinline__ float4 sum_splits4(uint32_t red_local, uint32_t off) 
   return a;
 }
 
+// This CTA's rows n = r + j S of the split tile, warp w taking j = w, w + 4,
+// ...: lane l sums columns 4l .. 4l + 3 of each over the SS partials (split
+// order) and hands them to fn(j, n, sums).  The next row's loads are issued
+// before fn runs on the current one, so a warp with several rows keeps one
+// row's remote requests in flight behind its epilogue.
+template <int SS, int BM, typename F>
+__device__ __forceinline__ void split_rows4(uint32_t red_local, int r, int J, int warp, int lane, F&& fn) {
+  float4 p[SS];
+  auto issue = [&](int j) {
+    const uint32_t off = (uint32_t)(((r + j * SS) * BM + lane * 4) * 4);
+#pragma unroll
+    for (int cc = 0; cc < SS; ++cc) p[cc] = ld_dsmem4(dsmem_addr(red_local, (uint32_t)cc) + off);
+  };
+  if (warp < J) issue(warp);
+  for (int j = warp; j < J; j += 4) {
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int cc = 0; cc < SS; ++cc) {
+      a.x += p[cc].x;
+      a.y += p[cc].y;
+      a.z += p[cc].z;
+      a.w += p[cc].w;
+    }
+    if (j + 4 < J) issue(j + 4);
+    fn(j, r + j * SS, a);
+  }
+}
+
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 // The new residual x of output (n, m): stored, with its captured bf16 copies.
@@ -683,30 +711,35 @@ __global__ void __launch_bounds__(128)
     const uint32_t red_local = smem_u32(red);
     const int J = rows > r ? (rows - r + S - 1) / S : 0;
     const bool ok = !flags[0];
-    for (int j = warp; j < J; j += 4) {
-      const int n = r + j * S;
-      const uint32_t off = (uint32_t)((n * C::BM + lane * 4) * 4);
-      float4 a;
-      switch (S) {  // the split counts the policy produces
-        case 1: a = *reinterpret_cast<const float4*>(red + n * C::BM + lane * 4); break;
-        case 2: a = sum_splits4<2>(red_local, off); break;
-        case 4: a = sum_splits4<4>(red_local, off); break;
-        case 8: a = sum_splits4<8>(red_local, off); break;
-        default:
-          a = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int cc = 0; cc < S; ++cc) {
-            const float4 p = ld_dsmem4(dsmem_addr(red_local, (uint32_t)cc) + off);
-            a.x += p.x;
-            a.y += p.y;
-            a.z += p.z;
-            a.w += p.w;
-          }
-      }
+    auto row_epi = [&](int j, int n, float4 a) {
       if (epi.in_ssq) {
         const float sc = rsc[n];
         a = make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
       }
       gemm_epi4(epi, n, m0 + lane * 4, a, ok, lane, pf, j, pre_x, pre_cs, pre_pos, status);
+    };
+    switch (S) {  // the split counts the policy produces
+      case 2: split_rows4<2, C::BM>(red_local, r, J, warp, lane, row_epi); break;
+      case 4: split_rows4<4, C::BM>(red_local, r, J, warp, lane, row_epi); break;
+      case 8: split_rows4<8, C::BM>(red_local, r, J, warp, lane, row_epi); break;
+      default:
+        for (int j = warp; j < J; j += 4) {
+          const int n = r + j * S;
+          float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (S == 1) {
+            a = *reinterpret_cast<const float4*>(red + n * C::BM + lane * 4);
+          } else {
+            const uint32_t off = (uint32_t)((n * C::BM + lane * 4) * 4);
+            for (int cc = 0; cc < S; ++cc) {
+              const float4 p = ld_dsmem4(dsmem_addr(red_local, (uint32_t)cc) + off);
+              a.x += p.x;
+              a.y += p.y;
+              a.z += p.z;
+              a.w += p.w;
+            }
+          }
+          row_epi(j, n, a);
+        }
     }
     cluster_arrive();  // this CTA has read the other partials
   } else {
