@@ -68,6 +68,29 @@ def test_linear_bf16_deterministic_and_row_invariant(ws):
     assert np.array_equal(outs[16], outs[128][:16])
 
 
+@pytest.mark.parametrize("M,K", [(1024, 4096), (24576, 512)])
+@pytest.mark.parametrize("rows", [5, 16, 128])
+def test_linear_bf16_unaligned_output_equals_aligned(ws, M, K, rows):
+    """An output that is not 16-byte aligned (a valid float array one element
+    into a buffer) takes the per-column epilogue, split (M = 1024) or not
+    (M = 24576); it holds the same values, bit for bit, as the aligned
+    output's four-column or staged path."""
+    x = synth.to_bf16_f32(synth.gaussian((rows, K), seed=16, stream=rows))
+    w = synth.to_bf16_f32(synth.gaussian((M, K), seed=17, stream=M, scale=0.02))
+    xd, wd = to_dev(x, "bf16"), to_dev(w, "bf16")
+    y = torch.empty(rows, M, dtype=torch.float32, device=dev())
+    buf = torch.zeros(rows * M + 4, dtype=torch.float32, device=dev())
+    yu = buf[1:1 + rows * M].view(rows, M)
+    assert y.data_ptr() % 16 == 0 and yu.data_ptr() % 16 == 4
+    capi.dflash_linear(capi.BF16, xd, wd, y, rows, M, K, ws)
+    capi.dflash_linear(capi.BF16, xd, wd, yu, rows, M, K, ws)
+    assert capi.dflash_status(ws) == 0
+    assert np.array_equal(y.cpu().numpy(), yu.cpu().numpy())
+    assert float(buf[0]) == 0.0 and float(buf[-3]) == 0.0  # nothing written outside the view
+    ref = O.linear(x, w)
+    assert_close(to_np(y), ref, "bf16", f"linear bf16 {rows}x{M}x{K}", tol=1e-4 * max(1.0, np.abs(ref).max()))
+
+
 # ---------------------------------------------------------------- rmsnorm
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
