@@ -146,6 +146,39 @@ __global__ void __launch_bounds__(256) embed_kernel(const T* __restrict__ E, int
   }
   const T* er = E + (size_t)tok * H;
   float* xr = x + (size_t)r * H;
+  if constexpr (sizeof(T) == 2) {
+    // eight entries per thread and pass: 16-byte loads of the row and the gains, 16-byte stores; the
+    // sums of squares of each 32 columns over the four lanes that hold them
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    if (xg && (H & 255) == 0 && al16(er) && al16(xr) && al16(g) && al16(xg + (size_t)r * H)) {  // uniform
+      for (int c = threadIdx.x; c < (H >> 3); c += blockDim.x) {
+        const uint4 ew = reinterpret_cast<const uint4*>(er)[c];
+        const uint4 gw = reinterpret_cast<const uint4*>(g)[c];
+        const uint32_t e4[4] = {ew.x, ew.y, ew.z, ew.w}, g4[4] = {gw.x, gw.y, gw.z, gw.w};
+        float v[8];
+        uint32_t o4[4];
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 ev = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&e4[k]));
+          const float2 gv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g4[k]));
+          v[2 * k] = ev.x;
+          v[2 * k + 1] = ev.y;
+          const __nv_bfloat162 pr = __floats2bfloat162_rn(ev.x * gv.x, ev.y * gv.y);
+          o4[k] = *reinterpret_cast<const uint32_t*>(&pr);
+          t += ev.x * ev.x;
+          t += ev.y * ev.y;
+        }
+        reinterpret_cast<float4*>(xr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4*>(xr)[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
+        reinterpret_cast<uint4*>(xg + (size_t)r * H)[c] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        t += __shfl_xor_sync(0xffffffffu, t, 1);
+        t += __shfl_xor_sync(0xffffffffu, t, 2);
+        if ((threadIdx.x & 3) == 0) ssq[(size_t)r * (H >> 5) + (c >> 2)] = t;
+      }
+      return;
+    }
+  }
   for (int i = threadIdx.x; i < H; i += blockDim.x) {
     const float v = to_f<T>(er[i]);
     xr[i] = v;
