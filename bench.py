@@ -591,22 +591,22 @@ def measure_ours(wl: synth.Workload, args, dist: Dist) -> dict:
         "stage_gbs": {k: (stage_by[k] / (stage_med[k] / 1e3) / 1e9 if stage_by[k] and stage_med[k] > 0 else None)
                       for k in stage_med},
         "ar_tokens_per_s": ar_tok_s,
-        "roofline": {"bound": "hbm", "kernel": "gemm_cl_kernel", "achieved": gemm_gbs, "peak": peak,
-                     "unit": "GB/s", "frac": (gemm_gbs / peak) if gemm_gbs else None,
+        "roofline": {"bound": "hbm", "kernel": "gemm_cl_kernel", "achieved": gemm_graph["gbs"], "peak": peak,
+                     "unit": "GB/s", "frac": gemm_graph["gbs"] / peak,
                      "traffic": GEMM_TRAFFIC["bytes_per_launch"] if wl.name == GEMM_TRAFFIC["workload"] else None,
-                     "algorithmic_bytes_per_launch": gemm_bytes / len(chains) if chains else None,
-                     "peak_kind": peak_kind, "timing": "eager",
+                     "algorithmic_bytes_per_launch": gemm_graph["bytes"] / gemm_graph["launches"],
+                     "peak_kind": peak_kind, "timing": "graph",
+                     "achieved_eager": gemm_gbs, "frac_eager": (gemm_gbs / peak) if gemm_gbs else None,
                      "frac_in_graph_lower_bound": gemm_bytes_step / (ms_step / 1e3) / 1e9 / peak,
-                     "achieved_graph": gemm_graph["gbs"], "frac_graph": gemm_graph["gbs"] / peak,
-                     "graph_note": f"the step's {gemm_graph['launches']} weight products alone, back to back in "
-                                   f"one CUDA graph (float-store epilogue, the model's weights): "
-                                   f"{gemm_graph['bytes'] / 1e9:.2f} GB in {gemm_graph['ms']:.3f} ms per replay",
-                     "note": f"{len(chains)} weight-product launches over {PS} eager steps (events around each "
-                             f"launch, so no overlap with its neighbours: an upper bound on the kernel's time in the "
-                             f"graph); achieved = weight bytes of the launches / their summed CUDA-event durations; "
-                             f"frac_in_graph_lower_bound = the products' bytes per step / the whole graph-timed step; "
-                             f"traffic = ncu DRAM read+write bytes per launch (null until recaptured for this "
-                             f"kernel)"},
+                     "note": f"achieved = weight bytes per launch / the average launch duration of the step's "
+                             f"{gemm_graph['launches']} weight products replayed back to back in one CUDA graph "
+                             f"(CUDA events around the replay on its stream; the model's weights, a float-store "
+                             f"epilogue): {gemm_graph['bytes'] / 1e9:.2f} GB in {gemm_graph['ms']:.3f} ms per "
+                             f"replay. achieved_eager = the same bytes over {len(chains)} launches timed one by one "
+                             f"with events around each in {PS} eager steps (no overlap with the neighbours: an upper "
+                             f"bound on the kernel's time in the graph). frac_in_graph_lower_bound = the products' "
+                             f"bytes per step / the whole graph-timed step. traffic = ncu DRAM read+write bytes per "
+                             f"launch over the step's product shapes (null for other workloads)"},
         "clocks": clk,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(kernels_per_step * K),
