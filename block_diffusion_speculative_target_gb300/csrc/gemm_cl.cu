@@ -313,8 +313,11 @@ __device__ __forceinline__ void gemm_epi4(const GemmEpi& e, int n, int m, float4
       }
       return;
     }
-    default:
+    case GE_QKV:
+    case GE_INJECT:
       break;
+    default:
+      return;
   }
   // GE_QKV / GE_INJECT: the head's 128 columns are this row's 32 lanes
   float pp[4];
