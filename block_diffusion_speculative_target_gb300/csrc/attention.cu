@@ -97,14 +97,14 @@ __global__ void __launch_bounds__(NT)
 // a row with few groups needs one trip to memory.  The denominator's per-lane
 // terms are added over a fixed butterfly.  The result depends only on the
 // row's own groups.  The kernel holds no shared memory and at most 80
-// registers a thread, so one 4-warp block fits beside an attention CTA and
-// waits there for it to finish.
+// registers a thread in 2-warp blocks (one (row, head) pair each), small
+// enough to wait beside an attention CTA for it to finish.
 constexpr int kCombineMaxChunks = 1024;
-constexpr int kCombineWarps = 4;
+constexpr int kCombineWarps = 2;
 constexpr int kCombineBatch = 16;  // partial rows in flight per lane
 
 template <typename T>
-__global__ void __launch_bounds__(kCombineWarps * 32, 6)
+__global__ void __launch_bounds__(kCombineWarps * 32, 12)
     attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int rows, int n, int nq,
                         int hd, int causal, int capacity, int window, int gk, const int32_t* __restrict__ len,
                         int nchunk, int swz_g, T* __restrict__ out) {
